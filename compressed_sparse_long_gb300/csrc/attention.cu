@@ -1,0 +1,302 @@
+// Shared-K=V attention over the selected (c4a) or all visible (c128a) compressed entries
+// plus the sliding window, with inverse RoPE on the output (steps a8, a9).
+//
+// [notes] "DeepSeek V4 in vLLM 技术博客详尽笔记", Inverse RoPE 的数学原理:
+//   out = (sum_x softmax_x(q~ . key_x) key_x) R^-1(theta_p),
+// one stored vector per entry serving as key and value (共享 Key-Value 向量), and
+// [blog] 短滑動窗口 for the 128 uncompressed local tokens.
+//
+// Key list of a query at p: positions [0, n_ent) are compressed entries (top-k list slots,
+// -1 slots masked; or entries 0..n_vis-1 when dense), positions [n_ent, n_ent + n_swa) the
+// window tokens max(0, p-swa+1) .. p. Split s of a query handles keys
+// [s*keys_per_split, (s+1)*keys_per_split); splits > 1 write (m, l, o) partials that
+// attn_merge combines.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace v4a {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kChunk = 32;        // keys per shared-memory chunk
+constexpr int kThreads = 256;     // 8 warps
+
+struct KeyRef {
+  int64_t slot;                   // pool row, or < 0 when masked
+  bool is_swa;
+};
+
+// Resolve key x of query (seq, p): entry or window token, its pool row, visibility.
+__device__ __forceinline__ KeyRef key_ref(const AttnParams& p, int qi, int seq, int64_t pos,
+                                          int64_t n_ent, int64_t n_vis, int64_t t0, int64_t x) {
+  KeyRef r{-1, false};
+  if (x < n_ent) {
+    int64_t j = p.topk ? (int64_t)__ldg(p.topk + (int64_t)qi * p.k + x) : x;
+    if (j < 0) return r;                         // padding slot of the top-k list
+    if (j >= n_vis) { raise_err(p.err, V4A_DEV_BAD_INDEX); return r; }
+    int64_t s = slot_of(p.attn, seq, j);
+    if (!slot_ok(s, p.err)) return r;
+    r.slot = s;
+  } else {
+    int64_t t = t0 + (x - n_ent);
+    int64_t s = slot_of(p.swa, seq, t);
+    if (!slot_ok(s, p.err)) return r;
+    r.slot = s;
+    r.is_swa = true;
+  }
+  return r;
+}
+
+// CUDA-core kernel: fp32 queries in shared memory, keys dequantised into a padded chunk.
+// Warp w owns heads w*HPW .. w*HPW+HPW-1; lane l owns dims l, l+32, ... of every head.
+template <typename QT, bool kFp8, typename OT, int H, int D>
+__global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ AttnParams p) {
+  constexpr int HPW = H / 8;
+  constexpr int DPL = D / 32;
+  constexpr int KS = D + 1;                      // padded key row (conflict-free columns)
+  extern __shared__ float smem[];
+  float* qs = smem;                              // [H][D]
+  float* kb = smem + H * D;                      // [kChunk][KS]
+  __shared__ int64_t kslot[kChunk];
+  __shared__ int kswa[kChunk];
+  __shared__ float csn[kMaxRopePairs][2];
+
+  const int qi = blockIdx.y, split = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq = __ldg(p.q_seq + qi);
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int64_t n_vis = visible_entries(pos, p.S, p.W, p.win_off);
+  const int64_t n_ent = p.topk ? p.k : n_vis;
+  const int64_t t0 = pos - p.swa_len + 1 > 0 ? pos - p.swa_len + 1 : 0;
+  const int64_t n_keys = n_ent + (pos - t0 + 1);
+  if (split == 0 && tid == 0 && n_keys > (int64_t)p.n_split * p.keys_per_split)
+    raise_err(p.err, V4A_DEV_BAD_POS);
+  const int64_t x_begin = (int64_t)split * p.keys_per_split;
+  const int64_t x_end = min(n_keys, x_begin + p.keys_per_split);
+
+  // RoPE(q, p) * scale * log2(e) into shared memory
+  const int n_pairs = p.rope.d_r / 2;
+  for (int i = tid; i < n_pairs; i += kThreads) {
+    float c, s;
+    rope_cs(p.rope, pos, i, c, s);
+    csn[i][0] = c;
+    csn[i][1] = s;
+  }
+  __syncthreads();
+  const QT* q = reinterpret_cast<const QT*>(p.q) + (int64_t)qi * H * D;
+  const float qscale = p.scale * kLog2e;
+  const int tail0 = D - p.rope.d_r;
+  for (int e = tid * 2; e < H * D; e += kThreads * 2) {
+    const int d = e % D;
+    float a = Elem<QT>::to_f(q[e]), b = Elem<QT>::to_f(q[e + 1]);
+    if (d >= tail0) {
+      const int i = (d - tail0) >> 1;
+      const float c = csn[i][0], s = csn[i][1];
+      const float ra = a * c - b * s, rb = a * s + b * c;
+      a = ra;
+      b = rb;
+    }
+    qs[e] = a * qscale;
+    qs[e + 1] = b * qscale;
+  }
+
+  float o[HPW][DPL];
+  float m[HPW], l[HPW];
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    m[hh] = -INFINITY;
+    l[hh] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[hh][i] = 0.f;
+  }
+
+  for (int64_t c0 = x_begin; c0 < x_end; c0 += kChunk) {
+    const int n_here = (int)min((int64_t)kChunk, x_end - c0);
+    __syncthreads();
+    if (tid < kChunk) {
+      KeyRef r{-1, false};
+      if (tid < n_here) r = key_ref(p, qi, seq, pos, n_ent, n_vis, t0, c0 + tid);
+      kslot[tid] = r.slot;
+      kswa[tid] = r.is_swa;
+    }
+    __syncthreads();
+    // dequantise the chunk: 8 threads per row, 16-byte segments
+    for (int task = tid; task < kChunk * (D / 16); task += kThreads) {
+      const int row = task / (D / 16), seg = task % (D / 16);
+      float* dst = kb + row * KS + seg * 16;
+      const int64_t s = kslot[row];
+      if (s < 0) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) dst[k] = 0.f;
+        continue;
+      }
+      const CacheView& cv = kswa[row] ? p.swa : p.attn;
+      if constexpr (kFp8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint8_t*>(cv.data) + s * (int64_t)cv.width + seg * 16));
+        const float sc = __ldg(cv.scale + s);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[4];
+          e4m3x4_decode(w4[v], f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[4 * v + k] = f[k] * sc;
+        }
+      } else {
+        const float* src = reinterpret_cast<const float*>(cv.data) + s * (int64_t)cv.width + seg * 16;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(src) + v);
+          dst[4 * v] = f.x; dst[4 * v + 1] = f.y; dst[4 * v + 2] = f.z; dst[4 * v + 3] = f.w;
+        }
+      }
+    }
+    __syncthreads();
+
+    // logits: lane = key of the chunk
+    float lg[HPW];
+#pragma unroll
+    for (int hh = 0; hh < HPW; ++hh) lg[hh] = 0.f;
+    const float* krow = kb + lane * KS;
+    for (int d = 0; d < D; ++d) {
+      const float kv = krow[d];
+#pragma unroll
+      for (int hh = 0; hh < HPW; ++hh) lg[hh] = fmaf(qs[(warp * HPW + hh) * D + d], kv, lg[hh]);
+    }
+    const bool valid = lane < n_here && kslot[lane] >= 0;
+#pragma unroll
+    for (int hh = 0; hh < HPW; ++hh) {
+      const float x = valid ? lg[hh] : -INFINITY;
+      const float cm = warp_max(x);
+      const float mn = fmaxf(m[hh], cm);
+      const float corr = mn == -INFINITY ? 1.f : exp2f(m[hh] - mn);
+      const float pr = valid ? exp2f(x - mn) : 0.f;
+      l[hh] = l[hh] * corr + warp_sum(pr);
+      m[hh] = mn;
+      lg[hh] = pr;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) o[hh][i] *= corr;
+    }
+    for (int x = 0; x < n_here; ++x) {
+      const float* kr = kb + x * KS;
+      float kv[DPL];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) kv[i] = kr[lane + 32 * i];
+#pragma unroll
+      for (int hh = 0; hh < HPW; ++hh) {
+        const float px = __shfl_sync(0xffffffffu, lg[hh], x);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[hh][i] = fmaf(px, kv[i], o[hh][i]);
+      }
+    }
+  }
+
+  if (p.n_split > 1) {
+    const int64_t base = ((int64_t)qi * p.n_split + split) * H;
+#pragma unroll
+    for (int hh = 0; hh < HPW; ++hh) {
+      const int h = warp * HPW + hh;
+      float* po = p.part_o + (base + h) * D;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) po[lane + 32 * i] = o[hh][i];
+      if (lane == 0) {
+        p.part_ml[(base + h) * 2] = m[hh];
+        p.part_ml[(base + h) * 2 + 1] = l[hh];
+      }
+    }
+    return;
+  }
+  // single split: normalise, inverse RoPE at p, store
+  OT* out = reinterpret_cast<OT*>(p.out) + (int64_t)qi * H * D;
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int h = warp * HPW + hh;
+    const float inv = l[hh] > 0.f ? 1.f / l[hh] : 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      float v = o[hh][i] * inv;
+      const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+      if (d >= tail0) {
+        const int pi = (d - tail0) >> 1;
+        const float c = csn[pi][0], s = csn[pi][1];
+        // inverse rotation: (a, b) -> (a c + b s, -a s + b c)
+        v = (d & 1) ? (-partner * s + v * c) : (v * c + partner * s);
+      }
+      out[(int64_t)h * D + d] = Elem<OT>::from_f(v);
+    }
+  }
+}
+
+// Combine split partials, normalise, inverse RoPE, store. One CTA per query; thread
+// items are (head, rotation pair).
+template <typename OT>
+__global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
+  const int qi = blockIdx.x;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int H = p.H, D = p.D, tail0 = D - p.rope.d_r;
+  OT* out = reinterpret_cast<OT*>(p.out) + (int64_t)qi * H * D;
+  for (int item = threadIdx.x; item < H * D / 2; item += blockDim.x) {
+    const int h = item / (D / 2), d = 2 * (item % (D / 2));
+    float mx = -INFINITY;
+    for (int s = 0; s < p.n_split; ++s)
+      mx = fmaxf(mx, p.part_ml[(((int64_t)qi * p.n_split + s) * H + h) * 2]);
+    float L = 0.f, a = 0.f, b = 0.f;
+    if (mx != -INFINITY) {
+      for (int s = 0; s < p.n_split; ++s) {
+        const int64_t base = ((int64_t)qi * p.n_split + s) * H + h;
+        const float ms = p.part_ml[base * 2];
+        if (ms == -INFINITY) continue;
+        const float wgt = exp2f(ms - mx);
+        L += p.part_ml[base * 2 + 1] * wgt;
+        a += p.part_o[base * D + d] * wgt;
+        b += p.part_o[base * D + d + 1] * wgt;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    a *= inv;
+    b *= inv;
+    if (d >= tail0) {
+      float c, s;
+      rope_cs(p.rope, pos, (d - tail0) >> 1, c, s);
+      const float ra = a * c + b * s, rb = -a * s + b * c;
+      a = ra;
+      b = rb;
+    }
+    out[(int64_t)h * D + d] = Elem<OT>::from_f(a);
+    out[(int64_t)h * D + d + 1] = Elem<OT>::from_f(b);
+  }
+}
+
+template <typename QT, bool kFp8, typename OT, int H, int D>
+cudaError_t launch_simt(const AttnParams& p, cudaStream_t st) {
+  const size_t smem = (size_t)(H * D + kChunk * (D + 1)) * sizeof(float);
+  cudaFuncSetAttribute(attn_simt<QT, kFp8, OT, H, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  dim3 grid((unsigned)p.n_split, (unsigned)p.n_q);
+  attn_simt<QT, kFp8, OT, H, D><<<grid, kThreads, smem, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_split == 1) return e;
+  attn_merge<OT><<<p.n_q, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
+  if (p.n_q == 0) return V4A_OK;
+  cudaError_t e;
+  if (dtype == V4A_BF16_FP8 && p.H == 64 && p.D == 512)
+    e = launch_simt<__nv_bfloat16, true, __nv_bfloat16, 64, 512>(p, st);
+  else if (dtype == V4A_FP32 && p.H == 8 && p.D == 128)
+    e = launch_simt<float, false, float, 8, 128>(p, st);
+  else if (dtype == V4A_FP32 && p.H == 64 && p.D == 512)
+    e = launch_simt<float, false, float, 64, 512>(p, st);
+  else
+    return V4A_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+}  // namespace v4a

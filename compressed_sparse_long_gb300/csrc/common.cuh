@@ -1,0 +1,195 @@
+// Device helpers shared by the v4a kernels: paged-cache views, slot lookup, RoPE angles,
+// fp8 e4m3 <-> fp32/bf16 conversion, warp reductions, the device error word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/v4a.h"
+
+namespace v4a {
+
+constexpr int kBlock = 256;       // native positions per logical block
+constexpr int kMaxRopePairs = 32; // d_r <= 64
+constexpr float kE4m3Max = 448.0f;
+
+// Kernel-parameter copy of a v4a_cache.
+struct CacheView {
+  void* data;
+  float* scale;
+  const int32_t* bt;
+  int64_t n_pages;
+  int32_t max_blocks;
+  int32_t R;
+  int32_t width;
+};
+
+inline CacheView view_of(const v4a_cache* c) {
+  CacheView v{};
+  if (c) {
+    v.data = c->data;
+    v.scale = c->scale;
+    v.bt = c->block_table;
+    v.n_pages = c->n_pages;
+    v.max_blocks = c->max_blocks;
+    v.R = c->rows_per_block;
+    v.width = c->row_width;
+  }
+  return v;
+}
+
+// Pool row of logical row r of sequence seq: page * R + r % R, -1 if the block has no
+// page (or r is out of the table), -2 if the page id is outside the pool.
+__device__ __forceinline__ int64_t slot_of(const CacheView& c, int seq, int64_t r) {
+  if (r < 0) return -1;
+  int64_t blk = r / c.R;
+  if (blk >= c.max_blocks) return -1;
+  int32_t page = __ldg(c.bt + (int64_t)seq * c.max_blocks + blk);
+  if (page < 0) return -1;
+  if (page >= c.n_pages) return -2;
+  return (int64_t)page * c.R + (r % c.R);
+}
+
+__device__ __forceinline__ void raise_err(int32_t* err, uint32_t bits) {
+  if (err) atomicOr(reinterpret_cast<unsigned int*>(err), bits);
+}
+
+// Report a failed slot lookup; returns true when the slot is usable.
+__device__ __forceinline__ bool slot_ok(int64_t s, int32_t* err) {
+  if (s >= 0) return true;
+  raise_err(err, s == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+  return false;
+}
+
+// RoPE frequencies theta_i = base^(-2i/d_r), computed on the host in double.
+struct Rope {
+  int32_t d_r;
+  int32_t D;
+  double theta[kMaxRopePairs];
+};
+
+// cos/sin of pos * theta_i. The angle is formed in double and reduced modulo 2*pi with a
+// two-constant Cody-Waite step (2*pi = hi + lo), so positions up to 2^31 keep ~1e-10 rad;
+// the reduced angle (|r| <= pi) then goes through fp32 sincosf.
+__device__ __forceinline__ void rope_cs(const Rope& rp, int64_t pos, int i, float& c, float& s) {
+  const double two_pi_hi = 6.283185307179586;
+  const double two_pi_lo = 2.4492935982947064e-16;
+  double a = (double)pos * rp.theta[i];
+  double n = rint(a * (1.0 / two_pi_hi));
+  double r = fma(-n, two_pi_hi, a);
+  r = fma(-n, two_pi_lo, r);
+  sincosf((float)r, &s, &c);
+}
+
+// ---------------------------------------------------------------- warp reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------- element access
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Load n contiguous elements (n * sizeof(T) a multiple of 4 bytes) into fp32 registers,
+// using the widest aligned vector the byte count allows.
+template <typename T, int N>
+__device__ __forceinline__ void load_f(const T* __restrict__ p, float (&out)[N]) {
+  constexpr int kBytes = N * (int)sizeof(T);
+  if constexpr (kBytes % 16 == 0) {
+    constexpr int kVec = kBytes / 16;
+    constexpr int kPer = 16 / sizeof(T);
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + v);
+      const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) out[v * kPer + k] = Elem<T>::to_f(e[k]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k) out[k] = Elem<T>::to_f(p[k]);
+  }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_f(T* __restrict__ p, const float (&in)[N]) {
+  constexpr int kBytes = N * (int)sizeof(T);
+  if constexpr (kBytes % 16 == 0) {
+    constexpr int kVec = kBytes / 16;
+    constexpr int kPer = 16 / sizeof(T);
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      uint4 u;
+      T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) e[k] = Elem<T>::from_f(in[v * kPer + k]);
+      reinterpret_cast<uint4*>(p)[v] = u;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k) p[k] = Elem<T>::from_f(in[k]);
+  }
+}
+
+// ---------------------------------------------------------------- fp8 e4m3
+// Encode: round-to-nearest-even, saturating to +-448 (cvt.rn.satfinite.e4m3x2.f32).
+__device__ __forceinline__ uint16_t e4m3x2_encode(float lo, float hi) {
+  __nv_fp8x2_storage_t r = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+  return (uint16_t)r;
+}
+
+// Decode 4 codes (one 32-bit word, code k in byte k) to fp32. e4m3 -> f16 is exact.
+__device__ __forceinline__ void e4m3x4_decode(uint32_t w, float (&f)[4]) {
+  uint32_t h01, h23;
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi; }"
+      : "=r"(h01), "=r"(h23) : "r"(w));
+  __half2 a = *reinterpret_cast<__half2*>(&h01);
+  __half2 b = *reinterpret_cast<__half2*>(&h23);
+  float2 fa = __half22float2(a), fb = __half22float2(b);
+  f[0] = fa.x; f[1] = fa.y; f[2] = fb.x; f[3] = fb.y;
+}
+
+// Decode 2 codes (byte 0 -> low half, byte 1 -> high half) to a bf16x2 word. e4m3 -> bf16
+// is exact: the code's sign and exponent/mantissa bits are placed in a bf16 whose
+// exponent is 120 too small, then scaled by 2^120 with an exact bf16 multiply (subnormal
+// codes land on bf16 subnormals first and become normal after the scaling).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes_in_low16) {
+  // byte k -> bits [16k+8, 16k+15]
+  uint32_t t = __byte_perm(two_codes_in_low16, 0u, 0x1404);  // [c0<<8 | c1<<24]
+  uint32_t mag = (t >> 4) & 0x07F007F0u;
+  uint32_t sgn = t & 0x80008000u;
+  uint32_t bits = mag | sgn;
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));
+  return r;
+}
+
+__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Number of entries visible to a query at p: entry j qualifies iff its last covered
+// position S*j + win_off + W - 1 is < p.
+__host__ __device__ __forceinline__ int64_t visible_entries(int64_t p, int S, int W, int win_off) {
+  int64_t num = p - win_off - W;
+  if (num < 0) return 0;
+  return num / S + 1;
+}
+
+}  // namespace v4a

@@ -1,0 +1,257 @@
+// DSA-style indexer scores and top-k selection of c4a entries (steps a6, a7).
+//
+// [blog] "vLLM DeepSeek V4 支援：高效長上下文注意力", DeepSeek Sparse Attention bullet: after
+// compression a query still only attends to its top-k compressed tokens; [notes] 压缩参数细节
+// (C4A top-k = 512) and 因果性条件 (only entries covering positions < p are candidates).
+//
+//   score_j = sum_h w_h * max(0, q_h . k_j),  k_j = e4m3 code * row scale (fp8 layers)
+//
+// The per-row scale is applied after the head sum: ReLU is positively homogeneous and the
+// scale is positive, so sum_h w_h ReLU(q_h . (c*k)) = c * sum_h w_h ReLU(q_h . k).
+//
+// Top-k: MSB-first radix select on the order-preserving uint32 image of the fp32 scores
+// (4 passes of 8-bit digits, warp-aggregated shared-memory histograms) finds the k-th
+// largest key; an ordered block compaction then emits every entry above it plus the
+// lowest-index entries equal to it, in ascending index order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace v4a {
+
+namespace {
+
+// ------------------------------------------------------------------ fp32 indexer scores
+// One thread per entry, the query's heads in shared memory (broadcast reads).
+template <typename T, bool kFp8, int HI, int DI>
+__global__ void __launch_bounds__(128) index_scores_simt(const __grid_constant__ IndexParams p) {
+  __shared__ float qs[HI * DI];
+  __shared__ float ws[HI];
+  const int qi = blockIdx.y;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  int64_t n_vis = visible_entries(pos, p.S, p.W, p.win_off);
+  if (n_vis > p.row_stride) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) raise_err(p.err, V4A_DEV_BAD_POS);
+    n_vis = p.row_stride;
+  }
+  if ((int64_t)blockIdx.x * 128 >= n_vis) return;
+  const T* q = reinterpret_cast<const T*>(p.q_idx) + (int64_t)qi * HI * DI;
+  for (int i = threadIdx.x; i < HI * DI; i += 128) qs[i] = Elem<T>::to_f(q[i]);
+  for (int i = threadIdx.x; i < HI; i += 128) ws[i] = __ldg(p.w + (int64_t)qi * HI + i);
+  __syncthreads();
+  const int64_t j = (int64_t)blockIdx.x * 128 + threadIdx.x;
+  if (j >= n_vis) return;
+  const int seq = __ldg(p.q_seq + qi);
+  const int64_t s = slot_of(p.idx, seq, j);
+  float* out = p.scores + (int64_t)qi * p.row_stride + j;
+  if (!slot_ok(s, p.err)) { *out = -INFINITY; return; }
+
+  float acc[HI];
+#pragma unroll
+  for (int h = 0; h < HI; ++h) acc[h] = 0.f;
+  for (int c = 0; c < DI; c += 32) {
+    float key[32];
+    if constexpr (kFp8) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(
+          reinterpret_cast<const uint8_t*>(p.idx.data) + s * (int64_t)p.idx.width + c);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        float f[4];
+        e4m3x4_decode(__ldg(src + v), f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) key[4 * v + k] = f[k];
+      }
+    } else {
+      load_f<float, 32>(reinterpret_cast<const float*>(p.idx.data) + s * (int64_t)p.idx.width + c, key);
+    }
+#pragma unroll
+    for (int h = 0; h < HI; ++h) {
+      float a = acc[h];
+#pragma unroll
+      for (int d = 0; d < 32; ++d) a = fmaf(qs[h * DI + c + d], key[d], a);
+      acc[h] = a;
+    }
+  }
+  float sc = 0.f;
+#pragma unroll
+  for (int h = 0; h < HI; ++h) sc = fmaf(ws[h], fmaxf(acc[h], 0.f), sc);
+  if constexpr (kFp8) sc *= __ldg(p.idx.scale + s);
+  *out = sc + 0.0f;   // canonical +0 for an all-zero sum
+}
+
+// ------------------------------------------------------------------------------ top-k
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t b = __float_as_uint(x + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkSmemMax = 49152;   // rows up to this length are staged in shared memory
+
+// Exclusive block-wide prefix count of `flag`; returns the tile total through *total.
+__device__ __forceinline__ uint32_t block_excl_count(bool flag, uint32_t* warp_tot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
+  const uint32_t in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) warp_tot[warp] = __popc(bal);
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t v = lane < (kTopkThreads / 32) ? warp_tot[lane] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    warp_tot[lane] = incl - v;              // exclusive offset of each warp
+    if (lane == 31) *total = incl;
+  }
+  __syncthreads();
+  const uint32_t r = warp_tot[warp] + in_warp;
+  __syncthreads();
+  return r;
+}
+
+template <bool kSmem>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ IndexParams p) {
+  extern __shared__ uint32_t row_keys[];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t s_digit, s_remaining, s_total;
+  const int qi = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int64_t n = min(visible_entries(pos, p.S, p.W, p.win_off), p.row_stride);
+  int32_t* out = p.topk + (int64_t)qi * p.k;
+  if (n <= p.k) {
+    for (int i = tid; i < p.k; i += kTopkThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  const float* row = p.scores + (int64_t)qi * p.row_stride;
+  if constexpr (kSmem) {
+    for (int64_t i = tid; i < n; i += kTopkThreads) row_keys[i] = order_key(row[i]);
+    __syncthreads();
+  }
+  auto key_at = [&](int64_t i) -> uint32_t {
+    if constexpr (kSmem) return row_keys[i];
+    else return order_key(__ldg(row + i));
+  };
+
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += kTopkThreads) {
+      const int64_t i = base + tid;
+      bool take = false;
+      uint32_t bin = 0;
+      if (i < n) {
+        const uint32_t u = key_at(i);
+        take = (u & mask) == prefix;
+        bin = (u >> shift) & 0xFFu;
+      }
+      const uint32_t act = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        const uint32_t same = __match_any_sync(act, bin);
+        if ((threadIdx.x & 31) == (__ffs(same) - 1)) atomicAdd(&hist[bin], __popc(same));
+      }
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l owns digits [255-8l-7, 255-8l], scanned from the top
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) { c[k] = hist[255 - 8 * tid - k]; sum += c[k]; }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      const uint32_t before = incl - sum;
+      const bool here = before < remaining && incl >= remaining;
+      if (here) {
+        uint32_t cum = before;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (cum + c[k] >= remaining) {
+            s_digit = 255 - 8 * tid - k;
+            s_remaining = remaining - cum;
+            break;
+          }
+          cum += c[k];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= s_digit << shift;
+    mask |= 0xFFu << shift;
+    remaining = s_remaining;
+    __syncthreads();
+  }
+
+  // prefix is the key of the k-th largest score; take all keys above it and the first
+  // `remaining` keys equal to it, in index order.
+  const uint32_t kth = prefix;
+  uint32_t ties_before = 0, written = 0;
+  for (int64_t base = 0; base < n; base += kTopkThreads) {
+    const int64_t i = base + tid;
+    const uint32_t u = i < n ? key_at(i) : 0u;
+    const bool eq = i < n && u == kth;
+    const bool gt = i < n && u > kth;
+    const uint32_t tie_rank = ties_before + block_excl_count(eq, warp_tot, &s_total);
+    const uint32_t tie_tile = s_total;
+    const bool sel = gt || (eq && tie_rank < remaining);
+    const uint32_t at = written + block_excl_count(sel, warp_tot, &s_total);
+    const uint32_t sel_tile = s_total;
+    if (sel && at < (uint32_t)p.k) out[at] = (int32_t)i;
+    ties_before += tie_tile;
+    written += sel_tile;
+    __syncthreads();
+  }
+  for (int64_t i = (int64_t)written + tid; i < p.k; i += kTopkThreads) out[i] = -1;
+}
+
+template <typename T, bool kFp8, int HI, int DI>
+cudaError_t launch_simt(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
+  dim3 grid((unsigned)((max_vis + 127) / 128), (unsigned)p.n_q);
+  index_scores_simt<T, kFp8, HI, DI><<<grid, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaStream_t st) {
+  if (p.n_q == 0 || max_vis == 0) return V4A_OK;
+  cudaError_t e;
+  if (dtype == V4A_BF16_FP8 && p.H_I == 64 && p.d_I == 128)
+    e = launch_simt<__nv_bfloat16, true, 64, 128>(p, max_vis, st);
+  else if (dtype == V4A_FP32 && p.H_I == 4 && p.d_I == 32)
+    e = launch_simt<float, false, 4, 32>(p, max_vis, st);
+  else if (dtype == V4A_FP32 && p.H_I == 64 && p.d_I == 128)
+    e = launch_simt<float, false, 64, 128>(p, max_vis, st);
+  else
+    return V4A_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
+  if (p.n_q == 0) return V4A_OK;
+  cudaError_t e;
+  if (max_vis <= kTopkSmemMax) {
+    const size_t smem = (size_t)max_vis * sizeof(uint32_t);
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTopkSmemMax * (int)sizeof(uint32_t));
+      attr_set = true;
+    }
+    topk_kernel<true><<<p.n_q, kTopkThreads, smem, st>>>(p);
+  } else {
+    topk_kernel<false><<<p.n_q, kTopkThreads, 0, st>>>(p);
+  }
+  e = cudaGetLastError();
+  return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+}  // namespace v4a

@@ -1,0 +1,72 @@
+// Launch parameters and launchers of the v4a kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace v4a {
+
+struct CompressParams {
+  int64_t n_tokens;
+  int32_t n_seq;
+  int32_t D, DI, W, S, win_off;
+  float eps;
+  const int32_t* cu;
+  const int64_t* start;
+  const void* kv;
+  const void* score;
+  const void* ikv;
+  const void* iscore;
+  const float* bias;
+  const float* gamma;
+  const float* ibias;
+  CacheView attn, idx, swa, state;
+  Rope rope;
+  int32_t* err;
+};
+
+struct IndexParams {
+  int32_t n_q;
+  int32_t H_I, d_I, W, S, win_off;
+  int32_t k;
+  int64_t row_stride;          // floats between consecutive score rows in the workspace
+  const int32_t* q_seq;
+  const int64_t* q_pos;
+  const void* q_idx;
+  const float* w;
+  CacheView idx;
+  float* scores;               // workspace [n_q, row_stride]
+  int32_t* topk;               // [n_q, k]
+  int32_t* err;
+};
+
+struct AttnParams {
+  int32_t n_q;
+  int32_t H, D, W, S, win_off, swa_len;
+  int32_t k;                   // top-k list width (0 with topk == nullptr: dense)
+  int32_t n_split;             // CTAs per query
+  int32_t keys_per_split;      // keys handled by one split (multiple of the key tile)
+  float scale;                 // softmax scale
+  const int32_t* q_seq;
+  const int64_t* q_pos;
+  const void* q;
+  const int32_t* topk;
+  CacheView attn, swa;
+  void* out;
+  float* part_o;               // [n_q, n_split, H, D]   (n_split > 1)
+  float* part_ml;              // [n_q, n_split, H, 2]   (n_split > 1)
+  Rope rope;
+  int32_t* err;
+};
+
+int launch_compress_insert(const CompressParams& p, int dtype, cudaStream_t st);
+int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaStream_t st);
+int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st);
+int launch_attention(const AttnParams& p, int dtype, cudaStream_t st);
+int launch_slot_mapping(const CacheView& c, int32_t n, const int32_t* seq, const int64_t* row,
+                        int32_t* slots, int32_t* err, cudaStream_t st);
+
+}  // namespace v4a

@@ -1,0 +1,209 @@
+/*
+ * v4a — one layer of DeepSeek-V4-style hybrid compressed attention on one GB300 (sm_103a).
+ *
+ * C ABI of the library. Every call is asynchronous on the caller's CUDA stream, allocates
+ * nothing, keeps no state between calls and may be called from several host threads.
+ * All pointers named "device" point to device memory owned by the caller; the library
+ * never frees or retains them after the call returns (the kernels it enqueued may still
+ * be reading them until the stream reaches that point). Structs passed by pointer
+ * (v4a_layer_cfg, v4a_cache) live in host memory and are copied during the call.
+ *
+ * Sources (page title, section):
+ *   [notes] "DeepSeek V4 in vLLM 技术博客详尽笔记" (vllm-deepseek-v4-notes.pages.dev)
+ *   [blog]  "vLLM DeepSeek V4 支援：高效長上下文注意力" (agentlenshq.com)
+ *   [serve] "DeepSeek-V4服务：百万token上下文成为推理系统难题" (ai-pulse-lab.com)
+ *
+ * Paged layout ([notes] 解决方案一：统一逻辑块大小): every cache is split into logical
+ * blocks of 256 native token positions. A block of a c4a entry cache holds 64 entries,
+ * a block of a c128a entry cache holds 2 entries, a block of a token cache (sliding
+ * window, compressor residual) holds 256 tokens. Row r of sequence b (a token position or
+ * an entry index) lives in logical block r / R (R = rows per block), whose physical page
+ * is block_table[b * max_blocks + r / R]; its pool row ("slot") is page * R + r % R.
+ * A page of -1 means the block is not allocated.
+ *
+ * Error behaviour: every call first validates its host-visible arguments and returns
+ * V4A_ERR_ARG or V4A_ERR_UNSUPPORTED without enqueuing anything. A failed launch returns
+ * V4A_ERR_CUDA. Problems only the device can see (a needed row whose block has no page, a
+ * page id outside the pool, a top-k entry that is not visible to its query) are OR-ed
+ * into the caller's device error word `dev_err` (may be NULL to ignore them); the affected
+ * row or query is skipped or zeroed, never read out of bounds. v4a_get_error() reads and
+ * clears that word.
+ */
+#ifndef V4A_H
+#define V4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* v4a_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+/* return codes */
+#define V4A_OK 0
+#define V4A_ERR_ARG (-1)          /* NULL pointer, misaligned pointer, inconsistent sizes */
+#define V4A_ERR_UNSUPPORTED (-2)  /* dims / dtype / kind without a kernel */
+#define V4A_ERR_CUDA (-3)         /* a CUDA launch or runtime call failed */
+#define V4A_ERR_DEVICE (-4)       /* v4a_get_error found device-side error bits */
+
+/* device error word bits */
+#define V4A_DEV_MISSING_PAGE 1u   /* a row the computation needs is in a block with no page */
+#define V4A_DEV_BAD_PAGE 2u       /* a block table names a page >= n_pages */
+#define V4A_DEV_BAD_INDEX 4u      /* a top-k list names an entry its query may not see */
+#define V4A_DEV_BAD_POS 8u        /* a query position above the max_pos the call was sized for;
+                                     the query's rows beyond that bound are ignored */
+
+/* layer kinds ([notes] 四大核心技术; 数学附录精要) */
+#define V4A_C4A 0                 /* entry = weighted sum of 8 tokens at stride 4 */
+#define V4A_C128A 1               /* entry = weighted sum of 128 tokens at stride 128 */
+
+/* arithmetic / storage */
+#define V4A_FP32 0                /* fp32 inputs, fp32 caches, fp32 output */
+#define V4A_BF16_FP8 1            /* bf16 inputs, fp8 e4m3 caches + fp32 row scale, bf16 output */
+
+typedef struct v4a_layer_cfg {
+  int32_t kind;          /* V4A_C4A or V4A_C128A */
+  int32_t dtype;         /* V4A_FP32 or V4A_BF16_FP8 */
+  int32_t head_dim;      /* D: dim of the shared K=V head and of each query head */
+  int32_t rope_dim;      /* d_r: the last d_r dims are rotated, as adjacent pairs */
+  int32_t n_heads;       /* H: query heads */
+  int32_t idx_heads;     /* H_I: indexer heads (c4a) */
+  int32_t idx_dim;       /* d_I: indexer head dim (c4a) */
+  int32_t window;        /* W: tokens per entry (8 for c4a, 128 for c128a) */
+  int32_t stride;        /* S: tokens between entries (4 / 128) */
+  int32_t win_off;       /* entry j covers S*j+win_off .. S*j+win_off+W-1, win_off in (-W, 0] */
+  int32_t swa;           /* sliding window: a query at p sees tokens [p-swa+1, p] */
+  float rope_base;       /* theta_i = rope_base^(-2i/d_r) */
+  float rms_eps;         /* RMSNorm epsilon of compressed entries */
+  float softmax_scale;   /* logit scale, usually 1/sqrt(D) */
+} v4a_layer_cfg;
+
+typedef struct v4a_cache {
+  void* data;                  /* device: [n_pages*rows_per_block, row_width] elements; e4m3
+                                  bytes for fp8 pools, fp32 or bf16 for the others */
+  float* scale;                /* device: [n_pages*rows_per_block] row scales (fp8 pools), else NULL */
+  const int32_t* block_table;  /* device: [n_seq, max_blocks] physical page per logical block, -1 = none */
+  int32_t max_blocks;          /* columns of block_table */
+  int32_t rows_per_block;      /* 64 (c4a entries), 2 (c128a entries), 256 (token caches) */
+  int64_t n_pages;             /* pages in the pool (bounds check of block-table values) */
+  int32_t row_width;           /* elements per row */
+  int32_t reserved;            /* must be 0 */
+} v4a_cache;
+
+/*
+ * v4a_compress_insert — insert one step's new tokens of every sequence (steps a1-a5).
+ *
+ * [blog] GPU 計算飽和度 / [notes] 优化一：三大内核融合 (fusion 1: compressor + RMSNorm +
+ * RoPE + cache insert; fusion 3's KV RoPE + K insert) and [notes] 解决方案二 (the compressor
+ * state kept as sliding-window KV).
+ *
+ * Sequence b owns input rows cu_tokens[b] .. cu_tokens[b+1]-1 at positions
+ * start_pos[b] + (row - cu_tokens[b]). For every new token t:
+ *   - swa row t      = RoPE(kv_t, t), stored (fp8: per-row scale amax/448, e4m3 RNE);
+ *   - state row t    = raw (kv_t | s_t | ik_t | is_t) if t is among the last W positions of
+ *                      the sequence's new tokens (what later calls can still need);
+ *   - if t completes entry j (t = S*j + win_off + W - 1, j >= 0):
+ *       attn row j   = RoPE(RMSNorm(sum_o softmax_o(s + bias[o]) * kv) * gamma, S*j),
+ *       idx row j    = sum_o softmax_o(is + ibias[o]) * ik (c4a only; no norm, no RoPE),
+ *     where the window's tokens before start_pos[b] are read from the state cache.
+ * Rows whose block has no page are not written (a needed state row without a page sets
+ * V4A_DEV_MISSING_PAGE and the entry is skipped).
+ *
+ * kv, score:    device [n_tokens, D]    (fp32 or bf16 per cfg->dtype)
+ * ikv, iscore:  device [n_tokens, d_I]  (c4a; NULL for c128a)
+ * bias:         device fp32 [W, D];  gamma: device fp32 [D];  ibias: device fp32 [W, d_I] (c4a)
+ * cu_tokens:    device int32 [n_seq+1], non-decreasing, cu_tokens[n_seq] == n_tokens
+ * start_pos:    device int64 [n_seq]
+ * attn:  entry cache (rows_per_block = 256/S, row_width = D)
+ * idx:   indexer-key cache (c4a: rows_per_block 64, row_width d_I; NULL for c128a)
+ * swa:   token cache (rows_per_block 256, row_width D)
+ * state: token cache of raw rows (rows_per_block 256, row_width 2D (+2 d_I for c4a)),
+ *        element type of the inputs.
+ * Pool data pointers must be 16-byte aligned.
+ */
+int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
+                        const int32_t* cu_tokens, const int64_t* start_pos,
+                        const void* kv, const void* score, const float* bias,
+                        const float* gamma, const void* ikv, const void* iscore,
+                        const float* ibias, const v4a_cache* attn, const v4a_cache* idx,
+                        const v4a_cache* swa, const v4a_cache* state, int32_t* dev_err,
+                        v4a_stream_t stream);
+
+/*
+ * v4a_index_topk — indexer scores and top-k selection of c4a entries (steps a6, a7).
+ *
+ * [blog] DeepSeek Sparse Attention (DSA) and [notes] 压缩参数细节 (C4A top-k 512).
+ * For query i of sequence q_seq[i] at position p = q_pos[i], over the visible entries
+ * j (every position S*j+win_off+o they cover is < p; [notes] 因果性条件):
+ *   score_j = sum_h w[i,h] * max(0, q_idx[i,h,:] . k_j)
+ * with k_j the dequantised indexer key. If at most k entries are visible, all are kept;
+ * otherwise the k largest scores, ties to the smaller j. topk_out[i, :] lists the kept j
+ * in ascending order, padded with -1.
+ *
+ * q_idx:    device [n_q, H_I, d_I] (fp32 or bf16)
+ * w:        device fp32 [n_q, H_I]
+ * q_seq:    device int32 [n_q];  q_pos: device int64 [n_q], every q_pos <= max_pos
+ * topk_out: device int32 [n_q, k]
+ * workspace: device, >= v4a_index_topk_workspace_size(...) bytes, 256-byte aligned.
+ */
+size_t v4a_index_topk_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos);
+int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                   const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
+                   const v4a_cache* idx, int32_t k, int32_t* topk_out, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream);
+
+/*
+ * v4a_attn_decode / v4a_attn_prefill — shared-K=V attention with inverse RoPE (a8, a9).
+ *
+ * [notes] Inverse RoPE 的数学原理: out = (sum softmax(q K^T) V) R^-1(theta_p), K = V;
+ * [blog] 短滑動窗口 (window of 128 uncompressed tokens).
+ * For query i at p = q_pos[i] of sequence b = q_seq[i]:
+ *   keys  = { attn row j : j in topk[i, :], j >= 0 }   (topk != NULL, c4a)
+ *         | { attn row j : j visible at p }             (topk == NULL, dense, c128a)
+ *         + { swa row t : max(0, p-swa+1) <= t <= p }
+ *   out_h = R^-1(p) * sum_x softmax_x(scale * RoPE(q_h, p) . key_x) * key_x
+ * Both calls compute the same function; decode splits each query's keys over several
+ * CTAs (few queries, one per sequence), prefill gives each query one CTA (many queries).
+ *
+ * q:    device [n_q, H, D] (fp32 or bf16);  out: device [n_q, H, D] (fp32 or bf16)
+ * topk: device int32 [n_q, k] or NULL
+ * attn: entry cache;  swa: token cache
+ * workspace: device, >= v4a_attn_workspace_size(...) bytes, 256-byte aligned.
+ */
+size_t v4a_attn_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos,
+                               int32_t k, int32_t prefill);
+int v4a_attn_decode(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                    const int64_t* q_pos, int64_t max_pos, const void* q, const int32_t* topk,
+                    int32_t k, const v4a_cache* attn, const v4a_cache* swa, void* out,
+                    void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                    v4a_stream_t stream);
+int v4a_attn_prefill(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                     const int64_t* q_pos, int64_t max_pos, const void* q,
+                     const int32_t* topk, int32_t k, const v4a_cache* attn,
+                     const v4a_cache* swa, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_err, v4a_stream_t stream);
+
+/*
+ * v4a_slot_mapping — pool rows of logical rows ([notes] 解决方案一: slot mapping in the
+ * unit of the 256-position block). slots[i] = page * R + row[i] % R with
+ * page = block_table[seq[i], row[i] / R], or -1 if the block has no page or lies beyond
+ * max_blocks (a page >= n_pages also gives -1 and sets V4A_DEV_BAD_PAGE).
+ * seq: device int32 [n]; row: device int64 [n]; slots: device int32 [n].
+ */
+int v4a_slot_mapping(const v4a_cache* cache, int32_t n, const int32_t* seq,
+                     const int64_t* row, int32_t* slots, int32_t* dev_err,
+                     v4a_stream_t stream);
+
+/* Synchronise `stream`, read the device error word, clear it. *flags_out (may be NULL)
+ * receives the bits. Returns V4A_OK, V4A_ERR_DEVICE if any bit was set, or V4A_ERR_CUDA. */
+int v4a_get_error(int32_t* dev_err, v4a_stream_t stream, int32_t* flags_out);
+
+/* Library version, for the binding's sanity check. */
+int32_t v4a_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* V4A_H */

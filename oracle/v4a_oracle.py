@@ -195,6 +195,23 @@ class Pools:
 class _Pool:
     def __init__(self, data, scale, bt, R):
         self.data, self.scale, self.bt, self.R = data, scale, bt, R
+        self.raw = {}          # pool row -> value before fp8 rounding (for the tests)
+
+    def slots(self, seq, rows) -> np.ndarray:
+        """slot() of many logical rows of one sequence."""
+        rows = np.asarray(rows, dtype=np.int64)
+        blk = rows // self.R
+        inside = (rows >= 0) & (blk < self.bt.shape[1])
+        page = np.where(inside, self.bt[seq, np.where(inside, blk, 0)], -1).astype(np.int64)
+        return np.where(page >= 0, page * self.R + rows % self.R, -1)
+
+    def read_many(self, seq, rows, fp8):
+        s = self.slots(seq, rows)
+        if (s < 0).any():
+            raise ValueError("a row of sequence %d has no page" % seq)
+        if fp8:
+            return e4m3_decode(self.data[s]) * self.scale[s][:, None]
+        return self.data[s].astype(np.float64)
 
     def read(self, seq, r, fp8):
         s = slot(self.bt, self.R, seq, r)
@@ -214,6 +231,7 @@ class _Pool:
             self.scale[s] = sc[0]
         else:
             self.data[s] = y
+        self.raw[s] = np.array(y, dtype=np.float64)
         return s
 
 
@@ -316,8 +334,7 @@ def index_topk(spec, pools: Pools, q_seq, q_pos, q_idx, w, k: int):
     for i in range(n_q):
         b, p = int(q_seq[i]), int(q_pos[i])
         n = visible_entries(spec.S, spec.W, spec.win_off, p)
-        keys = np.stack([pools.idx.read(b, j, spec.fp8) for j in range(n)]) if n else \
-            np.zeros((0, spec.d_I))
+        keys = pools.idx.read_many(b, np.arange(n), spec.fp8) if n else np.zeros((0, spec.d_I))
         sc = index_scores(np.asarray(q_idx[i], np.float64), np.asarray(w[i], np.float64), keys)
         out[i] = select_topk(sc, k)
         all_scores.append(sc)
@@ -346,9 +363,9 @@ def attend(q_row: np.ndarray, p: int, keys: np.ndarray, scale: float, d_r: int,
 def gather_keys(spec, pools: Pools, b: int, p: int, entries) -> np.ndarray:
     """Keys of a query at p: the listed compressed entries, then the window tokens
     [max(0, p-swa+1), p] (R3; [blog] 短滑動窗口)."""
-    rows = [pools.attn.read(b, int(j), spec.fp8) for j in entries]
-    rows += [pools.swa.read(b, t, spec.fp8) for t in range(max(0, p - spec.swa + 1), p + 1)]
-    return np.stack(rows)
+    ent = pools.attn.read_many(b, np.asarray(list(entries), dtype=np.int64), spec.fp8)
+    win = pools.swa.read_many(b, np.arange(max(0, p - spec.swa + 1), p + 1), spec.fp8)
+    return np.concatenate([ent.reshape(-1, spec.D), win])
 
 
 def attention(spec, pools: Pools, q_seq, q_pos, q, topk=None) -> np.ndarray:

@@ -1,0 +1,118 @@
+"""CPU-side checks of the C ABI: the library loads, exports every declared symbol, the
+ctypes structs match the C layout, and host-side validation rejects bad arguments
+without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import compressed_sparse_long_gb300 as v4a
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "v4a.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(v4a_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(v4a.LIB_PATH):
+        from compressed_sparse_long_gb300 import build
+        build.build()
+    return v4a.library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "v4a_compress_insert" in names and "v4a_attn_prefill" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", v4a.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r"\bT (v4a_\w+)", out))
+    assert set(names) <= exported
+    assert v4a.v4a_version() == 1
+
+
+def test_struct_layout_matches_c(tmp_path):
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "v4a.h"\n'
+                    'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(v4a_layer_cfg),'
+                    ' offsetof(v4a_layer_cfg, softmax_scale), sizeof(v4a_cache),'
+                    ' offsetof(v4a_cache, n_pages), offsetof(v4a_cache, row_width),'
+                    ' offsetof(v4a_cache, max_blocks)); return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(prog), "-o",
+                    str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(v4a.LayerCfg), v4a.LayerCfg.softmax_scale.offset,
+            ctypes.sizeof(v4a.Cache), v4a.Cache.n_pages.offset, v4a.Cache.row_width.offset,
+            v4a.Cache.max_blocks.offset]
+    assert got == want
+
+
+def _cfg(**kw):
+    base = dict(kind=v4a.C4A, dtype=v4a.BF16_FP8, head_dim=512, rope_dim=64, n_heads=64,
+                idx_heads=64, idx_dim=128, window=8, stride=4)
+    base.update(kw)
+    return v4a.layer_cfg(**base)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    cfg = _cfg()
+    c = v4a.Cache()
+    null = ctypes.POINTER(v4a.LayerCfg)()
+    # no config
+    assert lib.v4a_compress_insert(null, 1, 1, 8, 8, 8, 8, 8, 8, 8, 8, 8, None, None, None, None,
+                                   None, None) == v4a.ERR_ARG
+    # zero tokens / queries: nothing to do
+    assert lib.v4a_compress_insert(ctypes.byref(cfg), 1, 0, None, None, None, None, None, None,
+                                   None, None, None, None, None, None, None, None, None) == v4a.OK
+    assert lib.v4a_index_topk(ctypes.byref(cfg), 0, None, None, 0, None, None, ctypes.byref(c),
+                              512, None, None, 0, None, None) == v4a.OK
+    # missing pointers
+    assert lib.v4a_attn_decode(ctypes.byref(cfg), 4, None, None, 100, None, None, 0,
+                               ctypes.byref(c), ctypes.byref(c), None, None, 0, None,
+                               None) == v4a.ERR_ARG
+    # unsupported kind / odd rope dim / positive window offset
+    assert lib.v4a_index_topk(ctypes.byref(_cfg(kind=7)), 1, 8, 8, 0, 16, 16, ctypes.byref(c),
+                              1, 16, None, 0, None, None) == v4a.ERR_UNSUPPORTED
+    assert lib.v4a_index_topk(ctypes.byref(_cfg(rope_dim=3)), 1, 8, 8, 0, 16, 16,
+                              ctypes.byref(c), 1, 16, None, 0, None, None) == v4a.ERR_UNSUPPORTED
+    assert lib.v4a_index_topk(ctypes.byref(_cfg(win_off=1)), 1, 8, 8, 0, 16, 16, ctypes.byref(c),
+                              1, 16, None, 0, None, None) == v4a.ERR_ARG
+    # the indexer exists only for c4a layers
+    assert lib.v4a_index_topk(ctypes.byref(_cfg(kind=v4a.C128A, window=128, stride=128)), 1, 8,
+                              8, 0, 16, 16, ctypes.byref(c), 1, 16, None, 0, None,
+                              None) == v4a.ERR_UNSUPPORTED
+
+
+def test_cache_descriptor_checks(lib):
+    cfg = _cfg()
+    bt = 256
+    good = v4a.Cache(4096, 8192, bt, 4, 64, 10, 128, 0)
+    bad_width = v4a.Cache(4096, 8192, bt, 4, 64, 10, 96, 0)
+    misaligned = v4a.Cache(4100, 8192, bt, 4, 64, 10, 128, 0)
+    no_scale = v4a.Cache(4096, None, bt, 4, 64, 10, 128, 0)
+    for c, want in ((bad_width, v4a.ERR_ARG), (misaligned, v4a.ERR_ARG), (no_scale, v4a.ERR_ARG)):
+        assert lib.v4a_index_topk(ctypes.byref(cfg), 1, 16, 16, 100, 4096, 16, ctypes.byref(c),
+                                  4, 16, 4096, 1 << 20, None, None) == want
+    # workspace too small is refused before any launch
+    assert lib.v4a_index_topk(ctypes.byref(cfg), 1, 16, 16, 100, 4096, 16, ctypes.byref(good),
+                              4, 16, 4096, 8, None, None) == v4a.ERR_ARG
+    assert v4a.v4a_index_topk_workspace_size(cfg, 32, 32768) >= 32 * 8191 * 4
+
+
+def test_workspace_sizes_are_monotone():
+    cfg = _cfg()
+    a = v4a.v4a_index_topk_workspace_size(cfg, 8, 4096)
+    b = v4a.v4a_index_topk_workspace_size(cfg, 8, 8192)
+    assert 0 < a < b
+    assert v4a.v4a_attn_workspace_size(cfg, 8192, 131072, 512, 1) >= 256

@@ -1,0 +1,359 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded
+inputs. Marked gpu; the acceptance rules are in helpers.py."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_long_gb300 as v4a
+import workloads as wl
+from helpers import (DevInputs, T, check_fp8_rows, check_out, check_topk, device_layer,
+                     oracle_insert, oracle_pools)
+from oracle import v4a_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.synchronize()
+    yield
+    torch.cuda.synchronize()
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _gpu_rows(pool):
+    d = pool.data.cpu()
+    if d.dtype == torch.bfloat16:
+        d = d.float()
+    return d.numpy(), None if pool.scale is None else pool.scale.cpu().numpy()
+
+
+def _compare_written(dev_layer, pools, writes, fp8):
+    """Rows the oracle wrote must match the GPU's rows at the same pool slots."""
+    n_close = 0
+    for kind in ("attn", "idx", "swa", "state"):
+        slots = sorted({s for (k, _, _, s) in writes if k == kind and s >= 0})
+        if not slots:
+            continue
+        g_data, g_scale = _gpu_rows(getattr(dev_layer, kind))
+        ref = getattr(pools, kind)
+        if kind == "state":
+            assert np.array_equal(g_data[slots], ref.data[slots]), "residual rows differ"
+        elif fp8:
+            n_close += check_fp8_rows(g_data, g_scale, ref, slots)
+        else:
+            d = np.abs(g_data[slots] - ref.data[slots])
+            assert d.max() <= 1e-5, (kind, d.max())
+    return n_close
+
+
+# ------------------------------------------------------------------------- fp32 layer
+@pytest.mark.parametrize("win_off", [0, -4])
+def test_tiny_fp32_layer_every_position(win_off):
+    """Tiny fp32 c4a layer, one sequence of 1024 tokens, all 1024 positions queried:
+    insert, index + top-64, attention; max-abs 1e-4 against the oracle."""
+    w = wl.tiny_prefill(seed=0, L=1024, win_off=win_off)
+    h = w.layers[0]
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    out, topk = lay.step(x.cu, x.start, x.kv, x.s, x.ik, x.is_, x.q_seq, x.q_pos, x.max_pos,
+                         x.q, x.q_idx, x.w, prefill=True, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    pools = oracle_pools(h)
+    writes = oracle_insert(w, h, pools)
+    _compare_written(lay, pools, writes, fp8=False)
+    q = w.queries
+    ref_top, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, h.spec.top_k)
+    same = check_topk(topk.cpu().numpy(), ref_top, scores, h.spec.top_k)
+    assert len(same) >= 0.95 * len(q.pos)
+    ref = O.attention(h.spec, pools, q.seq[same], q.pos[same], q.q[same], ref_top[same])
+    check_out(out.cpu().numpy()[same], ref, fp8=False)
+
+
+def test_slot_mapping_bit_exact():
+    rng = np.random.default_rng(0)
+    for R in (256, 64, 2):
+        need = [set(rng.choice(40, 25, replace=False).tolist()) for _ in range(3)]
+        bt, n_pages = wl.block_table(rng, need, 40)
+        n = 5000
+        seq = rng.integers(0, 3, n).astype(np.int32)
+        row = rng.integers(-3, 40 * R + 10, n).astype(np.int64)
+        data = torch.zeros((n_pages * R, 16), dtype=torch.uint8, device="cuda")
+        bt_dev = T(bt, torch.int32)                 # must outlive the launch
+        c = v4a.cache(data, None, bt_dev, R)
+        slots = torch.empty(n, dtype=torch.int32, device="cuda")
+        v4a.v4a_slot_mapping(c, n, T(seq, torch.int32), T(row, torch.int64), slots)
+        want = np.array([O.slot(bt, R, int(s), int(r)) for s, r in zip(seq, row)])
+        assert np.array_equal(slots.cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------------ compressor
+@pytest.mark.parametrize("kind", ["c4a", "c128a"])
+def test_compress_insert_fp8_ragged_chunks(kind):
+    """Several sequences with ragged contexts and chunks (windows spanning the residual
+    pool, partial windows left behind); every written row is compared."""
+    spec = wl.LayerSpec(kind, True)
+    rng = np.random.default_rng(21)
+    ctx = [1000, 37, 127, 4096] if kind == "c4a" else [1000, 130, 127, 4096]
+    new = [300, 1, 129, 257]
+    h = wl.make_layer(rng, spec, ctx, new, prefill_cache=True)
+    h.bias, h.gamma, h.ibias = wl.layer_params(rng, spec)
+    b = wl.make_batch(rng, spec, ctx, new)
+    w = wl.Workload("ragged", [h], b, wl.make_queries(rng, spec, np.arange(4), np.array(ctx),
+                                                      False))
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    pools = oracle_pools(h)
+    writes = oracle_insert(w, h, pools)
+    assert any(k == "attn" for (k, _, _, _) in writes)
+    _compare_written(lay, pools, writes, fp8=True)
+
+
+def test_compress_chunking_invariance_gpu():
+    """One call or several ragged calls write identical bytes on the GPU."""
+    w = wl.c4a_prefill(seed=3, cached=4096, chunk=1000)
+    h = w.layers[0]
+    one, many = device_layer(h), device_layer(h)
+    x = DevInputs(w)
+    one.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_)
+    cuts = [0, 3, 4, 77, 500, 999, 1000]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        cu = torch.tensor([0, b - a], dtype=torch.int32, device="cuda")
+        st = torch.tensor([4096 + a], dtype=torch.int64, device="cuda")
+        many.compress_insert(cu, st, x.kv[a:b].contiguous(), x.s[a:b].contiguous(),
+                             x.ik[a:b].contiguous(), x.is_[a:b].contiguous())
+    for name in ("attn", "idx", "swa"):
+        p1, p2 = getattr(one, name), getattr(many, name)
+        assert torch.equal(p1.data, p2.data) and torch.equal(p1.scale, p2.scale), name
+
+
+# -------------------------------------------------------------------- indexer / top-k
+def _inject_subnormal_keys(h, rng, n=200):
+    """Give some indexer rows only subnormal e4m3 codes and a large scale, so a wrong
+    decoding of subnormal codes changes the scores."""
+    used = np.nonzero(h.idx.data.any(axis=1))[0]
+    rows = rng.choice(used, size=min(n, len(used)), replace=False)
+    codes = rng.integers(0, 8, size=(len(rows), h.idx.data.shape[1]))
+    codes |= rng.integers(0, 2, size=codes.shape) << 7
+    h.idx.data[rows] = codes.astype(np.uint8)
+    h.idx.scale[rows] = 2000.0
+
+
+def test_index_topk_fp8_decode():
+    w = wl.c4a_decode(seed=1, B=8, L=8192)
+    h = w.layers[0]
+    _inject_subnormal_keys(h, np.random.default_rng(5))
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    topk = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    pools = oracle_pools(h)
+    q = w.queries
+    ref, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, 512)
+    same = check_topk(topk.cpu().numpy(), ref, scores, 512)
+    assert len(same) >= 6
+
+
+@pytest.mark.parametrize("n_q,k", [(16, 512), (5, 64), (3, 2048)])
+def test_index_topk_prefill_positions(n_q, k):
+    """Queries at many positions of one sequence (ragged visibility, rows shorter and
+    longer than k)."""
+    w = wl.c4a_prefill(seed=3, cached=16384, chunk=n_q)
+    h = w.layers[0]
+    q = w.queries
+    q.pos = np.sort(np.random.default_rng(1).integers(0, 16384, n_q)).astype(np.int64)
+    q.pos[0] = 9                                   # two visible entries
+    lay, x = device_layer(h), DevInputs(w)
+    topk = lay.index_topk(x.q_seq, x.q_pos, int(q.pos.max()), x.q_idx, x.w, k=k)
+    pools = oracle_pools(h)
+    ref, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, k)
+    check_topk(topk.cpu().numpy(), ref, scores, k)
+
+
+def test_topk_ties_take_smaller_index():
+    """Equal scores: identical keys tie exactly; the smaller entry indices win."""
+    w = wl.c4a_decode(seed=7, B=2, L=4096)
+    h = w.layers[0]
+    h.idx.data[:] = h.idx.data[0]
+    h.idx.scale[:] = h.idx.scale[0]
+    lay, x = device_layer(h), DevInputs(w)
+    topk = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w).cpu().numpy()
+    for i in range(2):
+        assert np.array_equal(topk[i], np.arange(512))
+
+
+# ------------------------------------------------------------------------- attention
+def _random_lists(rng, pos, spec, k, n_pad=3):
+    out = np.full((len(pos), k), -1, np.int32)
+    for i, p in enumerate(pos):
+        n = O.visible_entries(spec.S, spec.W, spec.win_off, int(p))
+        m = max(0, min(k - n_pad, n))
+        out[i, :m] = np.sort(rng.choice(n, m, replace=False))
+    return out
+
+
+def _fill_query_window_row(h, w):
+    """Random stored window row at each query position (normally written by the insert)."""
+    rng = np.random.default_rng(99)
+    for b, p in zip(w.queries.seq, w.queries.pos):
+        s = O.slot(h.swa.bt, 256, int(b), int(p))
+        c, sc = wl.random_fp8_rows(rng, 1, h.spec.D)
+        h.swa.data[s], h.swa.scale[s] = c[0], sc[0]
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_fp8_c4a_lists(prefill):
+    w = wl.c4a_decode(seed=11, B=8, L=8192)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lists = _random_lists(np.random.default_rng(3), q.pos, h.spec, 512)
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32),
+                        prefill=prefill, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
+    check_out(out.float().cpu().numpy(), ref, fp8=True)
+
+
+def test_attention_fp8_c128a_dense():
+    w = wl.c128a_decode(seed=2, B=4, L=65536)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lay, x = device_layer(h), DevInputs(w)
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, None)
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, None)
+    check_out(out.float().cpu().numpy(), ref, fp8=True)
+
+
+def test_attention_k_covers_all_equals_dense():
+    """A top-k list holding every visible entry gives the dense result."""
+    w = wl.c4a_decode(seed=12, B=4, L=1024)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    lay, x = device_layer(h), DevInputs(w)
+    n = O.visible_entries(4, 8, 0, 1024)
+    lists = np.tile(np.concatenate([np.arange(n), -np.ones(512 - n)]).astype(np.int32), (4, 1))
+    a = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32))
+    d = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, None)
+    diff = (a.float() - d.float()).abs().max().item()
+    assert diff <= 1e-2, diff
+
+
+def test_attention_no_visible_entries_window_only():
+    """Queries before position 8 see no c4a entry: the layer is window attention."""
+    w = wl.tiny_prefill(seed=4, L=8)
+    h = w.layers[0]
+    lay, x = device_layer(h), DevInputs(w)
+    out, topk = lay.step(x.cu, x.start, x.kv, x.s, x.ik, x.is_, x.q_seq, x.q_pos, x.max_pos, x.q,
+                         x.q_idx, x.w, prefill=True)
+    assert (topk.cpu().numpy() == -1).all()
+    pools = oracle_pools(h)
+    oracle_insert(w, h, pools)
+    q = w.queries
+    ref = O.attention(h.spec, pools, q.seq, q.pos, q.q, np.full((8, 64), -1))
+    check_out(out.cpu().numpy(), ref, fp8=False)
+
+
+# ---------------------------------------------------------------------- device errors
+def test_missing_page_and_bad_index_raise_device_error():
+    w = wl.c4a_decode(seed=13, B=2, L=2048)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    h.attn.bt[1, 3] = -1                                   # hole in sequence 1's entries
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    lists = np.tile(np.arange(512, dtype=np.int32), (2, 1))
+    lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32), dev_err=err)
+    assert v4a.v4a_get_error(err) & v4a.DEV_MISSING_PAGE
+    assert v4a.v4a_get_error(err) == 0                     # read clears the word
+    lists[0, -1] = 600                                     # not visible at p = 2048
+    lists[1] = np.arange(512)
+    lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32), dev_err=err)
+    assert v4a.v4a_get_error(err) & v4a.DEV_BAD_INDEX
+
+
+def test_empty_calls_are_noops():
+    w = wl.c4a_decode(seed=14, B=2, L=1024)
+    lay = device_layer(w.layers[0])
+    z32 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    z64 = torch.zeros(0, dtype=torch.int64, device="cuda")
+    lay.compress_insert(torch.zeros(2, dtype=torch.int32, device="cuda"),
+                        torch.zeros(1, dtype=torch.int64, device="cuda"),
+                        torch.empty((0, 512), dtype=torch.bfloat16, device="cuda"),
+                        torch.empty((0, 512), dtype=torch.bfloat16, device="cuda"),
+                        torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"),
+                        torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"))
+    out = lay.attention(z32[:0], z64, 0, torch.empty((0, 64, 512), dtype=torch.bfloat16,
+                                                     device="cuda"), None)
+    assert out.shape[0] == 0
+
+
+# ------------------------------------------------------------- full-size workloads
+def _full_step(w, li=0, prefill=False):
+    h = w.layers[li]
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    out, topk = lay.step(x.cu, x.start, x.kv, x.s, x.ik, x.is_, x.q_seq, x.q_pos, x.max_pos,
+                         x.q, x.q_idx, x.w, prefill=prefill, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    return h, out.float().cpu().numpy(), None if topk is None else topk.cpu().numpy()
+
+
+def _oracle_sampled(w, h, sample, topk_gpu):
+    """The oracle's own insert, top-k and attention for the sampled queries."""
+    pools = oracle_pools(h)
+    oracle_insert(w, h, pools)
+    q = w.queries
+    if h.spec.has_indexer:
+        ref_top, scores = O.index_topk(h.spec, pools, q.seq[sample], q.pos[sample],
+                                       q.q_idx[sample], q.w[sample], h.spec.top_k)
+        same = check_topk(topk_gpu[sample], ref_top, scores, h.spec.top_k)
+        keep = [sample[i] for i in same]
+        ref = O.attention(h.spec, pools, q.seq[keep], q.pos[keep], q.q[keep], ref_top[same])
+    else:
+        keep = list(sample)
+        ref = O.attention(h.spec, pools, q.seq[keep], q.pos[keep], q.q[keep], None)
+    return keep, ref
+
+
+def test_c4a_decode_full_size_sampled():
+    """B=32 sequences of 32768 tokens, one new token and query each (full layer step)."""
+    w = wl.c4a_decode()
+    h, out, topk = _full_step(w)
+    keep, ref = _oracle_sampled(w, h, [0, 7, 19, 31], topk)
+    assert len(keep) >= 3
+    check_out(out[keep], ref, fp8=True)
+
+
+def test_c128a_decode_full_size_sampled():
+    """B=8 sequences of 2^20 tokens, dense over 8192 entries + window."""
+    w = wl.c128a_decode()
+    h, out, _ = _full_step(w)
+    keep, ref = _oracle_sampled(w, h, [0, 5], None)
+    check_out(out[keep], ref, fp8=True)
+
+
+def test_c4a_prefill_full_size_sampled():
+    """122880 cached tokens plus a chunk of 8192; sampled chunk queries."""
+    w = wl.c4a_prefill()
+    h, out, topk = _full_step(w, prefill=True)
+    sample = [0, 1, 3, 4095, 4096, 8190, 8191]
+    keep, ref = _oracle_sampled(w, h, sample, topk)
+    assert len(keep) >= 5
+    check_out(out[keep], ref, fp8=True)
+
+
+def test_mixed_decode_full_size_sampled():
+    """64 sequences, log-uniform lengths in [4096, 2^20), a c4a and a c128a layer."""
+    w = wl.mixed_decode()
+    for li in (0, 1):
+        h, out, topk = _full_step(w, li)
+        keep, ref = _oracle_sampled(w, h, [0, 13, 40, 63], topk)
+        assert len(keep) >= 3
+        check_out(out[keep], ref, fp8=True)
