@@ -1,0 +1,520 @@
+"""Benchmark of one hybrid-compressed-attention layer on GB300.
+
+Headline workload: c4a decode, B=32 sequences of 32768 context tokens, one new token and
+one query per sequence at position 32768. One step = one pass of the layer over the
+batch: insert the new tokens (compressor + window + residual), indexer scores + top-512,
+attention over the selected entries and the 128-token window with inverse RoPE.
+Secondary (reported alongside): chunked prefill of 8192 tokens after 122880 cached ones,
+with prefill attention TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (decode shards by
+sequence; there is no data-path collective); rank 0 prints one JSON line.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import contextlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "c4a decode queries/s + HBM GB/s at B=32x32k; prefill attn TFLOP/s"
+UNIT = "queries/s"
+B, L = 32, 32768
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ algorithmic work
+def decode_bytes_per_query(n_vis: int, k: int, swa: int, D: int = 512, H: int = 64,
+                           H_I: int = 64, d_I: int = 128) -> dict:
+    """Bytes one decode query must move at least (fp8 rows + fp32 row scale)."""
+    parts = {
+        "indexer_keys": n_vis * (d_I + 4),
+        "selected_rows": k * (D + 4),
+        "window_rows": swa * (D + 4),
+        "q_and_out": 2 * H * D * 2,
+        "q_idx_and_w": H_I * d_I * 2 + H_I * 4,
+        "topk_ids": 2 * k * 4,
+        "block_tables": 1024,
+        "insert": 2 * (2 * D + 2 * d_I) * 2 + (D + 4),   # new token in, residual + window out
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def index_bytes_per_query(n_vis: int, k: int, H_I: int = 64, d_I: int = 128) -> int:
+    return n_vis * (d_I + 4) + H_I * d_I * 2 + H_I * 4 + k * 4
+
+
+def attn_flops_per_query(n_keys: int, H: int = 64, D: int = 512) -> float:
+    return 4.0 * H * D * n_keys          # QK^T and PV, 2 flops per multiply-add
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), \
+            d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+# ------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------ oracle arm
+def oracle_sample_step(w, pools, sample):
+    """The oracle's layer step for the sampled sequences: insert their new tokens (the
+    other sequences get none), index + top-k, attention. Returns the queries processed."""
+    from oracle import v4a_oracle as O
+    h = w.layers[0]
+    b, q = w.batch, w.queries
+    sel = np.sort(np.asarray(sample))
+    n_new = np.zeros(len(b.start), np.int64)
+    n_new[sel] = b.cu[sel + 1] - b.cu[sel]
+    cu = np.concatenate([[0], np.cumsum(n_new)])
+    rows = np.concatenate([np.arange(b.cu[i], b.cu[i + 1]) for i in sel])
+    O.compress_insert(h.spec, h.bias, h.gamma, h.ibias, pools, cu, b.start, b.kv[rows],
+                      b.s[rows], b.ik[rows], b.is_[rows])
+    top, _ = O.index_topk(h.spec, pools, q.seq[sel], q.pos[sel], q.q_idx[sel], q.w[sel],
+                          h.spec.top_k)
+    O.attention(h.spec, pools, q.seq[sel], q.pos[sel], q.q[sel], top)
+    return len(sel)
+
+
+def run_oracle(steps: int, warmup: int, n_sample: int, budget_s: float | None):
+    """Time the oracle on host cores; each step is the layer step for n_sample queries."""
+    import workloads as wl
+    from oracle import v4a_oracle as O
+    w = wl.c4a_decode(seed=1, B=B, L=L)
+    h = w.layers[0]
+    pools = O.Pools(h.spec, h.attn, h.idx, h.swa, h.state)
+    rng = np.random.default_rng(0)
+    samples = [rng.choice(B, n_sample, replace=False) for _ in range(steps + warmup)]
+    for s in samples[:warmup]:
+        oracle_sample_step(w, pools, s)
+    t0 = time.perf_counter()
+    done = 0
+    n_steps = 0
+    for s in samples[warmup:]:
+        done += oracle_sample_step(w, pools, s)
+        n_steps += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, dt, n_steps, done
+
+
+def cpu_baseline_subprocess(n_sample: int, budget_s: float) -> dict:
+    """The oracle in a fresh single-threaded process (BLAS pinned to one thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import bench, json; v, dt, n, q = bench.run_oracle(1000, 1, %d, %f); "
+            "print(json.dumps([v, dt, n, q]))" % (n_sample, budget_s))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+    v, dt, n, q = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d layer steps of %d random sequences each (%d queries, %.1f s) of the "
+                      "B=32 L=32768 c4a decode workload: insert + index/top-512 + attention "
+                      "in numpy fp64" % (n, n_sample, q, dt)}
+
+
+def reference_main(args, rank: int):
+    if rank != 0:
+        return
+    n_sample = 2 if args.steps <= 500 else 1
+    v, dt, n, q = run_oracle(args.steps, args.warmup, n_sample, None)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(n, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "c4a decode B=32 L=32768, oracle sample of %d sequences "
+                                   "per step" % n_sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _blas_threads(),
+                             "kind": "oracle",
+                             "sample": "%d random sequences per step (insert + index/top-512 + "
+                                       "attention), %d steps" % (n_sample, n)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _blas_threads() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+# -------------------------------------------------------------------------- GPU arm
+def _dev(x, dt, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dev, dt)
+
+
+class DecodeReplica:
+    """One copy of the decode workload's device state (pools + step inputs/outputs)."""
+
+    def __init__(self, base_layer, w, dev, clone: bool):
+        import torch
+        self.lay = base_layer.clone_pools() if clone else base_layer
+        b, q = w.batch, w.queries
+        bf = torch.bfloat16
+        self.cu = _dev(b.cu, torch.int32, dev)
+        self.start = _dev(b.start, torch.int64, dev)
+        self.kv, self.s = _dev(b.kv, bf, dev), _dev(b.s, bf, dev)
+        self.ik, self.is_ = _dev(b.ik, bf, dev), _dev(b.is_, bf, dev)
+        self.q_seq, self.q_pos = _dev(q.seq, torch.int32, dev), _dev(q.pos, torch.int64, dev)
+        self.q, self.q_idx = _dev(q.q, bf, dev), _dev(q.q_idx, bf, dev)
+        self.w = _dev(q.w, torch.float32, dev)
+        self.max_pos = int(q.pos.max())
+        self.topk = torch.empty((len(q.pos), self.lay.top_k), dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+
+    def step(self):
+        self.lay.compress_insert(self.cu, self.start, self.kv, self.s, self.ik, self.is_)
+        self.lay.index_topk(self.q_seq, self.q_pos, self.max_pos, self.q_idx, self.w, self.topk)
+        self.lay.attention(self.q_seq, self.q_pos, self.max_pos, self.q, self.topk, out=self.out)
+
+    def touched_bytes(self):
+        n_vis = (self.max_pos - 8) // 4 + 1
+        return len(self.q) * decode_bytes_per_query(n_vis, self.lay.top_k, 128)["total"]
+
+
+def gpu_main(args, rank: int, world: int, local_rank: int):
+    import torch
+    import compressed_sparse_long_gb300 as v4a
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    v4a.library()
+    hbm_peak, tf_peak, tf_sus, peak_src = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or getattr(props, "l2_cache_size", 0) or (126 << 20)
+
+    w = wl.c4a_decode(seed=1 + 1000 * rank, B=B, L=L)
+    base = Layer.from_host(w.layers[0], dev)
+    r0 = DecodeReplica(base, w, dev, clone=False)
+    per_step = r0.touched_bytes()
+    n_rep = max(2, int(math.ceil(4.0 * l2 / per_step)))
+    reps = [r0] + [DecodeReplica(base, w, dev, clone=True) for _ in range(n_rep - 1)]
+    stream = torch.cuda.current_stream()
+
+    # warm-up (also allocates the workspaces), then one graph per replica
+    for r in reps:
+        r.step()
+    torch.cuda.synchronize()
+    graphs = []
+    for r in reps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            r.step()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    # compress (1) + indexer scores (1) + top-k (1) + attention (1) + split merge (0/1)
+    split = v4a.v4a_attn_workspace_size(base.cfg, B, L, 512, 0) > 256
+    launches_per_step = 4 + int(split)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # load phase so the clock sampler sees the GPU busy, then the timed region
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.warmup):
+            graphs[i % n_rep].replay()
+        t_end = time.perf_counter() + args.load_s
+        i = 0
+        while time.perf_counter() < t_end:
+            graphs[i % n_rep].replay()
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_rep].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    ms_max = _max_over_ranks(ms, world, dev)
+    queries = world * B * args.steps
+    value = queries / (ms_max / 1e3)
+    ms_per_step = ms_max / args.steps
+    algo_bytes_step = per_step
+    hbm_gbs = algo_bytes_step / (ms_per_step / 1e3) / 1e9
+
+    # per-call timing over the same rotating replicas (the dominant call's roofline)
+    calls = _per_call_times(reps, args.steps, stream)
+    n_vis = (L - 8) // 4 + 1
+    idx_bytes = B * index_bytes_per_query(n_vis, 512)
+    idx_gbs = idx_bytes / (calls["index_topk"] / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, random fp8 cache rows)",
+        "config": {"workload": "c4a decode B=32 L=32768: insert + index/top-512 + attention",
+                   "B": B, "L": L, "H": 64, "D": 512, "d_r": 64, "H_I": 64, "d_I": 128,
+                   "top_k": 512, "swa": 128, "cache": "fp8 e4m3 + fp32 row scale",
+                   "l2": "inputs larger than L2: %d rotating pool replicas, %.1f MB touched per "
+                         "step, %.0f MB L2" % (n_rep, per_step / 1e6, l2 / 2 ** 20),
+                   "launch": "one CUDA graph per replica, replayed"},
+        "hbm_gbs": hbm_gbs,
+        "hbm_frac": hbm_gbs / hbm_peak,
+        "per_call_ms": calls,
+        "roofline": {"kernel": "v4a_index_topk (indexer scores + top-k)", "bound": "hbm",
+                     "achieved": idx_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": idx_gbs / hbm_peak, "traffic": _profile_traffic(),
+                     "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": idx_bytes},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.skip_e2e:
+        line["e2e"] = _e2e(reps[0], w, args.steps, dev, world)
+    if not args.skip_prefill:
+        line["prefill"] = _prefill(dev, tf_peak, tf_sus)
+    if rank == 0 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline_subprocess(2, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _max_over_ranks(ms, world, dev):
+    if world == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _per_call_times(reps, steps, stream):
+    import torch
+    n = len(reps)
+    out = {}
+    for name in ("compress_insert", "index_topk", "attention"):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            r = reps[i % n]
+            ev[i][0].record(stream)
+            if name == "compress_insert":
+                r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_)
+            elif name == "index_topk":
+                r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk)
+            else:
+                r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        out[name] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    return out
+
+
+def _profile_traffic():
+    """DRAM bytes per launch of the dominant call from the committed ncu summary, if that
+    summary still describes the current kernels (it states the library version)."""
+    p = os.path.join(ROOT, "profiles", "index_topk_c4a_decode_B32_L32768.md")
+    if not os.path.exists(p):
+        return None
+    import compressed_sparse_long_gb300 as v4a
+    txt = open(p).read()
+    ver, traffic = None, None
+    for ln in txt.splitlines():
+        if ln.startswith("library_version:"):
+            ver = int(ln.split(":")[1])
+        if ln.startswith("traffic_bytes_per_call:"):
+            traffic = float(ln.split(":")[1])
+    return traffic if ver == v4a.v4a_version() else None
+
+
+def _e2e(r, w, steps, dev, world):
+    """Same step through the public API with host buffers: per step the new tokens and
+    queries go host->device from pinned memory and the output comes back."""
+    import torch
+    b, q = w.batch, w.queries
+    bf = torch.bfloat16
+
+    def pin(x, dt):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dt).pin_memory()
+
+    host_in = [pin(b.kv, bf), pin(b.s, bf), pin(b.ik, bf), pin(b.is_, bf), pin(q.q, bf),
+               pin(q.q_idx, bf), pin(q.w, torch.float32), pin(b.cu, torch.int32),
+               pin(b.start, torch.int64), pin(q.seq, torch.int32), pin(q.pos, torch.int64)]
+    dev_in = [x.to(dev) for x in host_in]
+    host_out = torch.empty(r.out.shape, dtype=bf).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for hsrc, d in zip(host_in, dev_in):
+            d.copy_(hsrc, non_blocking=True)
+        kv, s, ik, is_, qq, qi, ww, cu, st, qs, qp = dev_in
+        r.lay.step(cu, st, kv, s, ik, is_, qs, qp, r.max_pos, qq, qi, ww, out=r.out)
+        host_out.copy_(r.out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return {"value": world * B * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps}
+
+
+def _prefill(dev, tf_peak, tf_sus):
+    """Chunked prefill: 8192 new tokens after 122880 cached; each call timed with events."""
+    import torch
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+    w = wl.c4a_prefill(seed=3)
+    lay = Layer.from_host(w.layers[0], dev)
+    r = DecodeReplica(lay, w, dev, clone=False)
+    r.step()
+    torch.cuda.synchronize()
+    reps = 3
+    t = {}
+    for name in ("compress_insert", "index_topk", "attention"):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            if name == "compress_insert":
+                r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_)
+            elif name == "index_topk":
+                r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk)
+            else:
+                r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out,
+                                prefill=True)
+        e1.record()
+        torch.cuda.synchronize()
+        t[name] = e0.elapsed_time(e1) / reps
+    n_q = len(w.queries.pos)
+    flops = n_q * attn_flops_per_query(512 + 128)
+    pos = w.queries.pos
+    idx_flops = float(sum(((p - 8) // 4 + 1) for p in pos)) * 2 * 64 * 128
+    tot = sum(t.values())
+    return {"workload": "c4a prefill: 122880 cached + 8192-token chunk",
+            "attn_tflops": flops / (t["attention"] / 1e3) / 1e12,
+            "attn_frac_of_bf16_peak": flops / (t["attention"] / 1e3) / 1e12 / tf_peak,
+            "indexer_tflops": idx_flops / (t["index_topk"] / 1e3) / 1e12,
+            "tokens_per_s": n_q / (tot / 1e3), "ms": t,
+            "compress_tokens_per_s": n_q / (t["compress_insert"] / 1e3)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--load-s", type=float, default=1.5, dest="load_s")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, dest="cpu_budget_s")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_main(args, rank)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    gpu_main(args, rank, world, local_rank)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
