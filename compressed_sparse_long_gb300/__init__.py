@@ -72,6 +72,9 @@ _SIGS = {
     "v4a_attn_prefill": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
                                         _P, _P, _SZ, _P, _P]),
     "v4a_slot_mapping": (ctypes.c_int, [_CACHE, _I32, _P, _P, _P, _P, _P]),
+    "v4a_index_topk_noalloc_capacity": (_SZ, []),
+    "v4a_index_topk_noalloc": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _I32,
+                                              _P, _P, _P]),
     "v4a_get_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
 }
 
@@ -157,6 +160,19 @@ def v4a_index_topk(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, k, topk_out, 
         ctypes.byref(cfg), n_q, _ptr(q_seq), _ptr(q_pos), max_pos, _ptr(q_idx), _ptr(w),
         ctypes.byref(idx), k, _ptr(topk_out), _ptr(workspace), ws_bytes, _ptr(dev_err),
         _stream(stream)))
+
+
+def v4a_index_topk_noalloc_capacity() -> int:
+    return library().v4a_index_topk_noalloc_capacity()
+
+
+def v4a_index_topk_noalloc(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, k, topk_out,
+                           dev_err=None, stream=None):
+    """v4a_index_topk for callers that cannot provide or allocate a workspace: the scores
+    go to the library's fixed device scratch (see include/v4a.h for its limit and rules)."""
+    _check("v4a_index_topk_noalloc", library().v4a_index_topk_noalloc(
+        ctypes.byref(cfg), n_q, _ptr(q_seq), _ptr(q_pos), max_pos, _ptr(q_idx), _ptr(w),
+        ctypes.byref(idx), k, _ptr(topk_out), _ptr(dev_err), _stream(stream)))
 
 
 def v4a_attn_workspace_size(cfg, n_q, max_pos, k, prefill) -> int:

@@ -47,6 +47,7 @@ typedef struct CUstream_st* v4a_stream_t; /* a cudaStream_t; NULL = legacy defau
 #define V4A_ERR_UNSUPPORTED (-2)  /* dims / dtype / kind without a kernel */
 #define V4A_ERR_CUDA (-3)         /* a CUDA launch or runtime call failed */
 #define V4A_ERR_DEVICE (-4)       /* v4a_get_error found device-side error bits */
+#define V4A_ERR_TOO_LARGE (-5)    /* the request exceeds the fixed scratch of v4a_index_topk_noalloc */
 
 /* device error word bits */
 #define V4A_DEV_MISSING_PAGE 1u   /* a row the computation needs is in a block with no page */
@@ -153,6 +154,32 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                    const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
                    const v4a_cache* idx, int32_t k, int32_t* topk_out, void* workspace,
                    size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream);
+
+/*
+ * v4a_index_topk_noalloc — v4a_index_topk without a workspace argument, for callers that
+ * cannot allocate device memory and have none to lend: for example a library embedded in
+ * a framework or serving runtime that owns all device memory and gives its kernels no
+ * scratch, or a code path where an allocation would synchronise the device or exceed a
+ * memory budget fixed in advance. The pages have no counterpart to this call; it exists
+ * for such callers only.
+ *
+ * Same arguments, meaning and results as v4a_index_topk, minus workspace and
+ * workspace_bytes. The score rows live in a fixed 8 MiB array inside the library's device
+ * image (held by every GPU that loads the library until the process exits), so
+ * n_q * visible(max_pos) must not exceed v4a_index_topk_noalloc_capacity() floats
+ * (2,097,152; e.g. 64 queries at positions up to 131,072); larger requests return
+ * V4A_ERR_TOO_LARGE without enqueuing anything. The call itself allocates nothing.
+ * The first call on each device looks up the array's device address while that device
+ * is current; make that first call before any stream capture. All calls share the array
+ * and it keeps the previous call's contents (each call writes every score it reads, so no
+ * clearing is needed); calls that overlap on the GPU, e.g. on two unordered streams, race
+ * on it and must be serialised by the caller.
+ */
+size_t v4a_index_topk_noalloc_capacity(void);
+int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                           const int64_t* q_pos, int64_t max_pos, const void* q_idx,
+                           const float* w, const v4a_cache* idx, int32_t k, int32_t* topk_out,
+                           int32_t* dev_err, v4a_stream_t stream);
 
 /*
  * v4a_attn_decode / v4a_attn_prefill — shared-K=V attention with inverse RoPE (a8, a9).
