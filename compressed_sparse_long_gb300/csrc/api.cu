@@ -129,7 +129,7 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
   if (!q_seq || !q_pos || !q_idx || !w || !topk_out) return V4A_ERR_ARG;
   const bool fp8 = cfg->dtype == V4A_BF16_FP8;
   if ((rc = check_cache(idx, kBlock / cfg->stride, cfg->idx_dim, fp8))) return rc;
-  if (!aligned(q_idx, 16)) return V4A_ERR_ARG;
+  if (!aligned(q_idx, 16) || !aligned(w, 16)) return V4A_ERR_ARG;
   const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
   if (max_vis > 0) {
     if (!workspace || !aligned(workspace, 256)) return V4A_ERR_ARG;

@@ -67,7 +67,8 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
   if (n_q < 0 || k <= 0 || max_pos < 0) return V4A_ERR_ARG;
   if (n_q == 0) return V4A_OK;
   if (!q_seq || !q_pos || !q_idx || !w || !topk_out) return V4A_ERR_ARG;
-  if (reinterpret_cast<uintptr_t>(q_idx) % 16 != 0) return V4A_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(q_idx) % 16 != 0 || reinterpret_cast<uintptr_t>(w) % 16 != 0)
+    return V4A_ERR_ARG;
   const bool fp8 = cfg->dtype == V4A_BF16_FP8;
   if (!idx || !idx->data || !idx->block_table || idx->rows_per_block != kBlock / cfg->stride ||
       idx->row_width != cfg->idx_dim || idx->max_blocks <= 0 || idx->n_pages < 0 ||

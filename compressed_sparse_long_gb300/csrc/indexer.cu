@@ -225,7 +225,7 @@ int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaSt
   if (p.n_q == 0 || max_vis == 0) return V4A_OK;
   cudaError_t e;
   if (dtype == V4A_BF16_FP8 && p.H_I == 64 && p.d_I == 128)
-    e = launch_simt<__nv_bfloat16, true, 64, 128>(p, max_vis, st);
+    e = launch_index_scores_tc(p, max_vis, st);
   else if (dtype == V4A_FP32 && p.H_I == 4 && p.d_I == 32)
     e = launch_simt<float, false, 4, 32>(p, max_vis, st);
   else if (dtype == V4A_FP32 && p.H_I == 64 && p.d_I == 128)

@@ -64,6 +64,7 @@ struct AttnParams {
 
 int launch_compress_insert(const CompressParams& p, int dtype, cudaStream_t st);
 int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaStream_t st);
+cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st);
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st);
 int launch_attention(const AttnParams& p, int dtype, cudaStream_t st);
 int launch_slot_mapping(const CacheView& c, int32_t n, const int32_t* seq, const int64_t* row,

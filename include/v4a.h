@@ -55,6 +55,9 @@ typedef struct CUstream_st* v4a_stream_t; /* a cudaStream_t; NULL = legacy defau
 #define V4A_DEV_BAD_INDEX 4u      /* a top-k list names an entry its query may not see */
 #define V4A_DEV_BAD_POS 8u        /* a query position above the max_pos the call was sized for;
                                      the query's rows beyond that bound are ignored */
+#define V4A_DEV_TIMEOUT 16u       /* a bounded wait inside a kernel gave up (about 1 s); the
+                                     kernel drained its copies, released its tensor memory and
+                                     returned; its outputs are incomplete */
 
 /* layer kinds ([notes] 四大核心技术; 数学附录精要) */
 #define V4A_C4A 0                 /* entry = weighted sum of 8 tokens at stride 4 */
