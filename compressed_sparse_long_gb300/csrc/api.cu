@@ -177,10 +177,15 @@ SplitPlan plan_split(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   const int64_t want = (2LL * sms + n_q - 1) / n_q;            // ~2 CTAs per SM
-  const int64_t tile = 32;
+  const int64_t tile = cfg->dtype == V4A_BF16_FP8 ? 128 : 32;   // key tile of the kernel
   int64_t per = (max_keys + want - 1) / want;
   per = ((per + tile - 1) / tile) * tile;
   if (per < tile) per = tile;
+  const int64_t max_splits = 64;                               // the merge handles <= 64
+  if ((max_keys + per - 1) / per > max_splits) {
+    per = (max_keys + max_splits - 1) / max_splits;
+    per = ((per + tile - 1) / tile) * tile;
+  }
   s.keys_per_split = (int32_t)per;
   s.n_split = (int32_t)((max_keys + per - 1) / per);
   return s;

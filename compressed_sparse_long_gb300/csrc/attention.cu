@@ -230,32 +230,45 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
   }
 }
 
-// Combine split partials, normalise, inverse RoPE, store. One CTA per query; thread
-// items are (head, rotation pair).
+// Combine split partials, normalise, inverse RoPE, store. One CTA per (query, head); each
+// thread owns rotation pairs (d, d+1) of that head.
 template <typename OT>
-__global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
-  const int qi = blockIdx.x;
+__global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
+  const int qi = blockIdx.x, h = blockIdx.y;
   const int64_t pos = __ldg(p.q_pos + qi);
   const int H = p.H, D = p.D, tail0 = D - p.rope.d_r;
   OT* out = reinterpret_cast<OT*>(p.out) + (int64_t)qi * H * D;
-  for (int item = threadIdx.x; item < H * D / 2; item += blockDim.x) {
-    const int h = item / (D / 2), d = 2 * (item % (D / 2));
+  __shared__ float s_w[64];
+  __shared__ float s_inv;
+  if (threadIdx.x < 32) {
+    // split weights exp2(m_s - max m), normaliser 1 / sum_s l_s w_s (n_split <= 64)
     float mx = -INFINITY;
-    for (int s = 0; s < p.n_split; ++s)
+    for (int s = threadIdx.x; s < p.n_split; s += 32)
       mx = fmaxf(mx, p.part_ml[(((int64_t)qi * p.n_split + s) * H + h) * 2]);
-    float L = 0.f, a = 0.f, b = 0.f;
-    if (mx != -INFINITY) {
-      for (int s = 0; s < p.n_split; ++s) {
-        const int64_t base = ((int64_t)qi * p.n_split + s) * H + h;
-        const float ms = p.part_ml[base * 2];
-        if (ms == -INFINITY) continue;
-        const float wgt = exp2f(ms - mx);
-        L += p.part_ml[base * 2 + 1] * wgt;
-        a += p.part_o[base * D + d] * wgt;
-        b += p.part_o[base * D + d + 1] * wgt;
-      }
+    mx = warp_max(mx);
+    float L = 0.f;
+    for (int s = threadIdx.x; s < p.n_split; s += 32) {
+      const int64_t base = ((int64_t)qi * p.n_split + s) * H + h;
+      const float ms = p.part_ml[base * 2];
+      const float wgt = (mx == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - mx);
+      s_w[s] = wgt;
+      L += p.part_ml[base * 2 + 1] * wgt;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    L = warp_sum(L);
+    if (threadIdx.x == 0) s_inv = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  for (int d = 2 * threadIdx.x; d < D; d += 2 * blockDim.x) {
+    float a = 0.f, b = 0.f;
+    for (int s = 0; s < p.n_split; ++s) {
+      const float wgt = s_w[s];
+      if (wgt == 0.f) continue;
+      const float2 v = *reinterpret_cast<const float2*>(
+          p.part_o + (((int64_t)qi * p.n_split + s) * H + h) * D + d);
+      a = fmaf(v.x, wgt, a);
+      b = fmaf(v.y, wgt, b);
+    }
+    const float inv = s_inv;
     a *= inv;
     b *= inv;
     if (d >= tail0) {
@@ -279,7 +292,7 @@ cudaError_t launch_simt(const AttnParams& p, cudaStream_t st) {
   attn_simt<QT, kFp8, OT, H, D><<<grid, kThreads, smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split == 1) return e;
-  attn_merge<OT><<<p.n_q, 256, 0, st>>>(p);
+  attn_merge<OT><<<dim3((unsigned)p.n_q, (unsigned)p.H), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -289,7 +302,13 @@ int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
   if (p.n_q == 0) return V4A_OK;
   cudaError_t e;
   if (dtype == V4A_BF16_FP8 && p.H == 64 && p.D == 512)
-    e = launch_simt<__nv_bfloat16, true, __nv_bfloat16, 64, 512>(p, st);
+  {
+    e = launch_attention_tc(p, st);
+    if (e == cudaSuccess && p.n_split > 1) {
+      attn_merge<__nv_bfloat16><<<dim3((unsigned)p.n_q, (unsigned)p.H), 128, 0, st>>>(p);
+      e = cudaGetLastError();
+    }
+  }
   else if (dtype == V4A_FP32 && p.H == 8 && p.D == 128)
     e = launch_simt<float, false, float, 8, 128>(p, st);
   else if (dtype == V4A_FP32 && p.H == 64 && p.D == 512)

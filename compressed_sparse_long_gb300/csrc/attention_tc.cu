@@ -1,0 +1,578 @@
+// Shared-K=V attention on tcgen05 tensor cores (bf16 queries, fp8 e4m3 keys), with the
+// sliding window and inverse RoPE ([notes] "DeepSeek V4 in vLLM 技术博客详尽笔记", Inverse
+// RoPE 的数学原理 and 共享 Key-Value 向量; [blog] 短滑動窗口).
+//
+// Work item: one query (prefill) or one key range of one query (decode split). Keys come
+// in tiles of 128 rows gathered from the paged pools (top-k entries or all visible
+// entries, then the window tokens). Per tile:
+//   S^T = K Q~^T      M = 128 keys, N = 64 heads, K = 512 dims   (32 MMAs, TMEM cols 0..63)
+//   softmax over keys per head: column max with redux.sync.max.f32 across the warp and a
+//     4-warp exchange, column sums with a butterfly reduce-scatter; the running max is
+//     raised only when it grows by more than 2^8 (then the O^T accumulator is rescaled)
+//   O^T += V^T P'^T   M = 128 dims x 4 blocks, N = 64 heads, K = 128 keys (32 MMAs,
+//                     TMEM cols 64..319)
+// K = V: the same shared-memory key tile (fp8 codes converted exactly to bf16, 128-byte
+// swizzle) is read K-major by the first product and MN-major by the second. The fp8 row
+// scale is applied to the logits after S^T and folded into P' = p * scale before the
+// second product, so keys stay exact codes. Q~ = RoPE(q, p) * softmax_scale * log2(e) in
+// bf16; logits are in log2 units.
+//
+// Warps: 0-3 gather + convert keys (each warp its own 32 rows) and build Q~; 4-7 softmax
+// and epilogue (warp w reads TMEM lanes 32(w-4)..); 8 allocates TMEM and issues the MMAs.
+// Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace v4a {
+namespace {
+
+constexpr int kH = 64, kD = 512, kTile = 128;
+constexpr int kThreads = 288;
+constexpr int kKBytes = kTile * kD * 2;        // 128 KB key tile, 8 K-blocks of 16 KB
+constexpr int kQBytes = kH * kD * 2;           // 64 KB Q~, 8 K-blocks of 8 KB
+constexpr int kPBytes = kTile * kH * 2;        // 16 KB P'^T
+constexpr int kOffK = 0, kOffQ = kKBytes, kOffP = kOffQ + kQBytes;
+constexpr int kOffF = kOffP + kPBytes;         // floats: m_run[2][64] l_fin[2][64] red_max[2][256] red_sum[2][256]
+constexpr int kOffBar = kOffF + (128 + 128 + 512 + 512) * 4;
+constexpr int kNBar = 4 + 4 + 12;
+constexpr int kOffMisc = kOffBar + kNBar * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0, kOCol = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+
+struct Item {
+  int qi, split, seq;
+  int64_t pos, n_vis, n_ent, t0, x0, x1;
+  int n_tiles;
+};
+
+__device__ __forceinline__ Item make_item(const AttnParams& p, int it) {
+  Item I;
+  I.qi = it / p.n_split;
+  I.split = it % p.n_split;
+  I.seq = __ldg(p.q_seq + I.qi);
+  I.pos = __ldg(p.q_pos + I.qi);
+  I.n_vis = visible_entries(I.pos, p.S, p.W, p.win_off);
+  I.n_ent = p.topk ? p.k : I.n_vis;
+  I.t0 = I.pos - p.swa_len + 1 > 0 ? I.pos - p.swa_len + 1 : 0;
+  const int64_t n_keys = I.n_ent + (I.pos - I.t0 + 1);
+  I.x0 = (int64_t)I.split * p.keys_per_split;
+  I.x1 = min(n_keys, I.x0 + p.keys_per_split);
+  I.n_tiles = I.x1 > I.x0 ? (int)((I.x1 - I.x0 + kTile - 1) / kTile) : 0;
+  return I;
+}
+
+// Pool row of key x of an item (or -1 when masked), and whether it is a window token.
+__device__ __forceinline__ int64_t key_slot(const AttnParams& p, const Item& I, int64_t x, bool& swa,
+                                            bool report) {
+  swa = false;
+  if (x >= I.x1) return -1;
+  if (x < I.n_ent) {
+    const int64_t j = p.topk ? (int64_t)__ldg(p.topk + (int64_t)I.qi * p.k + x) : x;
+    if (j < 0) return -1;
+    if (j >= I.n_vis) {
+      if (report) raise_err(p.err, V4A_DEV_BAD_INDEX);
+      return -1;
+    }
+    const int64_t s = slot_of(p.attn, I.seq, j);
+    if (s < 0 && report) raise_err(p.err, s == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+    return s < 0 ? -1 : s;
+  }
+  swa = true;
+  const int64_t s = slot_of(p.swa, I.seq, I.t0 + (x - I.n_ent));
+  if (s < 0 && report) raise_err(p.err, s == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+  return s < 0 ? -1 : s;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+      "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+      "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+      "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Sum of v[h] over the 32 lanes, scattered: lane l ends with heads 2l and 2l+1.
+__device__ __forceinline__ float2 reduce_scatter_sum64(const float (&v)[64]) {
+  const int lane = threadIdx.x & 31;
+  float a[32];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float send = up ? v[j] : v[j + 32];
+      const float keep = up ? v[j + 32] : v[j];
+      a[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  float b[16];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float send = up ? a[j] : a[j + 16];
+      const float keep = up ? a[j + 16] : a[j];
+      b[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  float c[8];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float send = up ? b[j] : b[j + 8];
+      const float keep = up ? b[j + 8] : b[j];
+      c[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  float d[4];
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float send = up ? c[j] : c[j + 4];
+      const float keep = up ? c[j + 4] : c[j];
+      d[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+  }
+  float e[2];
+  {
+    const bool up = lane & 1;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = up ? d[j] : d[j + 2];
+      const float keep = up ? d[j + 2] : d[j];
+      e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+  }
+  return make_float2(e[0], e[1]);
+}
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* kbuf = sm + kOffK;
+  uint8_t* qbuf = sm + kOffQ;
+  uint8_t* pbuf = sm + kOffP;
+  float* m_run = reinterpret_cast<float*>(sm + kOffF);   // [2][64] by tile parity
+  float* l_fin = m_run + 128;                             // [2][64] by item parity
+  float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
+  float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* kfull = bars;
+  uint64_t* kempty = bars + 4;
+  uint64_t* qfull = bars + 8;
+  uint64_t* qempty = bars + 9;
+  uint64_t* sfull = bars + 10;
+  uint64_t* pfull = bars + 11;
+  uint64_t* pvdone = bars + 12;
+  uint64_t* ofull = bars + 13;
+  uint64_t* oempty = bars + 14;
+  uint64_t* redb = bars + 15;
+  uint64_t* done = bars + 16;
+  int* misc = reinterpret_cast<int*>(sm + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = misc + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_items = p.n_q * p.n_split;
+
+  if (tid == 0) {
+    for (int b = 0; b < 4; ++b) {
+      tc::mbar_init(kfull + b, 4);
+      tc::mbar_init(kempty + b, 1);
+    }
+    tc::mbar_init(qfull, 4);
+    tc::mbar_init(qempty, 1);
+    tc::mbar_init(sfull, 1);
+    tc::mbar_init(pfull, 4);
+    tc::mbar_init(pvdone, 1);
+    tc::mbar_init(ofull, 1);
+    tc::mbar_init(oempty, 4);
+    tc::mbar_init(redb, 4);
+    tc::mbar_init(done, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ gather / convert
+    int gi = 0, ni = 0;   // global tile / item counters of this CTA
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item I = make_item(p, it);
+      if (I.n_tiles == 0) continue;
+      // Q~ = RoPE(q, p) * scale * log2(e), bf16, K-major 128B-swizzled [64 heads][512]
+      if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      {
+        const int tail0 = kD - p.rope.d_r;
+        float c = 1.f, s = 0.f;
+        if (lane < p.rope.d_r / 2) rope_cs(p.rope, I.pos, lane, c, s);
+        const float qs = p.scale * kLog2e;
+        const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) + (int64_t)I.qi * kH * kD;
+        for (int item = tid; item < kH * (kD / 8); item += 128) {
+          const int h = item / (kD / 8), ch = item % (kD / 8);   // 8 dims per chunk
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + (int64_t)h * kD) + ch);
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+          float f[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = __bfloat162float(e[k]);
+          const int d0 = ch * 8;
+          const bool tail = d0 >= tail0;
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            const int pi = tail ? (d0 + k - tail0) >> 1 : 0;
+            const float cc = __shfl_sync(0xffffffffu, c, pi);
+            const float ss = __shfl_sync(0xffffffffu, s, pi);
+            if (tail) {
+              const float a = f[k], b = f[k + 1];
+              f[k] = a * cc - b * ss;
+              f[k + 1] = a * ss + b * cc;
+            }
+          }
+          uint4 o;
+          o.x = pack_bf16(f[0] * qs, f[1] * qs);
+          o.y = pack_bf16(f[2] * qs, f[3] * qs);
+          o.z = pack_bf16(f[4] * qs, f[5] * qs);
+          o.w = pack_bf16(f[6] * qs, f[7] * qs);
+          *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * 8192 + tc::sw128_off(h, ch & 7)) = o;
+        }
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(qfull);
+      }
+      for (int t = 0; t < I.n_tiles; ++t, ++gi) {
+        // this warp's 32 rows: lane resolves row 32*warp + lane
+        const int64_t x = I.x0 + (int64_t)t * kTile + warp * 32 + lane;
+        bool is_swa;
+        const int64_t slot = key_slot(p, I, x, is_swa, true);
+        const uint8_t* rowp = nullptr;
+        if (slot >= 0) {
+          const CacheView& cv = is_swa ? p.swa : p.attn;
+          rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
+        }
+        for (int b = 0; b < 4; ++b) {
+          if (!tc::mbar_wait(kempty + b, (gi & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+#pragma unroll 2
+          for (int k = 0; k < 8; ++k) {
+            const int rl = 4 * k + (lane >> 3), c = lane & 7;   // row in warp, 16-code chunk
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rowp), rl));
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+            if (src) {
+              const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + b * 128 + c * 16));
+              lo.x = e4m3x2_to_bf16x2(u.x & 0xFFFFu);
+              lo.y = e4m3x2_to_bf16x2(u.x >> 16);
+              lo.z = e4m3x2_to_bf16x2(u.y & 0xFFFFu);
+              lo.w = e4m3x2_to_bf16x2(u.y >> 16);
+              hi.x = e4m3x2_to_bf16x2(u.z & 0xFFFFu);
+              hi.y = e4m3x2_to_bf16x2(u.z >> 16);
+              hi.z = e4m3x2_to_bf16x2(u.w & 0xFFFFu);
+              hi.w = e4m3x2_to_bf16x2(u.w >> 16);
+            }
+            const int r = warp * 32 + rl;
+            const int c0 = 2 * c;                      // bf16 chunk within the 128-dim block
+            const int kb = 2 * b + (c0 >> 3);
+            *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, c0 & 7)) = lo;
+            *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, (c0 + 1) & 7)) = hi;
+          }
+          tc::fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(kfull + b);
+        }
+        if (!ok) break;
+      }
+      ++ni;
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + epilogue
+    // m_run[2][64]: running max by tile parity (written by the head's owner thread, read
+    // by all); the owner of head h (thread row h) also keeps its denominator in a register
+    // and publishes it in l_fin[item parity][64] for the epilogue.
+    const int quad = warp - 4;
+    const int row = quad * 32 + lane;             // TMEM lane: key (S^T) or dim (O^T)
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int gi = 0, ni = 0, ru = 0;
+    bool ok = true;
+    auto group_sync = [&]() -> bool {             // all four softmax warps
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(redb);
+      const bool r = tc::mbar_wait(redb, ru & 1, abort_flag, p.err);
+      ++ru;
+      return r;
+    };
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item I = make_item(p, it);
+      if (I.n_tiles == 0) {
+        if (kSplit) {
+          const int64_t base = ((int64_t)I.qi * p.n_split + I.split) * kH;
+          if (row < kH) {
+            p.part_ml[(base + row) * 2] = -INFINITY;
+            p.part_ml[(base + row) * 2 + 1] = 0.f;
+          }
+        }
+        continue;
+      }
+      float l_reg = 0.f;                          // owner threads (row < 64)
+      if (row < 64) m_run[row] = -INFINITY;       // buffer 0 for tile 0
+      for (int t = 0; t < I.n_tiles; ++t, ++gi) {
+        if (!tc::mbar_wait(sfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
+        tc::fence_after_sync();
+        float s[64];
+        {
+          float a[32];
+          tc::tmem_ld32(tmem + lane_base + kSCol, a);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s[h] = a[h];
+          tc::tmem_ld32(tmem + lane_base + kSCol + 32, a);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s[32 + h] = a[h];
+          tc::tmem_wait_ld();
+        }
+        const int64_t x = I.x0 + (int64_t)t * kTile + row;
+        bool is_swa;
+        const int64_t slot = key_slot(p, I, x, is_swa, false);
+        float sc = 0.f;
+        if (slot >= 0) sc = __ldg((is_swa ? p.swa.scale : p.attn.scale) + slot);
+#pragma unroll
+        for (int h = 0; h < 64; ++h) s[h] = slot >= 0 ? s[h] * sc : -INFINITY;
+        // ---- per-head max over the tile's 128 keys
+        float* rb = red_max + (ru & 1) * 256;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) {
+          const float mh = redux_max(s[h]);
+          if (lane == (h & 31)) rb[h * 4 + quad] = mh;
+        }
+        if (!group_sync()) { ok = false; break; }
+        const float* m_cur = m_run + (t & 1) * 64;
+        float* m_nxt = m_run + ((t + 1) & 1) * 64;
+        float corr[64];
+        bool any_rescale = false;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) {
+          const float4 v = *reinterpret_cast<const float4*>(rb + h * 4);
+          const float mt = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          const float mo = m_cur[h];
+          float mn = mo;
+          corr[h] = 1.f;
+          if (t == 0) {
+            mn = mt;                               // nothing accumulated yet
+          } else if (mt > mo + kRescaleThreshold) {
+            mn = mt;
+            corr[h] = exp2f(mo - mt);              // 0 when mo is -inf
+            any_rescale = true;
+          }
+          s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : exp2f(s[h] - mn);
+          if (row == h) m_nxt[h] = mn;
+        }
+        // ---- per-head sums of p over the tile's keys -> the owners' denominators
+        float* rs = red_sum + (ru & 1) * 256;
+        const float2 part = reduce_scatter_sum64(s);
+        rs[(2 * lane) * 4 + quad] = part.x;
+        rs[(2 * lane + 1) * 4 + quad] = part.y;
+        if (!group_sync()) { ok = false; break; }
+        if (row < 64) {
+          const float4 v = *reinterpret_cast<const float4*>(rs + row * 4);
+          l_reg = l_reg * corr[row] + ((v.x + v.y) + (v.z + v.w));
+        }
+        // ---- the P' buffer and O^T must be free of the previous tile's product
+        if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        if (any_rescale) {
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float o[32];
+              const uint32_t addr = tmem + lane_base + kOCol + b * 64 + half * 32;
+              tc::tmem_ld32(addr, o);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 32; ++h) o[h] *= corr[half * 32 + h];
+              tmem_st32(addr, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        // ---- P'^T row of this key: p * row scale, bf16, MN-major swizzled [128 keys][64 heads]
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v;
+          v.x = pack_bf16(s[8 * c + 0] * sc, s[8 * c + 1] * sc);
+          v.y = pack_bf16(s[8 * c + 2] * sc, s[8 * c + 3] * sc);
+          v.z = pack_bf16(s[8 * c + 4] * sc, s[8 * c + 5] * sc);
+          v.w = pack_bf16(s[8 * c + 6] * sc, s[8 * c + 7] * sc);
+          *reinterpret_cast<uint4*>(pbuf + tc::sw128_off(row, c)) = v;
+        }
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(pfull);
+      }
+      if (!ok) break;
+      // ---- publish the denominators, then read O^T (lanes: dims 128b + row; cols: heads)
+      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg;
+      const float m_final = row < 64 ? m_run[(I.n_tiles & 1) * 64 + row] : 0.f;
+      if (!group_sync()) { ok = false; break; }
+      const float* lden = l_fin + (ni & 1) * 64;
+      if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }
+      tc::fence_after_sync();
+      if (kSplit) {
+        const int64_t base = ((int64_t)I.qi * p.n_split + I.split) * kH;
+        for (int b = 0; b < 4; ++b) {
+          const int d = b * 128 + row;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float o[32];
+            tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + half * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) p.part_o[(base + half * 32 + h) * kD + d] = o[h];
+          }
+        }
+        if (row < 64) {
+          p.part_ml[(base + row) * 2] = m_final;
+          p.part_ml[(base + row) * 2 + 1] = l_reg;
+        }
+      } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)I.qi * kH * kD;
+        const int tail0 = kD - p.rope.d_r;
+        for (int b = 0; b < 4; ++b) {
+          const int d = b * 128 + row;
+          float c = 1.f, sn = 0.f;
+          const bool tail = d >= tail0;
+          if (tail) rope_cs(p.rope, I.pos, (d - tail0) >> 1, c, sn);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float o[32];
+            tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + half * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              const float L = lden[half * 32 + h];
+              float v = L > 0.f ? o[h] / L : 0.f;
+              const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+              if (tail) v = (d & 1) ? (-partner * sn + v * c) : (v * c + partner * sn);
+              out[(int64_t)(half * 32 + h) * kD + d] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(oempty);
+      ++ni;
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer (warp 8)
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16(kTile, kH);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16(128, kH, true, true);
+      const uint32_t k0 = tc::smem_u32(kbuf), q0 = tc::smem_u32(qbuf), p0 = tc::smem_u32(pbuf);
+      int gi = 0, ni = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item I = make_item(p, it);
+        if (I.n_tiles == 0) continue;
+        if (!tc::mbar_wait(qfull, ni & 1, abort_flag, p.err)) break;
+        for (int t = 0; t < I.n_tiles; ++t, ++gi) {
+          // S^T = K Q~^T over the 8 K-blocks, block pair b as soon as it is converted
+          for (int b = 0; b < 4; ++b) {
+            if (!tc::mbar_wait(kfull + b, gi & 1, abort_flag, p.err)) { ok = false; break; }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const int kb = 2 * b + kk;
+#pragma unroll
+              for (int s4 = 0; s4 < 4; ++s4) {
+                const uint64_t ad = tc::sdesc_sw128(k0 + kb * 16384 + s4 * 32, 16, 1024);
+                const uint64_t bd = tc::sdesc_sw128(q0 + kb * 8192 + s4 * 32, 16, 1024);
+                tc::mma_bf16(tmem + kSCol, ad, bd, idesc_qk, (kb | s4) ? 1u : 0u);
+              }
+            }
+          }
+          if (!ok) break;
+          tc::mma_commit(sfull);
+          if (t == I.n_tiles - 1) tc::mma_commit(qempty);
+          if (!tc::mbar_wait(pfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
+          if (t == 0 && ni > 0 && !tc::mbar_wait(oempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+          tc::fence_after_sync();
+          // O^T[dims of block b] += V^T P'^T; V^T is the key tile read MN-major
+          for (int b = 0; b < 4; ++b) {
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) {
+              const uint64_t ad = tc::sdesc_sw128(k0 + (2 * b) * 16384 + s8 * 2048, 16384, 1024);
+              const uint64_t bd = tc::sdesc_sw128(p0 + s8 * 2048, 8192, 1024);
+              tc::mma_bf16(tmem + kOCol + b * 64, ad, bd, idesc_pv, (t > 0 || s8 > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(kempty + b);
+          }
+          tc::mma_commit(pvdone);
+          if (t == I.n_tiles - 1) tc::mma_commit(ofull);
+        }
+        ++ni;
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait_drain(done, 0);
+    }
+    __syncwarp();
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n_items = (int64_t)p.n_q * p.n_split;
+  const int grid = (int)(n_items < sms ? n_items : sms);
+  cudaError_t e;
+  if (p.n_split > 1) {
+    e = cudaFuncSetAttribute(attn_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_tc<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_tc<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace v4a

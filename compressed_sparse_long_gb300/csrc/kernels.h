@@ -67,6 +67,7 @@ int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaSt
 cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st);
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st);
 int launch_attention(const AttnParams& p, int dtype, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st);
 int launch_slot_mapping(const CacheView& c, int32_t n, const int32_t* seq, const int64_t* row,
                         int32_t* slots, int32_t* err, cudaStream_t st);
 
