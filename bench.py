@@ -265,11 +265,14 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or getattr(props, "l2_cache_size", 0) or (126 << 20)
 
+    if args.only == "prefill":          # profiling aid: the prefill chunk alone
+        print(json.dumps({"prefill": _prefill(dev, tf_peak, tf_sus)}), flush=True)
+        return
     w = wl.c4a_decode(seed=1 + 1000 * rank, B=B, L=L)
     base = Layer.from_host(w.layers[0], dev)
     r0 = DecodeReplica(base, w, dev, clone=False)
     per_step = r0.touched_bytes()
-    n_rep = max(2, int(math.ceil(4.0 * l2 / per_step)))
+    n_rep = args.replicas or max(2, int(math.ceil(4.0 * l2 / per_step)))
     reps = [r0] + [DecodeReplica(base, w, dev, clone=True) for _ in range(n_rep - 1)]
     stream = torch.cuda.current_stream()
 
@@ -370,25 +373,33 @@ def _max_over_ranks(ms, world, dev):
 
 
 def _per_call_times(reps, steps, stream):
+    """Device time of each library call: one CUDA graph per (call, replica), replayed
+    round-robin over the replicas, timed with events on the launching stream."""
     import torch
     n = len(reps)
+    calls = {
+        "compress_insert": lambda r: r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_),
+        "index_topk": lambda r: r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk),
+        "attention": lambda r: r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out),
+    }
     out = {}
-    for name in ("compress_insert", "index_topk", "attention"):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
+    for name, fn in calls.items():
+        graphs = []
+        for r in reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(r)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % n].replay()
         torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
         for i in range(steps):
-            r = reps[i % n]
-            ev[i][0].record(stream)
-            if name == "compress_insert":
-                r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_)
-            elif name == "index_topk":
-                r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk)
-            else:
-                r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out)
-            ev[i][1].record(stream)
+            graphs[i % n].replay()
+        e1.record(stream)
         torch.cuda.synchronize()
-        out[name] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        out[name] = e0.elapsed_time(e1) / steps
     return out
 
 
@@ -499,6 +510,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0: enough to exceed 4x L2)")
+    ap.add_argument("--only", choices=["all", "prefill"], default="all")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -1,6 +1,7 @@
 // extern "C" entry points of libv4a: host-side validation, workspace layout, dispatch.
 #include <cmath>
 #include <cstring>
+#include <cstdint>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -13,12 +14,22 @@ constexpr int32_t kVersion = 1;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Turns per position phi_i = theta_i / (2 pi) and psi_i = frac(4096 phi_i), as fp32 hi/lo.
 Rope make_rope(const v4a_layer_cfg* c) {
   Rope r{};
   r.d_r = c->rope_dim;
   r.D = c->head_dim;
-  for (int i = 0; i < c->rope_dim / 2 && i < kMaxRopePairs; ++i)
-    r.theta[i] = std::pow((double)c->rope_base, -2.0 * i / (double)c->rope_dim);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < c->rope_dim / 2 && i < kMaxRopePairs; ++i) {
+    const double theta = std::pow((double)c->rope_base, -2.0 * i / (double)c->rope_dim);
+    const double phi = theta / two_pi;
+    double psi = 4096.0 * phi;
+    psi -= std::floor(psi);
+    r.phi_hi[i] = (float)phi;
+    r.phi_lo[i] = (float)(phi - (double)r.phi_hi[i]);
+    r.psi_hi[i] = (float)psi;
+    r.psi_lo[i] = (float)(psi - (double)r.psi_hi[i]);
+  }
   return r;
 }
 
@@ -44,7 +55,7 @@ int check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8) {
   if (c->rows_per_block != rows_per_block || c->row_width != width) return V4A_ERR_ARG;
   if (c->max_blocks <= 0 || c->n_pages < 0 || c->reserved != 0) return V4A_ERR_ARG;
   if (!aligned(c->data, 16)) return V4A_ERR_ARG;
-  if (fp8 && !c->scale) return V4A_ERR_ARG;
+  if (fp8 && (!c->scale || !aligned(c->scale, 16))) return V4A_ERR_ARG;
   return V4A_OK;
 }
 
@@ -176,16 +187,21 @@ SplitPlan plan_split(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
-  const int64_t want = (2LL * sms + n_q - 1) / n_q;            // ~2 CTAs per SM
+  // Split each query's keys into k ranges (whole key tiles). With one CTA per SM, a choice
+  // costs waves * (tiles per range + 1), the +1 standing for the per-range query setup;
+  // take the smallest k of least cost (the merge handles k <= 64).
   const int64_t tile = cfg->dtype == V4A_BF16_FP8 ? 128 : 32;   // key tile of the kernel
-  int64_t per = (max_keys + want - 1) / want;
-  per = ((per + tile - 1) / tile) * tile;
-  if (per < tile) per = tile;
-  const int64_t max_splits = 64;                               // the merge handles <= 64
-  if ((max_keys + per - 1) / per > max_splits) {
-    per = (max_keys + max_splits - 1) / max_splits;
-    per = ((per + tile - 1) / tile) * tile;
+  const int64_t tiles = (max_keys + tile - 1) / tile;
+  int64_t best_k = 1, best_cost = INT64_MAX;
+  for (int64_t k = 1; k <= tiles && k <= 64; ++k) {
+    const int64_t waves = (n_q * k + sms - 1) / sms;
+    const int64_t cost = waves * ((tiles + k - 1) / k + 1);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best_k = k;
+    }
   }
+  const int64_t per = ((tiles + best_k - 1) / best_k) * tile;
   s.keys_per_split = (int32_t)per;
   s.n_split = (int32_t)((max_keys + per - 1) / per);
   return s;

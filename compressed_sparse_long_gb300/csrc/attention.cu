@@ -230,56 +230,68 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
   }
 }
 
-// Combine split partials, normalise, inverse RoPE, store. One CTA per (query, head); each
-// thread owns rotation pairs (d, d+1) of that head.
-template <typename OT>
-__global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
-  const int qi = blockIdx.x, h = blockIdx.y;
-  const int64_t pos = __ldg(p.q_pos + qi);
+// Combine split partials, normalise, inverse RoPE, store. One warp per (query, head): the
+// lanes first reduce the split maxima and denominators (split s on lane s % 32), then lane
+// l owns the rotation pairs (d, d+1), d = 2l + 64i, of that head; all partial loads of a
+// group of splits are issued before they are used.
+template <typename OT, int kPairs>
+__global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qi = blockIdx.x, h = blockIdx.y * 8 + warp;
+  if (h >= p.H) return;
   const int H = p.H, D = p.D, tail0 = D - p.rope.d_r;
-  OT* out = reinterpret_cast<OT*>(p.out) + (int64_t)qi * H * D;
-  __shared__ float s_w[64];
-  __shared__ float s_inv;
-  if (threadIdx.x < 32) {
-    // split weights exp2(m_s - max m), normaliser 1 / sum_s l_s w_s (n_split <= 64)
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < p.n_split; s += 32)
-      mx = fmaxf(mx, p.part_ml[(((int64_t)qi * p.n_split + s) * H + h) * 2]);
-    mx = warp_max(mx);
-    float L = 0.f;
-    for (int s = threadIdx.x; s < p.n_split; s += 32) {
-      const int64_t base = ((int64_t)qi * p.n_split + s) * H + h;
-      const float ms = p.part_ml[base * 2];
-      const float wgt = (mx == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - mx);
-      s_w[s] = wgt;
-      L += p.part_ml[base * 2 + 1] * wgt;
-    }
-    L = warp_sum(L);
-    if (threadIdx.x == 0) s_inv = L > 0.f ? 1.f / L : 0.f;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int64_t row0 = (int64_t)qi * p.n_split * H + h;          // (qi, split 0, h)
+  float mx = -INFINITY;
+  for (int s = lane; s < p.n_split; s += 32) mx = fmaxf(mx, p.part_ml[(row0 + (int64_t)s * H) * 2]);
+  mx = warp_max(mx);
+  float L = 0.f;
+  for (int s = lane; s < p.n_split; s += 32) {
+    const float ms = p.part_ml[(row0 + (int64_t)s * H) * 2];
+    if (mx != -INFINITY && ms != -INFINITY) L += p.part_ml[(row0 + (int64_t)s * H) * 2 + 1] * exp2f(ms - mx);
   }
-  __syncthreads();
-  for (int d = 2 * threadIdx.x; d < D; d += 2 * blockDim.x) {
-    float a = 0.f, b = 0.f;
-    for (int s = 0; s < p.n_split; ++s) {
-      const float wgt = s_w[s];
-      if (wgt == 0.f) continue;
-      const float2 v = *reinterpret_cast<const float2*>(
-          p.part_o + (((int64_t)qi * p.n_split + s) * H + h) * D + d);
-      a = fmaf(v.x, wgt, a);
-      b = fmaf(v.y, wgt, b);
+  L = warp_sum(L);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float a[kPairs], b[kPairs];
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) a[i] = b[i] = 0.f;
+  for (int s0 = 0; s0 < p.n_split; s0 += 4) {
+    float2 v[4][kPairs];
+    float wg[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u;
+      float ms = -INFINITY;
+      if (s < p.n_split) ms = p.part_ml[(row0 + (int64_t)s * H) * 2];
+      wg[u] = (s < p.n_split && mx != -INFINITY && ms != -INFINITY) ? exp2f(ms - mx) : 0.f;
+      const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i)
+        v[u][i] = s < p.n_split ? *reinterpret_cast<const float2*>(src + 2 * lane + 64 * i)
+                                : make_float2(0.f, 0.f);
     }
-    const float inv = s_inv;
-    a *= inv;
-    b *= inv;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) {
+        a[i] = fmaf(v[u][i].x, wg[u], a[i]);
+        b[i] = fmaf(v[u][i].y, wg[u], b[i]);
+      }
+  }
+  OT* out = reinterpret_cast<OT*>(p.out) + ((int64_t)qi * H + h) * D;
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) {
+    const int d = 2 * lane + 64 * i;
+    float x = a[i] * inv, y = b[i] * inv;
     if (d >= tail0) {
-      float c, s;
-      rope_cs(p.rope, pos, (d - tail0) >> 1, c, s);
-      const float ra = a * c + b * s, rb = -a * s + b * c;
-      a = ra;
-      b = rb;
+      float c, sn;
+      rope_cs(p.rope, pos, (d - tail0) >> 1, c, sn);
+      const float rx = x * c + y * sn, ry = -x * sn + y * c;
+      x = rx;
+      y = ry;
     }
-    out[(int64_t)h * D + d] = Elem<OT>::from_f(a);
-    out[(int64_t)h * D + d + 1] = Elem<OT>::from_f(b);
+    out[d] = Elem<OT>::from_f(x);
+    out[d + 1] = Elem<OT>::from_f(y);
   }
 }
 
@@ -292,7 +304,7 @@ cudaError_t launch_simt(const AttnParams& p, cudaStream_t st) {
   attn_simt<QT, kFp8, OT, H, D><<<grid, kThreads, smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split == 1) return e;
-  attn_merge<OT><<<dim3((unsigned)p.n_q, (unsigned)p.H), 128, 0, st>>>(p);
+  attn_merge<OT, D / 64><<<dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -305,7 +317,7 @@ int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
   {
     e = launch_attention_tc(p, st);
     if (e == cudaSuccess && p.n_split > 1) {
-      attn_merge<__nv_bfloat16><<<dim3((unsigned)p.n_q, (unsigned)p.H), 128, 0, st>>>(p);
+      attn_merge<__nv_bfloat16, 8><<<dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), 256, 0, st>>>(p);
       e = cudaGetLastError();
     }
   }

@@ -17,8 +17,9 @@
 // second product, so keys stay exact codes. Q~ = RoPE(q, p) * softmax_scale * log2(e) in
 // bf16; logits are in log2 units.
 //
-// Warps: 0-3 gather + convert keys (each warp its own 32 rows) and build Q~; 4-7 softmax
-// and epilogue (warp w reads TMEM lanes 32(w-4)..); 8 allocates TMEM and issues the MMAs.
+// Warpgroups (setmaxnreg splits the registers): 0 = softmax and epilogue (warp w reads
+// TMEM lanes 32w..32w+31), 1-2 = eight gather/convert warps that also build Q~,
+// 3 = warp 12 allocates TMEM and issues the MMAs (warps 13-15 idle).
 // Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
 #include "common.cuh"
 #include "kernels.h"
@@ -28,14 +29,14 @@ namespace v4a {
 namespace {
 
 constexpr int kH = 64, kD = 512, kTile = 128;
-constexpr int kThreads = 288;
+constexpr int kThreads = 512;                 // 4 warpgroups
 constexpr int kKBytes = kTile * kD * 2;        // 128 KB key tile, 8 K-blocks of 16 KB
 constexpr int kQBytes = kH * kD * 2;           // 64 KB Q~, 8 K-blocks of 8 KB
 constexpr int kPBytes = kTile * kH * 2;        // 16 KB P'^T
 constexpr int kOffK = 0, kOffQ = kKBytes, kOffP = kOffQ + kQBytes;
 constexpr int kOffF = kOffP + kPBytes;         // floats: m_run[2][64] l_fin[2][64] red_max[2][256] red_sum[2][256]
-constexpr int kOffBar = kOffF + (128 + 128 + 512 + 512) * 4;
-constexpr int kNBar = 4 + 4 + 12;
+constexpr int kOffBar = kOffF + (128 + 128 + 512 + 512 + 256) * 4;
+constexpr int kNBar = 4 + 4 + 13;
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -90,6 +91,13 @@ __device__ __forceinline__ int64_t key_slot(const AttnParams& p, const Item& I, 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; the result is rounded to bf16).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 __device__ __forceinline__ float redux_max(float v) {
@@ -178,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   float* l_fin = m_run + 128;                             // [2][64] by item parity
   float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
   float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
+  float* sscale = red_sum + 512;                          // [2][128] row scales by tile parity
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = bars + 4;
@@ -190,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   uint64_t* oempty = bars + 14;
   uint64_t* redb = bars + 15;
   uint64_t* done = bars + 16;
+  uint64_t* scfull = bars + 17;
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
@@ -199,10 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 
   if (tid == 0) {
     for (int b = 0; b < 4; ++b) {
-      tc::mbar_init(kfull + b, 4);
+      tc::mbar_init(kfull + b, 8);
       tc::mbar_init(kempty + b, 1);
     }
-    tc::mbar_init(qfull, 4);
+    tc::mbar_init(qfull, 8);
     tc::mbar_init(qempty, 1);
     tc::mbar_init(sfull, 1);
     tc::mbar_init(pfull, 4);
@@ -211,10 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     tc::mbar_init(oempty, 4);
     tc::mbar_init(redb, 4);
     tc::mbar_init(done, 1);
+    tc::mbar_init(scfull, 8);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -223,13 +234,45 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp >= 4 && warp < 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 128;");
     // ------------------------------------------------------------ gather / convert
+    // Eight warps; warp cw owns key rows 16cw .. 16cw+15 of every tile (lanes 0-15 resolve
+    // them and publish their row scales). A lane holds 16 x 16 fp8 codes of a tile in
+    // registers: for block b (128 dims) and j = 0..3, row 16cw + 4j + lane/8, codes
+    // 128b + 16(lane%8) .. +15 (each warp load covers four 128-byte row segments). The
+    // next tile's loads are issued as soon as the current tile is converted, so they are
+    // in flight during the current tile's products and softmax.
+    const int cw = warp - 4;
     int gi = 0, ni = 0;   // global tile / item counters of this CTA
     bool ok = true;
+    uint4 d[4][4];        // [block][j]
+    float sc_row = 0.f;   // scale of row 16cw + lane (lanes < 16)
+    auto issue = [&](const Item& I, int t) {
+      const int64_t x = I.x0 + (int64_t)t * kTile + cw * 16 + (lane & 15);
+      bool is_swa;
+      const int64_t slot = key_slot(p, I, x, is_swa, lane < 16);
+      const uint8_t* rowp = nullptr;
+      sc_row = 0.f;
+      if (slot >= 0) {
+        const CacheView& cv = is_swa ? p.swa : p.attn;
+        rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
+        sc_row = __ldg(cv.scale + slot);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rowp), 4 * j + (lane >> 3)));
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          d[b][j] = src ? __ldg(reinterpret_cast<const uint4*>(src + b * 128 + (lane & 7) * 16))
+                        : make_uint4(0, 0, 0, 0);
+      }
+    };
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = make_item(p, it);
       if (I.n_tiles == 0) continue;
+      issue(I, 0);                                  // tile 0 of the item in flight
       // Q~ = RoPE(q, p) * scale * log2(e), bf16, K-major 128B-swizzled [64 heads][512]
       if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
       {
@@ -237,69 +280,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         float c = 1.f, s = 0.f;
         if (lane < p.rope.d_r / 2) rope_cs(p.rope, I.pos, lane, c, s);
         const float qs = p.scale * kLog2e;
-        const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) + (int64_t)I.qi * kH * kD;
-        for (int item = tid; item < kH * (kD / 8); item += 128) {
-          const int h = item / (kD / 8), ch = item % (kD / 8);   // 8 dims per chunk
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + (int64_t)h * kD) + ch);
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
-          float f[8];
+        const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                                        (int64_t)I.qi * kH * kD);
+        const int ct = cw * 32 + lane;              // 0..255
+#pragma unroll 1
+        for (int base = 0; base < kH * (kD / 8); base += 256 * 8) {
+          uint4 u[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] = __bfloat162float(e[k]);
-          const int d0 = ch * 8;
-          const bool tail = d0 >= tail0;
+          for (int k = 0; k < 8; ++k) u[k] = __ldg(q + base + k * 256 + ct);
 #pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            const int pi = tail ? (d0 + k - tail0) >> 1 : 0;
-            const float cc = __shfl_sync(0xffffffffu, c, pi);
-            const float ss = __shfl_sync(0xffffffffu, s, pi);
-            if (tail) {
-              const float a = f[k], b = f[k + 1];
-              f[k] = a * cc - b * ss;
-              f[k + 1] = a * ss + b * cc;
+          for (int k = 0; k < 8; ++k) {
+            const int item = base + k * 256 + ct;
+            const int h = item / (kD / 8), ch = item % (kD / 8);   // 8 dims per chunk
+            const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u[k]);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+            const int d0 = ch * 8;
+            const bool tail = d0 >= tail0;
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              const int pi = tail ? (d0 + j - tail0) >> 1 : 0;
+              const float cc = __shfl_sync(0xffffffffu, c, pi);
+              const float ss = __shfl_sync(0xffffffffu, s, pi);
+              if (tail) {
+                const float a0 = f[j], a1 = f[j + 1];
+                f[j] = a0 * cc - a1 * ss;
+                f[j + 1] = a0 * ss + a1 * cc;
+              }
             }
+            uint4 o;
+            o.x = pack_bf16(f[0] * qs, f[1] * qs);
+            o.y = pack_bf16(f[2] * qs, f[3] * qs);
+            o.z = pack_bf16(f[4] * qs, f[5] * qs);
+            o.w = pack_bf16(f[6] * qs, f[7] * qs);
+            *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * 8192 + tc::sw128_off(h, ch & 7)) = o;
           }
-          uint4 o;
-          o.x = pack_bf16(f[0] * qs, f[1] * qs);
-          o.y = pack_bf16(f[2] * qs, f[3] * qs);
-          o.z = pack_bf16(f[4] * qs, f[5] * qs);
-          o.w = pack_bf16(f[6] * qs, f[7] * qs);
-          *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * 8192 + tc::sw128_off(h, ch & 7)) = o;
         }
         tc::fence_proxy_async();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(qfull);
       }
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
-        // this warp's 32 rows: lane resolves row 32*warp + lane
-        const int64_t x = I.x0 + (int64_t)t * kTile + warp * 32 + lane;
-        bool is_swa;
-        const int64_t slot = key_slot(p, I, x, is_swa, true);
-        const uint8_t* rowp = nullptr;
-        if (slot >= 0) {
-          const CacheView& cv = is_swa ? p.swa : p.attn;
-          rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
-        }
         for (int b = 0; b < 4; ++b) {
           if (!tc::mbar_wait(kempty + b, (gi & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
-#pragma unroll 2
-          for (int k = 0; k < 8; ++k) {
-            const int rl = 4 * k + (lane >> 3), c = lane & 7;   // row in warp, 16-code chunk
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rowp), rl));
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (src) {
-              const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + b * 128 + c * 16));
-              lo.x = e4m3x2_to_bf16x2(u.x & 0xFFFFu);
-              lo.y = e4m3x2_to_bf16x2(u.x >> 16);
-              lo.z = e4m3x2_to_bf16x2(u.y & 0xFFFFu);
-              lo.w = e4m3x2_to_bf16x2(u.y >> 16);
-              hi.x = e4m3x2_to_bf16x2(u.z & 0xFFFFu);
-              hi.y = e4m3x2_to_bf16x2(u.z >> 16);
-              hi.z = e4m3x2_to_bf16x2(u.w & 0xFFFFu);
-              hi.w = e4m3x2_to_bf16x2(u.w >> 16);
-            }
-            const int r = warp * 32 + rl;
-            const int c0 = 2 * c;                      // bf16 chunk within the 128-dim block
+          if (b == 0) {
+            // row scales for the softmax warps; the previous tile's product is done, so the
+            // softmax warps have consumed the previous hand-off
+            if (lane < 16) sscale[(gi & 1) * kTile + cw * 16 + lane] = sc_row;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(scfull);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 u = d[b][j];
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_bf16x2(u.x & 0xFFFFu);
+            lo.y = e4m3x2_to_bf16x2(u.x >> 16);
+            lo.z = e4m3x2_to_bf16x2(u.y & 0xFFFFu);
+            lo.w = e4m3x2_to_bf16x2(u.y >> 16);
+            hi.x = e4m3x2_to_bf16x2(u.z & 0xFFFFu);
+            hi.y = e4m3x2_to_bf16x2(u.z >> 16);
+            hi.z = e4m3x2_to_bf16x2(u.w & 0xFFFFu);
+            hi.w = e4m3x2_to_bf16x2(u.w >> 16);
+            const int r = cw * 16 + 4 * j + (lane >> 3);
+            const int c0 = 2 * (lane & 7);               // bf16 chunk within the 128-dim block
             const int kb = 2 * b + (c0 >> 3);
             *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, c0 & 7)) = lo;
             *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, (c0 + 1) & 7)) = hi;
@@ -309,15 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           if (lane == 0) tc::mbar_arrive(kfull + b);
         }
         if (!ok) break;
+        if (t + 1 < I.n_tiles) issue(I, t + 1);     // next tile in flight during this one
       }
       ++ni;
     }
-  } else if (warp < 8) {
+  } else if (warp < 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
     // ------------------------------------------------------------ softmax + epilogue
     // m_run[2][64]: running max by tile parity (written by the head's owner thread, read
     // by all); the owner of head h (thread row h) also keeps its denominator in a register
     // and publishes it in l_fin[item parity][64] for the epilogue.
-    const int quad = warp - 4;
+    const int quad = warp;
     const int row = quad * 32 + lane;             // TMEM lane: key (S^T) or dim (O^T)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int gi = 0, ni = 0, ru = 0;
@@ -357,13 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           for (int h = 0; h < 32; ++h) s[32 + h] = a[h];
           tc::tmem_wait_ld();
         }
-        const int64_t x = I.x0 + (int64_t)t * kTile + row;
-        bool is_swa;
-        const int64_t slot = key_slot(p, I, x, is_swa, false);
-        float sc = 0.f;
-        if (slot >= 0) sc = __ldg((is_swa ? p.swa.scale : p.attn.scale) + slot);
+        if (!tc::mbar_wait(scfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
+        const float sc = sscale[(gi & 1) * kTile + row];   // 0 for a masked key
 #pragma unroll
-        for (int h = 0; h < 64; ++h) s[h] = slot >= 0 ? s[h] * sc : -INFINITY;
+        for (int h = 0; h < 64; ++h) s[h] = sc > 0.f ? s[h] * sc : -INFINITY;
         // ---- per-head max over the tile's 128 keys
         float* rb = red_max + (ru & 1) * 256;
 #pragma unroll
@@ -374,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         if (!group_sync()) { ok = false; break; }
         const float* m_cur = m_run + (t & 1) * 64;
         float* m_nxt = m_run + ((t + 1) & 1) * 64;
-        float corr[64];
+        // new running max (raised only past the threshold); the correction factor of head h
+        // is exp2(m_cur[h] - m_nxt[h]), read back from shared memory where needed
         bool any_rescale = false;
 #pragma unroll
         for (int h = 0; h < 64; ++h) {
@@ -382,26 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           const float mt = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
           const float mo = m_cur[h];
           float mn = mo;
-          corr[h] = 1.f;
           if (t == 0) {
             mn = mt;                               // nothing accumulated yet
           } else if (mt > mo + kRescaleThreshold) {
             mn = mt;
-            corr[h] = exp2f(mo - mt);              // 0 when mo is -inf
             any_rescale = true;
           }
-          s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : exp2f(s[h] - mn);
+          s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
           if (row == h) m_nxt[h] = mn;
-        }
-        // ---- per-head sums of p over the tile's keys -> the owners' denominators
-        float* rs = red_sum + (ru & 1) * 256;
-        const float2 part = reduce_scatter_sum64(s);
-        rs[(2 * lane) * 4 + quad] = part.x;
-        rs[(2 * lane + 1) * 4 + quad] = part.y;
-        if (!group_sync()) { ok = false; break; }
-        if (row < 64) {
-          const float4 v = *reinterpret_cast<const float4*>(rs + row * 4);
-          l_reg = l_reg * corr[row] + ((v.x + v.y) + (v.z + v.w));
         }
         // ---- the P' buffer and O^T must be free of the previous tile's product
         if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
@@ -416,7 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
               tc::tmem_ld32(addr, o);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; ++h) o[h] *= corr[half * 32 + h];
+              for (int h = 0; h < 32; ++h) {
+                const int hh = half * 32 + h;
+                const float mo = m_cur[hh], mn = m_nxt[hh];
+                o[h] *= mo == mn ? 1.f : fast_exp2(mo - mn);
+              }
               tmem_st32(addr, o);
             }
           }
@@ -436,6 +473,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(pfull);
+        // ---- per-head sums of p over the tile's keys -> the owners' denominators (these
+        // overlap the P'V product, which only needs P')
+        float* rs = red_sum + (ru & 1) * 256;
+        const float2 part = reduce_scatter_sum64(s);
+        rs[(2 * lane) * 4 + quad] = part.x;
+        rs[(2 * lane + 1) * 4 + quad] = part.y;
+        if (!group_sync()) { ok = false; break; }
+        if (row < 64) {
+          const float4 v = *reinterpret_cast<const float4*>(rs + row * 4);
+          const float cr = t == 0 ? 1.f : fast_exp2(m_cur[row] - m_nxt[row]);   // 0 if m_cur = -inf
+          l_reg = l_reg * cr + ((v.x + v.y) + (v.z + v.w));
+        }
       }
       if (!ok) break;
       // ---- publish the denominators, then read O^T (lanes: dims 128b + row; cols: heads)
@@ -492,11 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       ++ni;
     }
   } else {
-    // ------------------------------------------------------------ MMA issuer (warp 8)
-    if (lane == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    // ------------------------------------------------------------ MMA issuer (warp 12)
+    if (warp == 12 && lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kTile, kH);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, kH, true, true);
       const uint32_t k0 = tc::smem_u32(kbuf), q0 = tc::smem_u32(qbuf), p0 = tc::smem_u32(pbuf);
+      const uint64_t dk_k = tc::sdesc_sw128(k0, 16, 1024);        // key tile, K-major
+      const uint64_t dq_k = tc::sdesc_sw128(q0, 16, 1024);        // Q~, K-major
+      const uint64_t dk_mn = tc::sdesc_sw128(k0, 16384, 1024);    // key tile as V^T, MN-major
+      const uint64_t dp_mn = tc::sdesc_sw128(p0, 8192, 1024);     // P'^T, MN-major
       int gi = 0, ni = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -513,8 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
               const int kb = 2 * b + kk;
 #pragma unroll
               for (int s4 = 0; s4 < 4; ++s4) {
-                const uint64_t ad = tc::sdesc_sw128(k0 + kb * 16384 + s4 * 32, 16, 1024);
-                const uint64_t bd = tc::sdesc_sw128(q0 + kb * 8192 + s4 * 32, 16, 1024);
+                // descriptor start address field counts 16-byte units
+                const uint64_t ad = dk_k + (uint64_t)((kb * 16384 + s4 * 32) >> 4);
+                const uint64_t bd = dq_k + (uint64_t)((kb * 8192 + s4 * 32) >> 4);
                 tc::mma_bf16(tmem + kSCol, ad, bd, idesc_qk, (kb | s4) ? 1u : 0u);
               }
             }
@@ -529,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           for (int b = 0; b < 4; ++b) {
 #pragma unroll
             for (int s8 = 0; s8 < 8; ++s8) {
-              const uint64_t ad = tc::sdesc_sw128(k0 + (2 * b) * 16384 + s8 * 2048, 16384, 1024);
-              const uint64_t bd = tc::sdesc_sw128(p0 + s8 * 2048, 8192, 1024);
+              const uint64_t ad = dk_mn + (uint64_t)(((2 * b) * 16384 + s8 * 2048) >> 4);
+              const uint64_t bd = dp_mn + (uint64_t)((s8 * 2048) >> 4);
               tc::mma_bf16(tmem + kOCol + b * 64, ad, bd, idesc_pv, (t > 0 || s8 > 0) ? 1u : 0u);
             }
             tc::mma_commit(kempty + b);
@@ -548,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }

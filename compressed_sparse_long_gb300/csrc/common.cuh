@@ -63,24 +63,32 @@ __device__ __forceinline__ bool slot_ok(int64_t s, int32_t* err) {
   return false;
 }
 
-// RoPE frequencies theta_i = base^(-2i/d_r), computed on the host in double.
+// RoPE frequencies theta_i = base^(-2i/d_r), kept as turns per position
+// phi_i = theta_i / (2 pi) and psi_i = frac(4096 phi_i), each split into fp32 hi + lo parts
+// on the host (in double). The device never uses fp64.
 struct Rope {
   int32_t d_r;
   int32_t D;
-  double theta[kMaxRopePairs];
+  float phi_hi[kMaxRopePairs], phi_lo[kMaxRopePairs];
+  float psi_hi[kMaxRopePairs], psi_lo[kMaxRopePairs];
 };
 
-// cos/sin of pos * theta_i. The angle is formed in double and reduced modulo 2*pi with a
-// two-constant Cody-Waite step (2*pi = hi + lo), so positions up to 2^31 keep ~1e-10 rad;
-// the reduced angle (|r| <= pi) then goes through fp32 sincosf.
+// Fractional part of x * (yh + yl), x an integer below 2^24: x*yh = p + e exactly (fma),
+// p - rint(p) is exact, the remaining terms are tiny.
+__device__ __forceinline__ float frac_prod(float x, float yh, float yl) {
+  const float p = x * yh;
+  const float e = fmaf(x, yh, -p);
+  return (p - rintf(p)) + (e + x * yl);
+}
+
+// cos/sin of pos * theta_i. With pos = hi * 4096 + lo the angle in turns is
+// frac(hi * psi_i + lo * phi_i), reduced exactly in fp32 (error ~1e-7 turn for positions up
+// to 2^31); sincospif then evaluates the reduced angle.
 __device__ __forceinline__ void rope_cs(const Rope& rp, int64_t pos, int i, float& c, float& s) {
-  const double two_pi_hi = 6.283185307179586;
-  const double two_pi_lo = 2.4492935982947064e-16;
-  double a = (double)pos * rp.theta[i];
-  double n = rint(a * (1.0 / two_pi_hi));
-  double r = fma(-n, two_pi_hi, a);
-  r = fma(-n, two_pi_lo, r);
-  sincosf((float)r, &s, &c);
+  const float hi = (float)(pos >> 12), lo = (float)(pos & 4095);
+  float a = frac_prod(hi, rp.psi_hi[i], rp.psi_lo[i]) + frac_prod(lo, rp.phi_hi[i], rp.phi_lo[i]);
+  a -= rintf(a);
+  sincospif(2.0f * a, &s, &c);
 }
 
 // ---------------------------------------------------------------- warp reductions

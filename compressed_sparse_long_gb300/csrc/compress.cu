@@ -100,13 +100,16 @@ struct CompressKernel {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (i >= p.n_tokens) return;
 
-    // sequence of row i: the largest b with cu[b] <= i
-    int lo = 0, hi = p.n_seq - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.cu + mid) <= i) lo = mid; else hi = mid - 1;
+    // sequence of row i: the largest b with cu[b] <= i, 32 candidates per warp load
+    int b = -1;
+    for (int base = 0; base < p.n_seq && b < 0; base += 32) {
+      const int k = base + lane;
+      const bool le = k < p.n_seq && __ldg(p.cu + k) <= i;
+      const bool nxt_le = k + 1 < p.n_seq && __ldg(p.cu + k + 1) <= i;
+      const uint32_t hit = __ballot_sync(0xffffffffu, le && !nxt_le);
+      if (hit) b = base + __ffs(hit) - 1;
     }
-    const int b = lo;
+    if (b < 0) return;
     const int64_t row0 = __ldg(p.cu + b);
     const int64_t n_new = __ldg(p.cu + b + 1) - row0;
     const int64_t P0 = __ldg(p.start + b);
@@ -114,8 +117,17 @@ struct CompressKernel {
     const int64_t t = P0 + (i - row0);
 
     const TIn* kv_t = reinterpret_cast<const TIn*>(p.kv) + i * D;
-    float x[CPL];
+    float x[CPL], sv_t[CPL];
+    float ik_t[ICPL > 0 ? ICPL : 1], is_t[ICPL > 0 ? ICPL : 1];
+    const bool keep_state = t >= P1 - p.W;
     load_f<TIn, CPL>(kv_t + lane * CPL, x);
+    if (keep_state) {
+      load_f<TIn, CPL>(reinterpret_cast<const TIn*>(p.score) + i * D + lane * CPL, sv_t);
+      if constexpr (ICPL > 0) {
+        load_f<TIn, ICPL>(reinterpret_cast<const TIn*>(p.ikv) + i * DI + lane * ICPL, ik_t);
+        load_f<TIn, ICPL>(reinterpret_cast<const TIn*>(p.iscore) + i * DI + lane * ICPL, is_t);
+      }
+    }
 
     // (1) sliding-window row: RoPE(kv_t, t)
     {
@@ -132,20 +144,15 @@ struct CompressKernel {
     }
 
     // (2) raw residual row for the last W new positions
-    if (t >= P1 - p.W) {
+    if (keep_state) {
       int64_t s = slot_of(p.state, b, t);
       if (s >= 0) {
         TIn* dst = reinterpret_cast<TIn*>(p.state.data) + s * (int64_t)p.state.width;
-        float v[CPL];
         store_f<TIn, CPL>(dst + lane * CPL, x);
-        load_f<TIn, CPL>(reinterpret_cast<const TIn*>(p.score) + i * D + lane * CPL, v);
-        store_f<TIn, CPL>(dst + D + lane * CPL, v);
+        store_f<TIn, CPL>(dst + D + lane * CPL, sv_t);
         if constexpr (ICPL > 0) {
-          float u[ICPL];
-          load_f<TIn, ICPL>(reinterpret_cast<const TIn*>(p.ikv) + i * DI + lane * ICPL, u);
-          store_f<TIn, ICPL>(dst + 2 * D + lane * ICPL, u);
-          load_f<TIn, ICPL>(reinterpret_cast<const TIn*>(p.iscore) + i * DI + lane * ICPL, u);
-          store_f<TIn, ICPL>(dst + 2 * D + DI + lane * ICPL, u);
+          store_f<TIn, ICPL>(dst + 2 * D + lane * ICPL, ik_t);
+          store_f<TIn, ICPL>(dst + 2 * D + DI + lane * ICPL, is_t);
         }
       } else if (s == -2) {
         raise_err(p.err, V4A_DEV_BAD_PAGE);
@@ -169,6 +176,7 @@ struct CompressKernel {
 #pragma unroll
     for (int k = 0; k < (ICPL > 0 ? ICPL : 1); ++k) { im[k] = -INFINITY; il[k] = 0.f; iacc[k] = 0.f; }
 
+#pragma unroll 8
     for (int o = 0; o < p.W; ++o) {
       const int64_t pos = j * p.S + p.win_off + o;
       if (pos < 0) continue;                       // before the sequence: absent

@@ -73,7 +73,7 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
   if (!idx || !idx->data || !idx->block_table || idx->rows_per_block != kBlock / cfg->stride ||
       idx->row_width != cfg->idx_dim || idx->max_blocks <= 0 || idx->n_pages < 0 ||
       idx->reserved != 0 || reinterpret_cast<uintptr_t>(idx->data) % 16 != 0 ||
-      (fp8 && !idx->scale))
+      (fp8 && (!idx->scale || reinterpret_cast<uintptr_t>(idx->scale) % 16 != 0)))
     return V4A_ERR_ARG;
   const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
   if ((uint64_t)n_q * (uint64_t)max_vis > kNoallocScoreFloats) return V4A_ERR_TOO_LARGE;

@@ -10,7 +10,7 @@
 // scale is positive, so sum_h w_h ReLU(q_h . (c*k)) = c * sum_h w_h ReLU(q_h . k).
 //
 // Top-k: MSB-first radix select on the order-preserving uint32 image of the fp32 scores
-// (4 passes of 8-bit digits, warp-aggregated shared-memory histograms) finds the k-th
+// (4 passes of 8-bit digits, per-warp shared-memory histograms) finds the k-th
 // largest key; an ordered block compaction then emits every entry above it plus the
 // lowest-index entries equal to it, in ascending index order.
 #include "common.cuh"
@@ -84,29 +84,34 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkSmemMax = 49152;   // rows up to this length are staged in shared memory
 
-// Exclusive block-wide prefix count of `flag`; returns the tile total through *total.
-__device__ __forceinline__ uint32_t block_excl_count(bool flag, uint32_t* warp_tot, uint32_t* total) {
+// Exclusive block-wide prefix sum of one value per thread; the total through *total.
+__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-  const uint32_t in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[warp] = __popc(bal);
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    uint32_t v = lane < (kTopkThreads / 32) ? warp_tot[lane] : 0u;
-    uint32_t incl = v;
+    const uint32_t w = lane < (kTopkThreads / 32) ? warp_tot[lane] : 0u;
+    uint32_t z = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+      const uint32_t y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
     }
-    warp_tot[lane] = incl - v;              // exclusive offset of each warp
-    if (lane == 31) *total = incl;
+    warp_tot[lane] = z - w;
+    if (lane == 31) *total = z;
   }
   __syncthreads();
-  const uint32_t r = warp_tot[warp] + in_warp;
+  const uint32_t r = warp_tot[warp] + incl - v;
   __syncthreads();
   return r;
 }
@@ -115,6 +120,7 @@ template <bool kSmem>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ IndexParams p) {
   extern __shared__ uint32_t row_keys[];
   __shared__ uint32_t hist[256];
+  __shared__ uint32_t whist[kTopkWarps][256];   // per-warp histograms (no cross-warp contention)
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t s_digit, s_remaining, s_total;
   const int qi = blockIdx.x;
@@ -139,22 +145,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    uint32_t* my = whist[tid >> 5];
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&whist[0][0])[i] = 0;
     __syncthreads();
-    for (int64_t base = 0; base < n; base += kTopkThreads) {
-      const int64_t i = base + tid;
-      bool take = false;
-      uint32_t bin = 0;
-      if (i < n) {
-        const uint32_t u = key_at(i);
-        take = (u & mask) == prefix;
-        bin = (u >> shift) & 0xFFu;
-      }
-      const uint32_t act = __ballot_sync(0xffffffffu, take);
-      if (take) {
-        const uint32_t same = __match_any_sync(act, bin);
-        if ((threadIdx.x & 31) == (__ffs(same) - 1)) atomicAdd(&hist[bin], __popc(same));
-      }
+    for (int64_t i = tid; i < n; i += kTopkThreads) {
+      const uint32_t u = key_at(i);
+      if ((u & mask) == prefix) atomicAdd(&my[(u >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += kTopkThreads) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) t += whist[w][b];
+      hist[b] = t;
     }
     __syncthreads();
     if (tid < 32) {
@@ -191,25 +194,30 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   }
 
   // prefix is the key of the k-th largest score; take all keys above it and the first
-  // `remaining` keys equal to it, in index order.
+  // `remaining` keys equal to it, in index order. Thread t owns the contiguous chunk
+  // [t*C, (t+1)*C): one block scan of its (ties, above) counts gives where its selected
+  // entries go, and it writes them in order.
   const uint32_t kth = prefix;
-  uint32_t ties_before = 0, written = 0;
-  for (int64_t base = 0; base < n; base += kTopkThreads) {
-    const int64_t i = base + tid;
-    const uint32_t u = i < n ? key_at(i) : 0u;
-    const bool eq = i < n && u == kth;
-    const bool gt = i < n && u > kth;
-    const uint32_t tie_rank = ties_before + block_excl_count(eq, warp_tot, &s_total);
-    const uint32_t tie_tile = s_total;
-    const bool sel = gt || (eq && tie_rank < remaining);
-    const uint32_t at = written + block_excl_count(sel, warp_tot, &s_total);
-    const uint32_t sel_tile = s_total;
-    if (sel && at < (uint32_t)p.k) out[at] = (int32_t)i;
-    ties_before += tie_tile;
-    written += sel_tile;
-    __syncthreads();
+  const int64_t C = (n + kTopkThreads - 1) / kTopkThreads;
+  const int64_t c0 = (int64_t)tid * C, c1 = min(n, c0 + C);
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int64_t i = c0; i < c1; ++i) {
+    const uint32_t u = key_at(i);
+    n_gt += u > kth;
+    n_eq += u == kth;
   }
-  for (int64_t i = (int64_t)written + tid; i < p.k; i += kTopkThreads) out[i] = -1;
+  const uint32_t ex_gt = block_excl_sum(n_gt, warp_tot, &s_total);
+  const uint32_t ex_eq = block_excl_sum(n_eq, warp_tot, &s_total);
+  uint32_t at = ex_gt + min(ex_eq, remaining);
+  uint32_t tie = ex_eq;
+  for (int64_t i = c0; i < c1; ++i) {
+    const uint32_t u = key_at(i);
+    if (u > kth || (u == kth && tie < remaining)) {
+      if (at < (uint32_t)p.k) out[at] = (int32_t)i;
+      ++at;
+    }
+    tie += u == kth;
+  }
 }
 
 template <typename T, bool kFp8, int HI, int DI>

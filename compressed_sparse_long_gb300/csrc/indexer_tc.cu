@@ -32,8 +32,11 @@ namespace {
 constexpr int kHI = 64;
 constexpr int kDI = 128;
 constexpr int kTile = 128;                  // entries per tile
-constexpr int kStages = 4;
-constexpr int kStageBytes = kTile * kDI;    // fp8 codes
+constexpr int kStageBytes = kTile * kDI;    // fp8 codes of one tile (two 64-entry pages)
+// a stage: codes, then the two pages' 64 row scales, then two page-status words
+constexpr int kStageScaleOff = kStageBytes;
+constexpr int kStageMetaOff = kStageBytes + 2 * 64 * 4;
+constexpr int kStageStride = kStageBytes + 1024;
 constexpr int kABytes = kTile * kDI * 2;    // bf16, two 64-wide K blocks of 16 KB
 constexpr int kThreads = 320;
 constexpr int kConv0 = 2, kEpi0 = 6;        // first converter / epilogue warp
@@ -41,10 +44,11 @@ constexpr int kConv0 = 2, kEpi0 = 6;        // first converter / epilogue warp
 template <int NQ>
 struct Layout {
   static constexpr int N = NQ * kHI;
+  static constexpr int kStages = NQ == 1 ? 6 : 4;
   static constexpr int kBBytes = N * kDI * 2;
   static constexpr int kTmemCols = 2 * N;   // two accumulators
   static constexpr int off_stage = 0;
-  static constexpr int off_a = off_stage + kStages * kStageBytes;
+  static constexpr int off_a = off_stage + kStages * kStageStride;
   static constexpr int off_b = off_a + 2 * kABytes;
   static constexpr int off_w = off_b + kBBytes;
   static constexpr int off_bar = off_w + N * 4;
@@ -167,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   uint8_t* bbuf = sm + Lay::off_b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::off_bar);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* afull = bars + 2 * kStages;
+  uint64_t* empty = bars + Lay::kStages;
+  uint64_t* afull = bars + 2 * Lay::kStages;
   uint64_t* aempty = afull + 2;
   uint64_t* tfull = afull + 4;
   uint64_t* tempty = afull + 6;
@@ -185,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   const int n_groups = (p.n_q + NQ - 1) / NQ;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < Lay::kStages; ++i) {
       tc::mbar_init(full + i, 1);
-      tc::mbar_init(empty + i, 4);
+      tc::mbar_init(empty + i, 8);          // converter and epilogue warps
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(afull + i, 4);
@@ -275,28 +279,35 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       int issued = 0;
       uint32_t had_copy = 0;
       for (int i = 0; i < n_units; ++i) {
-        const int st = i % kStages;
-        if (!tc::mbar_wait(empty + st, ((i / kStages) & 1) ^ 1, abort_flag, p.err)) break;
+        const int st = i % Lay::kStages;
+        if (!tc::mbar_wait(empty + st, ((i / Lay::kStages) & 1) ^ 1, abort_flag, p.err)) break;
         const int seq = w.G.sub_seq[w.s];
+        uint8_t* sb = stage + st * kStageStride;
         int64_t src[2];
         int nv = 0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int64_t blk = 2 * (int64_t)w.t + h;
           src[h] = -1;
+          int status = -1;                              // no page
           if (blk < p.idx.max_blocks) {
             const int32_t page = __ldg(p.idx.bt + (int64_t)seq * p.idx.max_blocks + blk);
+            if (page >= p.idx.n_pages) status = -2;     // page id outside the pool
             if (page >= 0 && page < p.idx.n_pages) {
-              src[h] = (int64_t)page * 64 * kDI;
+              src[h] = page;
+              status = 0;
               ++nv;
             }
           }
+          reinterpret_cast<int*>(sb + kStageMetaOff)[h] = status;
         }
         if (nv) {
-          tc::mbar_arrive_tx(full + st, (uint32_t)(nv * 64 * kDI));
+          tc::mbar_arrive_tx(full + st, (uint32_t)(nv * (64 * kDI + 64 * 4)));
           for (int h = 0; h < 2; ++h)
-            if (src[h] >= 0) tc::bulk_g2s(stage + st * kStageBytes + h * 64 * kDI, idx_data + src[h],
-                                          64 * kDI, full + st);
+            if (src[h] >= 0) {
+              tc::bulk_g2s(sb + h * 64 * kDI, idx_data + src[h] * 64 * kDI, 64 * kDI, full + st);
+              tc::bulk_g2s(sb + kStageScaleOff + h * 256, p.idx.scale + src[h] * 64, 256, full + st);
+            }
           had_copy |= 1u << st;
         } else {
           tc::mbar_arrive(full + st);
@@ -306,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         w.next(p, n_groups);
       }
       if (*abort_flag) {   // drain copies still in flight
-        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-          if (had_copy & (1u << (i % kStages))) tc::mbar_wait_drain(full + i % kStages, (i / kStages) & 1);
+        for (int i = issued > Lay::kStages ? issued - Lay::kStages : 0; i < issued; ++i)
+          if (had_copy & (1u << (i % Lay::kStages))) tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -354,13 +365,24 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         if (gc > 0 && !tc::mbar_wait(bempty, (gc - 1) & 1, abort_flag, p.err)) break;
         // the group's queries -> B operand [N rows = query*64 + head][128 dims]
         const __nv_bfloat16* qsrc = reinterpret_cast<const __nv_bfloat16*>(p.q_idx);
-        for (int item = ct; item < N * 16; item += 128) {
-          const int n = item >> 4, c = item & 15;
-          const int qi = w.g * NQ + n / kHI;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (qi < p.n_q)
-            v = __ldg(reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + (n % kHI)) * kDI) + c);
-          *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + tc::sw128_off(n, c & 7)) = v;
+#pragma unroll 1
+        for (int base = 0; base < N * 16; base += 128 * 8) {   // 8 loads in flight per thread
+          uint4 v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int item = base + k * 128 + ct;
+            const int n = item >> 4, c = item & 15;
+            const int qi = w.g * NQ + n / kHI;
+            v[k] = qi < p.n_q
+                       ? __ldg(reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + (n % kHI)) * kDI) + c)
+                       : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int item = base + k * 128 + ct;
+            const int n = item >> 4, c = item & 15;
+            *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + tc::sw128_off(n, c & 7)) = v[k];
+          }
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -368,10 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         ++gc;
         prev_g = w.g;
       }
-      const int st = i % kStages, ab = i & 1;
-      if (!tc::mbar_wait(full + st, (i / kStages) & 1, abort_flag, p.err)) break;
+      const int st = i % Lay::kStages, ab = i & 1;
+      if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
       if (!tc::mbar_wait(aempty + ab, ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-      const uint8_t* src = stage + st * kStageBytes;
+      const uint8_t* src = stage + st * kStageStride;
       uint8_t* dst = abuf + ab * kABytes;
 #pragma unroll 2
       for (int item = ct; item < kTile * 8; item += 128) {
@@ -404,13 +426,16 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     const int row = quad * 32 + lane;
     Walk<NQ> w = start;
     for (int i = 0; i < n_units; ++i) {
-      const int ab = i & 1;
+      const int ab = i & 1, st = i % Lay::kStages;
+      // the tile's page status and row scales arrive with its codes in the stage
+      if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
+      const uint8_t* sb = stage + st * kStageStride;
+      const int status = reinterpret_cast<const int*>(sb + kStageMetaOff)[row >> 6];
+      const float sc = status == 0 ? reinterpret_cast<const float*>(sb + kStageScaleOff)[row] : 0.f;
       if (!tc::mbar_wait(tfull + ab, (i >> 1) & 1, abort_flag, p.err)) break;
       tc::fence_after_sync();
       const int seq = w.G.sub_seq[w.s];
       const int64_t j = (int64_t)w.t * kTile + row;
-      const int64_t slot = slot_of(p.idx, seq, j);
-      const float sc = slot >= 0 ? __ldg(p.idx.scale + slot) : 0.f;
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         if (w.G.seq[q] != seq) continue;            // warp-uniform
@@ -432,10 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         }
         if (j < w.G.nvis[q]) {
           float out;
-          if (slot >= 0) {
+          if (status == 0) {
             out = s * sc + 0.0f;
           } else {
-            raise_err(p.err, slot == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+            raise_err(p.err, status == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
             out = -INFINITY;
           }
           p.scores[(int64_t)(w.g * NQ + q) * p.row_stride + j] = out;
@@ -443,7 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty + ab);
+      if (lane == 0) {
+        tc::mbar_arrive(tempty + ab);
+        tc::mbar_arrive(empty + st);
+      }
       w.next(p, n_groups);
     }
   }

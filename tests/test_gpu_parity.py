@@ -76,6 +76,30 @@ def test_tiny_fp32_layer_every_position(win_off):
     check_out(out.cpu().numpy()[same], ref, fp8=False)
 
 
+def test_tiny_fp32_decode_splits_and_merge():
+    """fp32 layer, a few late queries through the decode call (keys split over CTAs and
+    merged), against the oracle on the same stored rows."""
+    w = wl.tiny_prefill(seed=9, L=1024)
+    h = w.layers[0]
+    lay, x = device_layer(h), DevInputs(w)
+    lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_)
+    sel = np.array([300, 511, 777, 1000, 1023])
+    q = w.queries
+    topk = lay.index_topk(x.q_seq[sel], x.q_pos[sel], 1023, x.q_idx[sel].contiguous(),
+                          x.w[sel].contiguous())
+    out = lay.attention(x.q_seq[sel], x.q_pos[sel], 1023, x.q[sel].contiguous(), topk)
+    assert lay.cfg.n_heads == 8
+    pools = oracle_pools(h)
+    oracle_insert(w, h, pools)
+    ref_top, scores = O.index_topk(h.spec, pools, q.seq[sel], q.pos[sel], q.q_idx[sel], q.w[sel],
+                                   h.spec.top_k)
+    same = check_topk(topk.cpu().numpy(), ref_top, scores, h.spec.top_k)
+    assert len(same) >= 4
+    ref = O.attention(h.spec, pools, q.seq[sel][same], q.pos[sel][same], q.q[sel][same],
+                      ref_top[same])
+    check_out(out.cpu().numpy()[same], ref, fp8=False)
+
+
 def test_slot_mapping_bit_exact():
     rng = np.random.default_rng(0)
     for R in (256, 64, 2):
