@@ -333,16 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint4 u = d[b][j];
             uint4 lo, hi;
-            lo.x = e4m3x2_to_bf16x2(u.x & 0xFFFFu);
-            lo.y = e4m3x2_to_bf16x2(u.x >> 16);
-            lo.z = e4m3x2_to_bf16x2(u.y & 0xFFFFu);
-            lo.w = e4m3x2_to_bf16x2(u.y >> 16);
-            hi.x = e4m3x2_to_bf16x2(u.z & 0xFFFFu);
-            hi.y = e4m3x2_to_bf16x2(u.z >> 16);
-            hi.z = e4m3x2_to_bf16x2(u.w & 0xFFFFu);
-            hi.w = e4m3x2_to_bf16x2(u.w >> 16);
+            e4m3x16_to_bf16x16(d[b][j], lo, hi);
             const int r = cw * 16 + 4 * j + (lane >> 3);
             const int c0 = 2 * (lane & 7);               // bf16 chunk within the 128-dim block
             const int kb = 2 * b + (c0 >> 3);

@@ -190,6 +190,25 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes_in_low16
   return r;
 }
 
+// Four codes (byte k of w is code k) to two bf16x2 words (codes 0,1 -> lo; 2,3 -> hi),
+// with the same exact placement-and-scale as e4m3x2_to_bf16x2.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t0 = __byte_perm(w, 0u, 0x1404);   // c0 << 8 | c1 << 24
+  const uint32_t t1 = __byte_perm(w, 0u, 0x3424);   // c2 << 8 | c3 << 24
+  const uint32_t b0 = ((t0 >> 4) & 0x07F007F0u) | (t0 & 0x80008000u);
+  const uint32_t b1 = ((t1 >> 4) & 0x07F007F0u) | (t1 & 0x80008000u);
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(b0), "r"(0x7B807B80u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b1), "r"(0x7B807B80u));
+}
+
+// 16 codes -> 16 bf16 (two 16-byte chunks: codes 0-7 in lo, 8-15 in hi).
+__device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4& u, uint4& lo, uint4& hi) {
+  e4m3x4_to_bf16x4(u.x, lo.x, lo.y);
+  e4m3x4_to_bf16x4(u.y, lo.z, lo.w);
+  e4m3x4_to_bf16x4(u.z, hi.x, hi.y);
+  e4m3x4_to_bf16x4(u.w, hi.z, hi.w);
+}
+
 __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Number of entries visible to a query at p: entry j qualifies iff its last covered

@@ -38,8 +38,9 @@ constexpr int kStageScaleOff = kStageBytes;
 constexpr int kStageMetaOff = kStageBytes + 2 * 64 * 4;
 constexpr int kStageStride = kStageBytes + 1024;
 constexpr int kABytes = kTile * kDI * 2;    // bf16, two 64-wide K blocks of 16 KB
-constexpr int kThreads = 320;
-constexpr int kConv0 = 2, kEpi0 = 6;        // first converter / epilogue warp
+constexpr int kThreads = 448;
+constexpr int kConv0 = 2, kEpi0 = 10;       // first converter / epilogue warp
+constexpr int kConvThreads = (kEpi0 - kConv0) * 32;
 
 template <int NQ>
 struct Layout {
@@ -54,7 +55,7 @@ struct Layout {
   static constexpr int off_bar = off_w + N * 4;
   static constexpr int n_bar = 2 * kStages + 8 + 3;
   static constexpr int off_misc = off_bar + n_bar * 8;
-  static constexpr int bytes = off_misc + 64 + 1024;   // + alignment slack
+  static constexpr int bytes = off_misc + 128 + 1024;  // + alignment slack
 };
 
 struct Group {
@@ -182,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   int* misc = reinterpret_cast<int*>(sm + Lay::off_misc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
-  int* scan_buf = misc + 2;          // 10 ints
-  int* scan_tot = misc + 12;
+  int* scan_buf = misc + 4;          // one int per warp
+  int* scan_tot = misc + 20;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_groups = (p.n_q + NQ - 1) / NQ;
@@ -191,15 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   if (tid == 0) {
     for (int i = 0; i < Lay::kStages; ++i) {
       tc::mbar_init(full + i, 1);
-      tc::mbar_init(empty + i, 8);          // converter and epilogue warps
+      tc::mbar_init(empty + i, 12);         // 8 converter + 4 epilogue warps
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(afull + i, 4);
+      tc::mbar_init(afull + i, 8);
       tc::mbar_init(aempty + i, 1);
       tc::mbar_init(tfull + i, 1);
       tc::mbar_init(tempty + i, 4);
     }
-    tc::mbar_init(bfull, 4);
+    tc::mbar_init(bfull, 8);
     tc::mbar_init(bempty, 1);
     tc::mbar_init(done, 1);
     *abort_flag = 0;
@@ -210,8 +211,22 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     tc::tmem_relinquish();
   }
 
-  // ---- this CTA's slice of the units
+  // ---- this CTA's slice of the units (one block scan when the groups fit the block)
+  __shared__ int s_g0, s_off;
   int total_units = 0;
+  if (n_groups <= kThreads) {
+    const int g = tid;
+    const int u = g < n_groups ? load_group<NQ>(p, g, true).units : 0;
+    const int incl = block_scan(u, scan_buf, scan_tot);
+    total_units = *scan_tot;
+    const int64_t ub = (int64_t)total_units * blockIdx.x / gridDim.x;
+    if (tid == 0) { s_g0 = n_groups; s_off = 0; }
+    __syncthreads();
+    if (u > 0 && incl - u <= ub && ub < incl) {
+      s_g0 = g;
+      s_off = (int)(ub - (incl - u));
+    }
+  } else {
   for (int base = 0; base < n_groups; base += kThreads) {
     const int g = base + tid;
     const int u = g < n_groups ? load_group<NQ>(p, g, true).units : 0;
@@ -222,10 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     __syncthreads();
   }
   const int64_t u_begin = (int64_t)total_units * blockIdx.x / gridDim.x;
-  const int64_t u_end = (int64_t)total_units * (blockIdx.x + 1) / gridDim.x;
-  const int n_units = (int)(u_end - u_begin);
   // locate u_begin: group g0 and the offset inside it
-  __shared__ int s_g0, s_off;
   if (tid == 0) { s_g0 = n_groups; s_off = 0; }
   __syncthreads();
   {
@@ -243,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       __syncthreads();
     }
   }
+  }
+  const int64_t u_begin = (int64_t)total_units * blockIdx.x / gridDim.x;
+  const int64_t u_end = (int64_t)total_units * (blockIdx.x + 1) / gridDim.x;
+  const int n_units = (int)(u_end - u_begin);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -274,30 +290,47 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0 && n_units > 0) {
+    // The whole warp keeps the page ids of 32 consecutive blocks (16 tiles) of the current
+    // sequence in registers, one per lane; lane 0 waits on the ring and issues the copies.
+    if (n_units > 0) {
       Walk<NQ> w = start;
       int issued = 0;
       uint32_t had_copy = 0;
+      int cache_seq = -1;
+      int64_t cache_blk0 = 0;
+      int32_t cache_page = -1;
+      bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         const int st = i % Lay::kStages;
-        if (!tc::mbar_wait(empty + st, ((i / Lay::kStages) & 1) ^ 1, abort_flag, p.err)) break;
         const int seq = w.G.sub_seq[w.s];
+        const int64_t blk0 = 2 * (int64_t)w.t;
+        if (seq != cache_seq || blk0 < cache_blk0 || blk0 + 1 >= cache_blk0 + 32) {
+          cache_seq = seq;
+          cache_blk0 = blk0;
+          const int64_t b = blk0 + lane;
+          cache_page = b < p.idx.max_blocks ? __ldg(p.idx.bt + (int64_t)seq * p.idx.max_blocks + b) : -1;
+        }
+        const int32_t pg0 = __shfl_sync(0xffffffffu, cache_page, (int)(blk0 - cache_blk0));
+        const int32_t pg1 = __shfl_sync(0xffffffffu, cache_page, (int)(blk0 + 1 - cache_blk0));
+        if (lane == 0) {
+          if (!tc::mbar_wait(empty + st, ((i / Lay::kStages) & 1) ^ 1, abort_flag, p.err)) ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
         uint8_t* sb = stage + st * kStageStride;
         int64_t src[2];
         int nv = 0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int64_t blk = 2 * (int64_t)w.t + h;
+          const int32_t page = h ? pg1 : pg0;
           src[h] = -1;
           int status = -1;                              // no page
-          if (blk < p.idx.max_blocks) {
-            const int32_t page = __ldg(p.idx.bt + (int64_t)seq * p.idx.max_blocks + blk);
-            if (page >= p.idx.n_pages) status = -2;     // page id outside the pool
-            if (page >= 0 && page < p.idx.n_pages) {
-              src[h] = page;
-              status = 0;
-              ++nv;
-            }
+          if (page >= p.idx.n_pages) status = -2;       // page id outside the pool
+          if (page >= 0 && page < p.idx.n_pages) {
+            src[h] = page;
+            status = 0;
+            ++nv;
           }
           reinterpret_cast<int*>(sb + kStageMetaOff)[h] = status;
         }
@@ -313,10 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
           tc::mbar_arrive(full + st);
           had_copy &= ~(1u << st);
         }
+        }
         issued = i + 1;
         w.next(p, n_groups);
       }
-      if (*abort_flag) {   // drain copies still in flight
+      if (lane == 0 && *abort_flag) {   // drain copies still in flight
         for (int i = issued > Lay::kStages ? issued - Lay::kStages : 0; i < issued; ++i)
           if (had_copy & (1u << (i % Lay::kStages))) tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
       }
@@ -366,22 +400,23 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         // the group's queries -> B operand [N rows = query*64 + head][128 dims]
         const __nv_bfloat16* qsrc = reinterpret_cast<const __nv_bfloat16*>(p.q_idx);
 #pragma unroll 1
-        for (int base = 0; base < N * 16; base += 128 * 8) {   // 8 loads in flight per thread
+        for (int base = 0; base < N * 16; base += kConvThreads * 8) {   // 8 loads in flight per thread
           uint4 v[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int item = base + k * 128 + ct;
+            const int item = base + k * kConvThreads + ct;
             const int n = item >> 4, c = item & 15;
             const int qi = w.g * NQ + n / kHI;
-            v[k] = qi < p.n_q
+            v[k] = (item < N * 16 && qi < p.n_q)
                        ? __ldg(reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + (n % kHI)) * kDI) + c)
                        : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int item = base + k * 128 + ct;
+            const int item = base + k * kConvThreads + ct;
             const int n = item >> 4, c = item & 15;
-            *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + tc::sw128_off(n, c & 7)) = v[k];
+            if (item < N * 16)                           // N rows x 16 chunks of 16 bytes
+              *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + tc::sw128_off(n, c & 7)) = v[k];
           }
         }
         tc::fence_proxy_async();
@@ -395,19 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       if (!tc::mbar_wait(aempty + ab, ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
       const uint8_t* src = stage + st * kStageStride;
       uint8_t* dst = abuf + ab * kABytes;
-#pragma unroll 2
-      for (int item = ct; item < kTile * 8; item += 128) {
+      uint4 raw[kTile * 8 / kConvThreads];
+#pragma unroll
+      for (int k = 0; k < kTile * 8 / kConvThreads; ++k)
+        raw[k] = *reinterpret_cast<const uint4*>(src + (ct + k * kConvThreads) * 16);
+#pragma unroll
+      for (int k = 0; k < kTile * 8 / kConvThreads; ++k) {
+        const int item = ct + k * kConvThreads;
         const int r = item >> 3, v = item & 7;      // 16 codes = dims 16v .. 16v+15
-        const uint4 u = *reinterpret_cast<const uint4*>(src + item * 16);
         uint4 lo, hi;
-        lo.x = e4m3x2_to_bf16x2(u.x & 0xFFFFu);
-        lo.y = e4m3x2_to_bf16x2(u.x >> 16);
-        lo.z = e4m3x2_to_bf16x2(u.y & 0xFFFFu);
-        lo.w = e4m3x2_to_bf16x2(u.y >> 16);
-        hi.x = e4m3x2_to_bf16x2(u.z & 0xFFFFu);
-        hi.y = e4m3x2_to_bf16x2(u.z >> 16);
-        hi.z = e4m3x2_to_bf16x2(u.w & 0xFFFFu);
-        hi.w = e4m3x2_to_bf16x2(u.w >> 16);
+        e4m3x16_to_bf16x16(raw[k], lo, hi);
         const int c0 = 2 * v;                        // bf16 chunk index over 128 dims
         *reinterpret_cast<uint4*>(dst + (c0 >> 3) * (kTile * 128) + tc::sw128_off(r, c0 & 7)) = lo;
         *reinterpret_cast<uint4*>(dst + ((c0 + 1) >> 3) * (kTile * 128) + tc::sw128_off(r, (c0 + 1) & 7)) = hi;
