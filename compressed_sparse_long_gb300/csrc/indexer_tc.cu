@@ -11,12 +11,13 @@
 // per-thread loop in the epilogue.
 //
 // One persistent CTA per SM, warp-specialised, every hand-off an mbarrier:
-//   warp 0      producer: two 8 KB cp.async.bulk copies of fp8 pages per tile (4 stages)
+//   warp 0      producer: per tile two 8 KB cp.async.bulk copies of fp8 pages plus their
+//               row scales into one ring stage (6 stages for one query per group, 4 for four)
 //   warp 1      MMA: allocates TMEM, one thread issues 8 x tcgen05.mma (K = 16) per tile
 //               into one of two TMEM accumulators, commits to the barriers
-//   warps 2-5   converters: fp8 e4m3 -> bf16 (exact) into the 128B-swizzled K-major A
+//   warps 2-9   converters: fp8 e4m3 -> bf16 (exact) into the 128B-swizzled K-major A
 //               operand (two buffers); load the group's queries into the B operand
-//   warps 6-9   epilogue: tcgen05.ld of the accumulator, ReLU, head-weighted sum, row
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator, ReLU, head-weighted sum, row
 //               scale, store of the fp32 scores
 // Work: units = (query group, sequence sub-pass, tile); each CTA takes a contiguous slice
 // of the units of all groups (found with a block scan), so long and short rows balance.
@@ -38,7 +39,7 @@ constexpr int kStageScaleOff = kStageBytes;
 constexpr int kStageMetaOff = kStageBytes + 2 * 64 * 4;
 constexpr int kStageStride = kStageBytes + 1024;
 constexpr int kABytes = kTile * kDI * 2;    // bf16, two 64-wide K blocks of 16 KB
-constexpr int kThreads = 448;
+constexpr int kThreads = 448;              // 14 warps
 constexpr int kConv0 = 2, kEpi0 = 10;       // first converter / epilogue warp
 constexpr int kConvThreads = (kEpi0 - kConv0) * 32;
 
@@ -183,8 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   int* misc = reinterpret_cast<int*>(sm + Lay::off_misc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
-  int* scan_buf = misc + 4;          // one int per warp
-  int* scan_tot = misc + 20;
+  int* scan_buf = misc + 4;          // one int per warp (kThreads / 32 <= 24)
+  int* scan_tot = misc + 28;
+  static_assert(kThreads / 32 <= 24, "scan buffer holds 24 warps");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_groups = (p.n_q + NQ - 1) / NQ;
@@ -272,8 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     start.G = load_group<NQ>(p, start.g, false);
     int off = s_off;
     start.settle(p, n_groups);
-    while (off > 0) {          // offset inside the group: walk its sub-passes
+    // offset inside the group: walk its sub-passes (each step consumes at least one unit;
+    // the walk stops at the end of the groups)
+    while (off > 0 && start.g < n_groups) {
       const int left = start.G.sub_tiles[start.s] - start.t;
+      if (left <= 0) break;
       if (off < left) {
         start.t += off;
         off = 0;
@@ -301,10 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       int32_t cache_page = -1;
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
+        if (w.g >= n_groups) break;                    // every role stops at the same tile
         const int st = i % Lay::kStages;
         const int seq = w.G.sub_seq[w.s];
         const int64_t blk0 = 2 * (int64_t)w.t;
-        if (seq != cache_seq || blk0 < cache_blk0 || blk0 + 1 >= cache_blk0 + 32) {
+        if (seq != cache_seq || blk0 < cache_blk0 || blk0 + 1 >= cache_blk0 + 32) {   // warp-uniform
           cache_seq = seq;
           cache_blk0 = blk0;
           const int64_t b = blk0 + lane;
@@ -352,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       }
       if (lane == 0 && *abort_flag) {   // drain copies still in flight
         for (int i = issued > Lay::kStages ? issued - Lay::kStages : 0; i < issued; ++i)
-          if (had_copy & (1u << (i % Lay::kStages))) tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
+          if (had_copy & (1u << (i % Lay::kStages)))
+            tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -362,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       int prev_g = -1, gc = 0;
       const uint32_t a0 = tc::smem_u32(abuf), b0 = tc::smem_u32(bbuf);
       for (int i = 0; i < n_units; ++i) {
+        if (w.g >= n_groups) break;
         if (w.g != prev_g) {
           if (!tc::mbar_wait(bfull, gc & 1, abort_flag, p.err)) break;
           ++gc;
@@ -395,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     Walk<NQ> w = start;
     int prev_g = -1, gc = 0;
     for (int i = 0; i < n_units; ++i) {
+      if (w.g >= n_groups) break;
       if (w.g != prev_g) {
         if (gc > 0 && !tc::mbar_wait(bempty, (gc - 1) & 1, abort_flag, p.err)) break;
         // the group's queries -> B operand [N rows = query*64 + head][128 dims]
@@ -458,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     const int row = quad * 32 + lane;
     Walk<NQ> w = start;
     for (int i = 0; i < n_units; ++i) {
+      if (w.g >= n_groups) break;
       const int ab = i & 1, st = i % Lay::kStages;
       // the tile's page status and row scales arrive with its codes in the stage
       if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
             s = fmaf(ww.w, fmaxf(acc[4 * h4 + 3], 0.f), s);
           }
         }
-        if (j < w.G.nvis[q]) {
+        if (j < w.G.nvis[q] && w.g * NQ + q < p.n_q) {
           float out;
           if (status == 0) {
             out = s * sc + 0.0f;
