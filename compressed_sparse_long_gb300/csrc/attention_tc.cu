@@ -34,8 +34,8 @@ constexpr int kKBytes = kTile * kD * 2;        // 128 KB key tile, 8 K-blocks of
 constexpr int kQBytes = kH * kD * 2;           // 64 KB Q~, 8 K-blocks of 8 KB
 constexpr int kPBytes = kTile * kH * 2;        // 16 KB P'^T
 constexpr int kOffK = 0, kOffQ = kKBytes, kOffP = kOffQ + kQBytes;
-constexpr int kOffF = kOffP + kPBytes;         // floats: m_run[2][64] l_fin[2][64] red_max[2][256] red_sum[2][256]
-constexpr int kOffBar = kOffF + (128 + 128 + 512 + 512 + 256) * 4;
+constexpr int kOffF = kOffP + kPBytes;         // floats: l_fin[2][64] red_max[2][256] red_sum[2][256] sscale[2][128]
+constexpr int kOffBar = kOffF + (128 + 512 + 512 + 256) * 4;
 constexpr int kNBar = 4 + 4 + 13;
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
@@ -182,8 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   uint8_t* kbuf = sm + kOffK;
   uint8_t* qbuf = sm + kOffQ;
   uint8_t* pbuf = sm + kOffP;
-  float* m_run = reinterpret_cast<float*>(sm + kOffF);   // [2][64] by tile parity
-  float* l_fin = m_run + 128;                             // [2][64] by item parity
+  float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] by item parity
   float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
   float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
   float* sscale = red_sum + 512;                          // [2][128] row scales by tile parity
@@ -353,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   } else if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
     // ------------------------------------------------------------ softmax + epilogue
-    // m_run[2][64]: running max by tile parity (written by the head's owner thread, read
-    // by all); the owner of head h (thread row h) also keeps its denominator in a register
-    // and publishes it in l_fin[item parity][64] for the epilogue.
+    // Every lane keeps the running max of heads `lane` and `lane + 32` in registers (all
+    // four warps hold the same copy); the owner of head h (thread row h) keeps its
+    // denominator in a register and publishes it in l_fin[item parity][64] for the epilogue.
     const int quad = warp;
     const int row = quad * 32 + lane;             // TMEM lane: key (S^T) or dim (O^T)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -381,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         continue;
       }
       float l_reg = 0.f;                          // owner threads (row < 64)
-      if (row < 64) m_run[row] = -INFINITY;       // buffer 0 for tile 0
+      float mc0 = -INFINITY, mc1 = -INFINITY;     // running max of heads lane, lane + 32
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
         if (!tc::mbar_wait(sfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
         tc::fence_after_sync();
@@ -408,25 +407,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           if (lane == (h & 31)) rb[h * 4 + quad] = mh;
         }
         if (!group_sync()) { ok = false; break; }
-        const float* m_cur = m_run + (t & 1) * 64;
-        float* m_nxt = m_run + ((t + 1) & 1) * 64;
-        // new running max (raised only past the threshold); the correction factor of head h
-        // is exp2(m_cur[h] - m_nxt[h]), read back from shared memory where needed
+        // new running max of heads lane and lane + 32 (raised only past the threshold) and
+        // the correction factors exp2(old - new) of the accumulated O^T and denominators
+        float mn0, mn1, cr0 = 1.f, cr1 = 1.f;
         bool any_rescale = false;
+        {
+          const float4 v0 = *reinterpret_cast<const float4*>(rb + lane * 4);
+          const float4 v1 = *reinterpret_cast<const float4*>(rb + (lane + 32) * 4);
+          const float mt0 = fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w));
+          const float mt1 = fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w));
+          if (t == 0) {                          // nothing accumulated yet
+            mn0 = mt0;
+            mn1 = mt1;
+          } else {
+            mn0 = mt0 > mc0 + kRescaleThreshold ? mt0 : mc0;
+            mn1 = mt1 > mc1 + kRescaleThreshold ? mt1 : mc1;
+            if (mn0 != mc0) cr0 = fast_exp2(mc0 - mn0);   // 0 when the old max is -inf
+            if (mn1 != mc1) cr1 = fast_exp2(mc1 - mn1);
+            any_rescale = __any_sync(0xffffffffu, mn0 != mc0 || mn1 != mc1);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < 64; ++h) {
-          const float4 v = *reinterpret_cast<const float4*>(rb + h * 4);
-          const float mt = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-          const float mo = m_cur[h];
-          float mn = mo;
-          if (t == 0) {
-            mn = mt;                               // nothing accumulated yet
-          } else if (mt > mo + kRescaleThreshold) {
-            mn = mt;
-            any_rescale = true;
-          }
+          const float mn = __shfl_sync(0xffffffffu, h < 32 ? mn0 : mn1, h & 31);
           s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
-          if (row == h) m_nxt[h] = mn;
         }
         // ---- the P' buffer and O^T must be free of the previous tile's product
         if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
@@ -441,11 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
               tc::tmem_ld32(addr, o);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; ++h) {
-                const int hh = half * 32 + h;
-                const float mo = m_cur[hh], mn = m_nxt[hh];
-                o[h] *= mo == mn ? 1.f : fast_exp2(mo - mn);
-              }
+              for (int h = 0; h < 32; ++h) o[h] *= __shfl_sync(0xffffffffu, half ? cr1 : cr0, h);
               tmem_st32(addr, o);
             }
           }
@@ -472,16 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         rs[(2 * lane) * 4 + quad] = part.x;
         rs[(2 * lane + 1) * 4 + quad] = part.y;
         if (!group_sync()) { ok = false; break; }
+        mc0 = mn0;
+        mc1 = mn1;
         if (row < 64) {
           const float4 v = *reinterpret_cast<const float4*>(rs + row * 4);
-          const float cr = t == 0 ? 1.f : fast_exp2(m_cur[row] - m_nxt[row]);   // 0 if m_cur = -inf
-          l_reg = l_reg * cr + ((v.x + v.y) + (v.z + v.w));
+          l_reg = l_reg * (quad == 0 ? cr0 : cr1) + ((v.x + v.y) + (v.z + v.w));
         }
       }
       if (!ok) break;
       // ---- publish the denominators, then read O^T (lanes: dims 128b + row; cols: heads)
       if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg;
-      const float m_final = row < 64 ? m_run[(I.n_tiles & 1) * 64 + row] : 0.f;
+      const float m_final = quad == 0 ? mc0 : mc1;   // used by the owners (row < 64)
       if (!group_sync()) { ok = false; break; }
       const float* lden = l_fin + (ni & 1) * 64;
       if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }

@@ -220,6 +220,138 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   }
 }
 
+// Register-resident variant for rows of up to ITEMS * THREADS entries: entry i = r*THREADS
+// + tid is held by thread tid as u[r] (coalesced loads). Each 8-bit pass counts with one
+// atomic per distinct digit per warp (__match_any_sync) into one of two histograms, so a
+// pass needs two barriers; the compaction ranks entries in index order, (round, warp,
+// lane), from one scan of packed (above, equal) ballot counts.
+template <int ITEMS, int THREADS>
+__global__ void __launch_bounds__(THREADS) topk_reg_kernel(const __grid_constant__ IndexParams p) {
+  constexpr int kWarps = THREADS / 32;
+  constexpr int kCnt = ITEMS * kWarps;
+  static_assert(kCnt % 32 == 0, "count table splits over one warp");
+  static_assert(ITEMS * THREADS <= 65535, "packed 16-bit counts");
+  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t cnt[kCnt];
+  __shared__ uint32_t s_digit, s_remaining;
+  const int qi = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int64_t n = min(visible_entries(pos, p.S, p.W, p.win_off), p.row_stride);
+  int32_t* out = p.topk + (int64_t)qi * p.k;
+  if (n <= p.k) {
+    for (int i = tid; i < p.k; i += THREADS) out[i] = i < n ? i : -1;
+    return;
+  }
+  const float* row = p.scores + (int64_t)qi * p.row_stride;
+  const int nn = (int)n;   // <= ITEMS * THREADS (the launcher's choice)
+  uint32_t u[ITEMS];
+#pragma unroll
+  for (int r = 0; r < ITEMS; ++r) {
+    const int i = r * THREADS + tid;
+    u[r] = i < nn ? order_key(__ldg(row + i)) : 0u;
+  }
+  for (int i = tid; i < 512; i += THREADS) (&hist[0][0])[i] = 0u;
+  __syncthreads();
+
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    uint32_t* h = hist[pass & 1];
+    // the other histogram was last read before the previous pass's second barrier
+    if (pass > 0)
+      for (int i = tid; i < 256; i += THREADS) hist[(pass + 1) & 1][i] = 0u;
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {
+      const bool in = r * THREADS + tid < nn && (u[r] & mask) == prefix;
+      const uint32_t bin = in ? (u[r] >> shift) & 0xFFu : 0x100u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l-7 .. 255-8l, scanned from the top; exactly one lane holds
+      // the digit where the running count reaches `remaining`
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = h[255 - 8 * lane - k];
+        sum += c[k];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t before = incl - sum;
+      if (before < remaining && incl >= remaining) {
+        uint32_t cum = before;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (cum + c[k] >= remaining) {
+            s_digit = 255 - 8 * lane - k;
+            s_remaining = remaining - cum;
+            break;
+          }
+          cum += c[k];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= s_digit << shift;
+    mask |= 0xFFu << shift;
+    remaining = s_remaining;
+  }
+
+  // prefix is the key of the k-th largest score: take every key above it and the first
+  // `remaining` keys equal to it, in index order
+  const uint32_t kth = prefix;
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int r = 0; r < ITEMS; ++r) {
+    const bool v = r * THREADS + tid < nn;
+    const uint32_t bg = __ballot_sync(0xffffffffu, v && u[r] > kth);
+    const uint32_t be = __ballot_sync(0xffffffffu, v && u[r] == kth);
+    if (lane == 0) cnt[r * kWarps + warp] = ((uint32_t)__popc(bg) << 16) | (uint32_t)__popc(be);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kPer = kCnt / 32;
+    uint32_t c[kPer], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      c[j] = cnt[lane * kPer + j];
+      sum += c[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t ex = incl - sum;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      cnt[lane * kPer + j] = ex;
+      ex += c[j];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < ITEMS; ++r) {
+    const bool v = r * THREADS + tid < nn;
+    const bool gt = v && u[r] > kth, eq = v && u[r] == kth;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t base = cnt[r * kWarps + warp];
+    const uint32_t n_gt = (base >> 16) + (uint32_t)__popc(bg & lt);
+    const uint32_t n_eq = (base & 0xFFFFu) + (uint32_t)__popc(be & lt);
+    if (gt || (eq && n_eq < remaining)) out[n_gt + min(n_eq, remaining)] = r * THREADS + tid;
+  }
+}
+
 template <typename T, bool kFp8, int HI, int DI>
 cudaError_t launch_simt(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   dim3 grid((unsigned)((max_vis + 127) / 128), (unsigned)p.n_q);
@@ -246,7 +378,11 @@ int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaSt
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.n_q == 0) return V4A_OK;
   cudaError_t e;
-  if (max_vis <= kTopkSmemMax) {
+  if (max_vis <= 16 * 512) {
+    topk_reg_kernel<16, 512><<<p.n_q, 512, 0, st>>>(p);
+  } else if (max_vis <= 32 * 1024) {
+    topk_reg_kernel<32, 1024><<<p.n_q, 1024, 0, st>>>(p);
+  } else if (max_vis <= kTopkSmemMax) {
     const size_t smem = (size_t)max_vis * sizeof(uint32_t);
     static bool attr_set = false;
     if (!attr_set) {
