@@ -59,6 +59,11 @@ def index_bytes_per_query(n_vis: int, k: int, H_I: int = 64, d_I: int = 128) -> 
     return n_vis * (d_I + 4) + H_I * d_I * 2 + H_I * 4 + k * 4
 
 
+def attn_bytes_per_query(k: int, swa: int, H: int = 64, D: int = 512) -> int:
+    """Selected and window rows (fp8 codes + fp32 scale), their ids, the query and the output."""
+    return (k + swa) * (D + 4) + k * 4 + 2 * H * D * 2
+
+
 def attn_flops_per_query(n_keys: int, H: int = 64, D: int = 512) -> float:
     return 4.0 * H * D * n_keys          # QK^T and PV, 2 flops per multiply-add
 
@@ -241,11 +246,15 @@ class DecodeReplica:
         self.max_pos = int(q.pos.max())
         self.topk = torch.empty((len(q.pos), self.lay.top_k), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)   # device error bits
 
     def step(self):
-        self.lay.compress_insert(self.cu, self.start, self.kv, self.s, self.ik, self.is_)
-        self.lay.index_topk(self.q_seq, self.q_pos, self.max_pos, self.q_idx, self.w, self.topk)
-        self.lay.attention(self.q_seq, self.q_pos, self.max_pos, self.q, self.topk, out=self.out)
+        self.lay.compress_insert(self.cu, self.start, self.kv, self.s, self.ik, self.is_,
+                                 dev_err=self.err)
+        self.lay.index_topk(self.q_seq, self.q_pos, self.max_pos, self.q_idx, self.w, self.topk,
+                            dev_err=self.err)
+        self.lay.attention(self.q_seq, self.q_pos, self.max_pos, self.q, self.topk, out=self.out,
+                           dev_err=self.err)
 
     def touched_bytes(self):
         n_vis = (self.max_pos - 8) // 4 + 1
@@ -325,11 +334,25 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     algo_bytes_step = per_step
     hbm_gbs = algo_bytes_step / (ms_per_step / 1e3) / 1e9
 
-    # per-call timing over the same rotating replicas (the dominant call's roofline)
+    # per-call timing over the same rotating replicas; the roofline line is the slower of
+    # the two large calls (both HBM-bound by arithmetic intensity)
     calls = _per_call_times(reps, args.steps, stream)
     n_vis = (L - 8) // 4 + 1
-    idx_bytes = B * index_bytes_per_query(n_vis, 512)
-    idx_gbs = idx_bytes / (calls["index_topk"] / 1e3) / 1e9
+    roof = {}
+    for call, kern, nbytes in (
+            ("index_topk", "v4a_index_topk (indexer scores + top-k)",
+             B * index_bytes_per_query(n_vis, 512)),
+            ("attention", "v4a_attn_decode (attention + split merge)",
+             B * attn_bytes_per_query(512, 128))):
+        gbs = nbytes / (calls[call] / 1e3) / 1e9
+        roof[call] = {"kernel": kern, "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                      "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": _profile_traffic(call),
+                      "peak_source": peak_src, "algorithmic_bytes_per_launch": nbytes,
+                      "us_per_launch": calls[call] * 1e3}
+    dominant = max(roof, key=lambda c: calls[c])
+    err_bits = 0
+    for r in reps:
+        err_bits |= int(r.err.item())
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -345,11 +368,9 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / hbm_peak,
         "per_call_ms": calls,
-        "roofline": {"kernel": "v4a_index_topk (indexer scores + top-k)", "bound": "hbm",
-                     "achieved": idx_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": idx_gbs / hbm_peak, "traffic": _profile_traffic(),
-                     "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": idx_bytes},
+        "roofline": roof[dominant],
+        "roofline_other": roof["attention" if dominant == "index_topk" else "index_topk"],
+        "device_error_bits": err_bits,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -361,6 +382,8 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         line["cpu_baseline"] = cpu_baseline_subprocess(2, args.cpu_budget_s)
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if err_bits:
+        raise SystemExit("device error bits 0x%x raised during the decode steps" % err_bits)
 
 
 def _max_over_ranks(ms, world, dev):
@@ -403,10 +426,10 @@ def _per_call_times(reps, steps, stream):
     return out
 
 
-def _profile_traffic():
-    """DRAM bytes per launch of the dominant call from the committed ncu summary, if that
-    summary still describes the current kernels (it states the library version)."""
-    p = os.path.join(ROOT, "profiles", "index_topk_c4a_decode_B32_L32768.md")
+def _profile_traffic(call: str):
+    """DRAM bytes per launch of a call from its committed ncu summary, if that summary still
+    describes the current kernels (it states the library version)."""
+    p = os.path.join(ROOT, "profiles", "%s_c4a_decode_B32_L32768.md" % call)
     if not os.path.exists(p):
         return None
     import compressed_sparse_long_gb300 as v4a

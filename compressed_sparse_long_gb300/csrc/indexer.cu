@@ -220,20 +220,33 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   }
 }
 
+__device__ __forceinline__ float key_value(uint32_t u) {   // inverse of order_key
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
 // Register-resident variant for rows of up to ITEMS * THREADS entries: entry i = r*THREADS
-// + tid is held by thread tid as u[r] (coalesced loads). Each 8-bit pass counts with one
-// atomic per distinct digit per warp (__match_any_sync) into one of two histograms, so a
-// pass needs two barriers; the compaction ranks entries in index order, (round, warp,
-// lane), from one scan of packed (above, equal) ballot counts.
+// + tid is held by thread tid as u[r] (coalesced loads).
+// Threshold: 1024 buckets linear in the score between the row's min and max (a monotone
+// map, so every entry of a higher bucket scores strictly higher); the bucket where the
+// count from the top reaches k holds the k-th score, and the exact k-th key is found among
+// that bucket's entries alone (a handful for spread-out scores). When the bucket is large
+// (many equal or clustered scores) or the range is not finite, four 8-bit radix passes find
+// it instead (one atomic per distinct digit per warp, two histograms, two barriers a pass).
+// The compaction ranks entries in index order, (round, warp, lane), from one scan of packed
+// (above, equal) ballot counts.
 template <int ITEMS, int THREADS>
-__global__ void __launch_bounds__(THREADS) topk_reg_kernel(const __grid_constant__ IndexParams p) {
+__global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_constant__ IndexParams p) {
   constexpr int kWarps = THREADS / 32;
   constexpr int kCnt = ITEMS * kWarps;
   static_assert(kCnt % 32 == 0, "count table splits over one warp");
   static_assert(ITEMS * THREADS <= 65535, "packed 16-bit counts");
+  constexpr int kBuckets = 1024, kCandMax = 512;
   __shared__ uint32_t hist[2][256];
   __shared__ uint32_t cnt[kCnt];
-  __shared__ uint32_t s_digit, s_remaining;
+  __shared__ uint32_t bhist[kBuckets];
+  __shared__ uint32_t cand[kCandMax];
+  __shared__ float s_min[kWarps], s_max[kWarps];
+  __shared__ uint32_t s_digit, s_remaining, s_bucket, s_above, s_ncand, s_kth;
   const int qi = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t pos = __ldg(p.q_pos + qi);
@@ -252,62 +265,159 @@ __global__ void __launch_bounds__(THREADS) topk_reg_kernel(const __grid_constant
     u[r] = i < nn ? order_key(__ldg(row + i)) : 0u;
   }
   for (int i = tid; i < 512; i += THREADS) (&hist[0][0])[i] = 0u;
-  __syncthreads();
-
-  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.k;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    uint32_t* h = hist[pass & 1];
-    // the other histogram was last read before the previous pass's second barrier
-    if (pass > 0)
-      for (int i = tid; i < 256; i += THREADS) hist[(pass + 1) & 1][i] = 0u;
+  for (int i = tid; i < kBuckets; i += THREADS) bhist[i] = 0u;
+  if (tid == 0) s_ncand = 0u;
+  {
+    float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
     for (int r = 0; r < ITEMS; ++r) {
-      const bool in = r * THREADS + tid < nn && (u[r] & mask) == prefix;
-      const uint32_t bin = in ? (u[r] >> shift) & 0xFFu : 0x100u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+      if (r * THREADS + tid < nn) {
+        const float x = key_value(u[r]);
+        lo = fminf(lo, x);
+        hi = x != x ? INFINITY : fmaxf(hi, x);   // a NaN score sends the row to the radix path
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+      s_min[warp] = lo;
+      s_max[warp] = hi;
+    }
+  }
+  __syncthreads();
+  float lo = s_min[0], hi = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    lo = fminf(lo, s_min[w]);
+    hi = fmaxf(hi, s_max[w]);
+  }
+  uint32_t kth = 0, remaining = 0;
+  bool found = false;
+  const float span = hi - lo;
+  if (span > 0.f && span <= 3.0e38f) {           // finite, not all equal (block-uniform)
+    const float inv = (float)kBuckets / span;
+    auto bucket = [&](uint32_t key) -> int {
+      return max(0, min((int)((key_value(key) - lo) * inv), kBuckets - 1));
+    };
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r)
+      if (r * THREADS + tid < nn) atomicAdd(&bhist[bucket(u[r])], 1u);
     __syncthreads();
     if (warp == 0) {
-      // lane l owns digits 255-8l-7 .. 255-8l, scanned from the top; exactly one lane holds
-      // the digit where the running count reaches `remaining`
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        c[k] = h[255 - 8 * lane - k];
-        sum += c[k];
-      }
+      // lane l owns buckets 1023-32l-31 .. 1023-32l, scanned from the top
+      uint32_t sum = 0;
+      for (int j = 0; j < 32; ++j) sum += bhist[kBuckets - 1 - 32 * lane - j];
       uint32_t incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const uint32_t before = incl - sum;
-      if (before < remaining && incl >= remaining) {
+      const uint32_t before = incl - sum, kk = (uint32_t)p.k;
+      if (before < kk && incl >= kk) {
         uint32_t cum = before;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (cum + c[k] >= remaining) {
-            s_digit = 255 - 8 * lane - k;
-            s_remaining = remaining - cum;
+        for (int j = 0; j < 32; ++j) {
+          const int b = kBuckets - 1 - 32 * lane - j;
+          const uint32_t c = bhist[b];
+          if (cum + c >= kk) {
+            s_bucket = (uint32_t)b;
+            s_above = cum;
             break;
           }
-          cum += c[k];
+          cum += c;
         }
       }
     }
     __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= 0xFFu << shift;
-    remaining = s_remaining;
+    const int bstar = (int)s_bucket;
+    const uint32_t r_need = (uint32_t)p.k - s_above;   // entries still to take from bstar
+    if (bhist[bstar] <= (uint32_t)kCandMax) {          // block-uniform
+#pragma unroll
+      for (int r = 0; r < ITEMS; ++r)
+        if (r * THREADS + tid < nn && bucket(u[r]) == bstar) cand[atomicAdd(&s_ncand, 1u)] = u[r];
+      __syncthreads();
+      const int nc = (int)s_ncand;
+      // the candidate whose key has fewer than r_need keys above it and at least r_need at
+      // or above it holds the k-th key (all such candidates hold the same key)
+      for (int c = tid; c < nc; c += THREADS) {
+        const uint32_t uc = cand[c];
+        uint32_t gt = 0, ge = 0;
+        for (int j = 0; j < nc; ++j) {
+          const uint32_t v = cand[j];
+          gt += v > uc;
+          ge += v >= uc;
+        }
+        if (gt < r_need && r_need <= ge) {
+          s_kth = uc;
+          s_remaining = r_need - gt;
+        }
+      }
+      __syncthreads();
+      kth = s_kth;
+      remaining = s_remaining;
+      found = true;
+    }
+  }
+  if (!found) {
+    uint32_t prefix = 0, mask = 0;
+    remaining = (uint32_t)p.k;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      uint32_t* h = hist[pass & 1];
+      // the other histogram was last read before the previous pass's second barrier
+      if (pass > 0)
+        for (int i = tid; i < 256; i += THREADS) hist[(pass + 1) & 1][i] = 0u;
+#pragma unroll
+      for (int r = 0; r < ITEMS; ++r) {
+        const bool in = r * THREADS + tid < nn && (u[r] & mask) == prefix;
+        const uint32_t bin = in ? (u[r] >> shift) & 0xFFu : 0x100u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns digits 255-8l-7 .. 255-8l, scanned from the top; exactly one lane holds
+        // the digit where the running count reaches `remaining`
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c[k] = h[255 - 8 * lane - k];
+          sum += c[k];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t before = incl - sum;
+        if (before < remaining && incl >= remaining) {
+          uint32_t cum = before;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (cum + c[k] >= remaining) {
+              s_digit = 255 - 8 * lane - k;
+              s_remaining = remaining - cum;
+              break;
+            }
+            cum += c[k];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= s_digit << shift;
+      mask |= 0xFFu << shift;
+      remaining = s_remaining;
+    }
+    kth = prefix;
   }
 
-  // prefix is the key of the k-th largest score: take every key above it and the first
+  // kth is the key of the k-th largest score: take every key above it and the first
   // `remaining` keys equal to it, in index order
-  const uint32_t kth = prefix;
   const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
   for (int r = 0; r < ITEMS; ++r) {
@@ -348,7 +458,8 @@ __global__ void __launch_bounds__(THREADS) topk_reg_kernel(const __grid_constant
     const uint32_t base = cnt[r * kWarps + warp];
     const uint32_t n_gt = (base >> 16) + (uint32_t)__popc(bg & lt);
     const uint32_t n_eq = (base & 0xFFFFu) + (uint32_t)__popc(be & lt);
-    if (gt || (eq && n_eq < remaining)) out[n_gt + min(n_eq, remaining)] = r * THREADS + tid;
+    const uint32_t at = n_gt + min(n_eq, remaining);
+    if ((gt || (eq && n_eq < remaining)) && at < (uint32_t)p.k) out[at] = r * THREADS + tid;
   }
 }
 

@@ -230,7 +230,8 @@ int v4a_slot_mapping(const v4a_cache* cache, int32_t n, const int32_t* seq,
  * receives the bits. Returns V4A_OK, V4A_ERR_DEVICE if any bit was set, or V4A_ERR_CUDA. */
 int v4a_get_error(int32_t* dev_err, v4a_stream_t stream, int32_t* flags_out);
 
-/* Library version, for the binding's sanity check. */
+/* Library version, raised whenever an entry point or a kernel changes (profiles and the
+ * binding compare against it). */
 int32_t v4a_version(void);
 
 #ifdef __cplusplus

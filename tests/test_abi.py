@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
                          text=True).stdout
     exported = set(re.findall(r"\bT (v4a_\w+)", out))
     assert set(names) <= exported
-    assert v4a.v4a_version() == 1
+    assert v4a.v4a_version() >= 1
 
 
 def test_struct_layout_matches_c(tmp_path):

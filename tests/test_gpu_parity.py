@@ -212,6 +212,37 @@ def test_topk_ties_take_smaller_index():
         assert np.array_equal(topk[i], np.arange(512))
 
 
+@pytest.mark.parametrize("n_tied,rank", [(300, 0), (300, 412), (1200, 0)])
+def test_topk_tied_block(n_tied, rank):
+    """A block of identical indexer keys (so identical scores) placed wholly above the k-th
+    score, across it, or larger than k at the top of the row: the output holds every entry
+    scoring above the block and exactly the smallest-index members of the block."""
+    w = wl.c4a_decode(seed=11, B=2, L=16384)
+    h = w.layers[0]
+    q = w.queries
+    rng = np.random.default_rng(17)
+    _, scores = O.index_topk(h.spec, oracle_pools(h), q.seq, q.pos, q.q_idx, q.w, 512)
+    tied = []
+    for i in range(len(q.pos)):
+        b, sc = int(q.seq[i]), np.asarray(scores[i])
+        src = int(np.argsort(-sc, kind="stable")[rank])
+        others = rng.choice(np.setdiff1d(np.arange(len(sc)), [src]), n_tied - 1, replace=False)
+        r0 = O.slot(h.idx.bt, 64, b, src)
+        for j in others:
+            r = O.slot(h.idx.bt, 64, b, int(j))
+            h.idx.data[r], h.idx.scale[r] = h.idx.data[r0], h.idx.scale[r0]
+        tied.append(np.sort(np.append(others, src)))
+    lay, x = device_layer(h), DevInputs(w)
+    got = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w).cpu().numpy()
+    ref, scores = O.index_topk(h.spec, oracle_pools(h), q.seq, q.pos, q.q_idx, q.w, 512)
+    check_topk(got, ref, scores, 512)
+    for i in range(len(q.pos)):
+        sel = np.intersect1d(got[i], tied[i])
+        assert np.array_equal(sel, tied[i][:len(sel)]), "tied block must be taken by index"
+        if rank == 0:
+            assert len(sel) == min(n_tied, 512)
+
+
 # ------------------------------------------------------------------------- attention
 def _random_lists(rng, pos, spec, k, n_pad=3):
     out = np.full((len(pos), k), -1, np.int32)
