@@ -1,28 +1,44 @@
-// Indexer scores on the 5th-generation tensor cores (tcgen05), bf16 x bf16 -> fp32.
+// Indexer scores on the 5th-generation tensor cores (tcgen05), fp8 x fp8 -> fp32.
 //
 //   score[q, j] = scale_j * sum_h w[q,h] * max(0, q_idx[q,h,:] . code_j)
 //
 // ([blog] "vLLM DeepSeek V4 支援：高效長上下文注意力", DeepSeek Sparse Attention bullet; the
-// scale is applied after the head sum because ReLU is positively homogeneous.)
+// row scale is applied after the head sum because ReLU is positively homogeneous.)
 //
-// Tile: M = 128 consecutive c4a entries of one sequence (two 64-entry pages of the paged
-// cache), N = 64 heads x NQ queries of the same sequence, K = d_I = 128. Entries sit on
-// the M axis so each TMEM lane holds one entry's head dot products and the head sum is a
-// per-thread loop in the epilogue.
+// Keys stay in their fp8 e4m3 codes: a page (64 entries x 128 bytes) is copied by a TMA
+// tensor copy with 128-byte swizzle straight into the K-major operand layout, so nothing is
+// converted or rewritten on chip. The bf16 query row of head h is split exactly into two
+// e4m3 terms, q*s = hi + lo with s = 2^(7 - exponent(max|q_h|)): hi is q*s rounded to e4m3
+// and the remainder lo = q*s - hi has at most four significant bits, so it is an e4m3 value
+// too (up to the e4m3 subnormal step, 2^-9, for elements below 2^-2 after scaling). Both
+// terms sit on the N axis of one product (kind::f8f6f4, fp32 accumulation); the epilogue
+// adds them and applies w_h / s.
+//
+// Tile: M = 128 consecutive c4a entries of one sequence (two 64-entry pages), N = 128 rows
+// per query (64 heads x {hi, lo}) x NQ queries of the same sequence, K = d_I = 128 (four
+// MMAs of K = 32). Entries sit on the M axis so each TMEM lane holds one entry's head dot
+// products and the head sum is a per-thread loop in the epilogue.
 //
 // One persistent CTA per SM, warp-specialised, every hand-off an mbarrier:
-//   warp 0      producer: per tile two 8 KB cp.async.bulk copies of fp8 pages plus their
-//               row scales into one ring stage (6 stages for one query per group, 4 for four)
-//   warp 1      MMA: allocates TMEM, one thread issues 8 x tcgen05.mma (K = 16) per tile
-//               into one of two TMEM accumulators, commits to the barriers
-//   warps 2-9   converters: fp8 e4m3 -> bf16 (exact) into the 128B-swizzled K-major A
-//               operand (two buffers); load the group's queries into the B operand
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator, ReLU, head-weighted sum, row
-//               scale, store of the fp32 scores
+//   warps 0,14-16 producers: a tile's two pages are copied into one ring stage by two
+//               warps, one per page; even tiles go to warps 0 and 14, odd tiles to 15 and
+//               16 (a warp serialises its bulk copies, ~0.3 us each). Each warp arms the
+//               stage barrier with its own bytes and leaves its page id (or status) there.
+//   warp 1      MMA: allocates TMEM, one thread issues 4 tcgen05.mma per tile into one of
+//               four accumulators (two for two queries per group); commits release the
+//               stage and hand the tile over
+//   warps 2-9   epilogue, two sets of four (one per TMEM lane quadrant) taking even and
+//               odd tiles: tcgen05.ld, hi + lo, ReLU, weighted head sum, row scale, store
+//   warps 10-13 query preparation: the hi/lo B operand and w/s of each query group, double
+//               buffered across groups
 // Work: units = (query group, sequence sub-pass, tile); each CTA takes a contiguous slice
 // of the units of all groups (found with a block scan), so long and short rows balance.
 // Every wait is bounded (~1 s): on expiry the CTA sets V4A_DEV_TIMEOUT, drains its copies
 // and MMAs, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -33,31 +49,56 @@ namespace {
 constexpr int kHI = 64;
 constexpr int kDI = 128;
 constexpr int kTile = 128;                  // entries per tile
-constexpr int kStageBytes = kTile * kDI;    // fp8 codes of one tile (two 64-entry pages)
-// a stage: codes, then the two pages' 64 row scales, then two page-status words
-constexpr int kStageScaleOff = kStageBytes;
-constexpr int kStageMetaOff = kStageBytes + 2 * 64 * 4;
+constexpr int kPageBytes = 64 * kDI;        // one 64-entry page of fp8 codes
+constexpr int kStageBytes = kTile * kDI;    // codes of one tile (two pages)
+// a stage: codes, then the two pages' ids (-1: no page, -2: id outside the pool); stages
+// stay 1 KB aligned for the swizzled copies
+constexpr int kStageMetaOff = kStageBytes;
 constexpr int kStageStride = kStageBytes + 1024;
-constexpr int kABytes = kTile * kDI * 2;    // bf16, two 64-wide K blocks of 16 KB
-constexpr int kThreads = 448;              // 14 warps
-constexpr int kConv0 = 2, kEpi0 = 10;       // first converter / epilogue warp
-constexpr int kConvThreads = (kEpi0 - kConv0) * 32;
+constexpr int kThreads = 544;              // 17 warps
+constexpr int kEpi0 = 2, kPrep0 = 10;       // first epilogue / query-preparation warp
+constexpr int kProd1 = 14;                  // producers: warp 0 and warps 14-16
 
 template <int NQ>
 struct Layout {
-  static constexpr int N = NQ * kHI;
-  static constexpr int kStages = NQ == 1 ? 6 : 4;
-  static constexpr int kBBytes = N * kDI * 2;
-  static constexpr int kTmemCols = 2 * N;   // two accumulators
+  static constexpr int N = NQ * 2 * kHI;    // hi and lo rows of each query
+  static constexpr int kStages = NQ == 1 ? 10 : 8;   // even: tiles alternate producer pairs
+  static constexpr int kBBytes = N * kDI;   // fp8 B operand of one group
+  static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators (512 columns)
+  static constexpr int kTmemCols = kAcc * N;
   static constexpr int off_stage = 0;
-  static constexpr int off_a = off_stage + kStages * kStageStride;
-  static constexpr int off_b = off_a + 2 * kABytes;
-  static constexpr int off_w = off_b + kBBytes;
-  static constexpr int off_bar = off_w + N * 4;
-  static constexpr int n_bar = 2 * kStages + 8 + 3;
+  static constexpr int off_b = kStages * kStageStride;            // 1 KB aligned
+  static constexpr int off_w = off_b + 2 * kBBytes;               // w_h / s_h [2][NQ * 64]
+  static constexpr int off_bar = off_w + 2 * NQ * kHI * 4;
+  static constexpr int n_bar = 2 * kStages + 2 * kAcc + 6 + 1;
   static constexpr int off_misc = off_bar + n_bar * 8;
   static constexpr int bytes = off_misc + 128 + 1024;  // + alignment slack
+  static_assert(off_b % 1024 == 0, "swizzled operands need 1 KB alignment");
 };
+
+// tcgen05.mma kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format
+// code 0), both K-major, shape M x N.
+constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2-D TMA tensor copy global -> shared (box given by the tensor map), completion on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
+}
 
 struct Group {
   int n_sub;
@@ -67,6 +108,23 @@ struct Group {
   int sub_seq[4];
   int sub_tiles[4];
 };
+
+// Element i of a small array through unrolled selects, so the array stays in registers
+// (dynamic indexing would place it in local memory).
+template <typename T>
+__device__ __forceinline__ T pick4(const T (&a)[4], int i) {
+  T r = a[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (i == k) r = a[k];
+  return r;
+}
+template <typename T>
+__device__ __forceinline__ void put4(T (&a)[4], int i, T v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (i == k) a[k] = v;
+}
 
 template <int NQ>
 __device__ __forceinline__ Group load_group(const IndexParams& p, int g, bool flag_pos) {
@@ -90,20 +148,26 @@ __device__ __forceinline__ Group load_group(const IndexParams& p, int g, bool fl
     }
   }
 #pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    G.sub_seq[s] = -1;
+    G.sub_tiles[s] = 0;
+  }
+#pragma unroll
   for (int q = 0; q < NQ; ++q) {
     if (G.seq[q] < 0) continue;
     int k = -1;
-    for (int s = 0; s < G.n_sub; ++s)
-      if (G.sub_seq[s] == G.seq[q]) k = s;
+#pragma unroll
+    for (int s = 0; s < NQ; ++s)
+      if (s < G.n_sub && G.sub_seq[s] == G.seq[q]) k = s;
     if (k < 0) {
       k = G.n_sub++;
-      G.sub_seq[k] = G.seq[q];
-      G.sub_tiles[k] = 0;
+      put4(G.sub_seq, k, G.seq[q]);
     }
     const int tiles = (int)((G.nvis[q] + kTile - 1) / kTile);
-    if (tiles > G.sub_tiles[k]) G.sub_tiles[k] = tiles;
+    if (tiles > pick4(G.sub_tiles, k)) put4(G.sub_tiles, k, tiles);
   }
-  for (int s = 0; s < G.n_sub; ++s) G.units += G.sub_tiles[s];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) G.units += G.sub_tiles[s];
   return G;
 }
 
@@ -115,7 +179,7 @@ struct Walk {
   __device__ void settle(const IndexParams& p, int n_groups) {
     // move forward to the first existing unit at or after (g, s, t)
     while (g < n_groups) {
-      while (s < G.n_sub && t >= G.sub_tiles[s]) {
+      while (s < G.n_sub && t >= pick4(G.sub_tiles, s)) {
         ++s;
         t = 0;
       }
@@ -162,25 +226,25 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int* total) {
 }
 
 template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_constant__ IndexParams p) {
+__global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_constant__ IndexParams p,
+                                                                const __grid_constant__ CUtensorMap pages) {
   using Lay = Layout<NQ>;
   constexpr int N = Lay::N;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* stage = sm + Lay::off_stage;
-  uint8_t* abuf = sm + Lay::off_a;
-  uint8_t* bbuf = sm + Lay::off_b;
+  uint8_t* bbuf = sm + Lay::off_b;                          // [2][N rows x 128 bytes]
+  float* wsm = reinterpret_cast<float*>(sm + Lay::off_w);   // [2][NQ * 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::off_bar);
   uint64_t* full = bars;
   uint64_t* empty = bars + Lay::kStages;
-  uint64_t* afull = bars + 2 * Lay::kStages;
-  uint64_t* aempty = afull + 2;
-  uint64_t* tfull = afull + 4;
-  uint64_t* tempty = afull + 6;
-  uint64_t* bfull = afull + 8;
-  uint64_t* bempty = afull + 9;
-  uint64_t* done = afull + 10;
+  uint64_t* tfull = bars + 2 * Lay::kStages;   // [kAcc]
+  uint64_t* tempty = tfull + Lay::kAcc;
+  uint64_t* bfull = tempty + Lay::kAcc;  // [2] query operand ready (by group parity)
+  uint64_t* bempty = bfull + 2;    // [2] products of the group done
+  uint64_t* egone = bempty + 2;    // [2] epilogue left the group
+  uint64_t* done = egone + 2;
   int* misc = reinterpret_cast<int*>(sm + Lay::off_misc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
@@ -193,17 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
 
   if (tid == 0) {
     for (int i = 0; i < Lay::kStages; ++i) {
-      tc::mbar_init(full + i, 1);
-      tc::mbar_init(empty + i, 12);         // 8 converter + 4 epilogue warps
+      tc::mbar_init(full + i, 2);           // the tile's two page producers
+      tc::mbar_init(empty + i, 5);          // the tile's products + its four epilogue warps
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(afull + i, 8);
-      tc::mbar_init(aempty + i, 1);
+    for (int i = 0; i < Lay::kAcc; ++i) {
       tc::mbar_init(tfull + i, 1);
       tc::mbar_init(tempty + i, 4);
     }
-    tc::mbar_init(bfull, 8);
-    tc::mbar_init(bempty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bfull + i, 4);
+      tc::mbar_init(bempty + i, 1);
+      tc::mbar_init(egone + i, 8);
+    }
     tc::mbar_init(done, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -277,26 +342,27 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     // offset inside the group: walk its sub-passes (each step consumes at least one unit;
     // the walk stops at the end of the groups)
     while (off > 0 && start.g < n_groups) {
-      const int left = start.G.sub_tiles[start.s] - start.t;
+      const int left = pick4(start.G.sub_tiles, start.s) - start.t;
       if (left <= 0) break;
       if (off < left) {
         start.t += off;
         off = 0;
       } else {
         off -= left;
-        start.t = start.G.sub_tiles[start.s];
+        start.t = pick4(start.G.sub_tiles, start.s);
         start.settle(p, n_groups);
       }
     }
   }
 
-  constexpr uint32_t idesc = tc::idesc_bf16(kTile, N);
-  const int8_t* idx_data = reinterpret_cast<const int8_t*>(p.idx.data);
+  constexpr uint32_t idesc = idesc_e4m3(kTile, N);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 0 || warp >= kProd1) {
+    // ------------------------------------------------------------------ producers
+    const int pw = warp == 0 ? 0 : warp - kProd1 + 1;
+    const int ph = pw & 1, parity = pw >> 1;            // page of the tile, tiles i % 2 == parity
     // The whole warp keeps the page ids of 32 consecutive blocks (16 tiles) of the current
-    // sequence in registers, one per lane; lane 0 waits on the ring and issues the copies.
+    // sequence in registers, one per lane; lane 0 waits on the ring and issues the copy.
     if (n_units > 0) {
       Walk<NQ> w = start;
       int issued = 0;
@@ -307,8 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         if (w.g >= n_groups) break;                    // every role stops at the same tile
+        if ((i & 1) != parity) {                       // the other pair's tile (stages of
+          w.next(p, n_groups);                         // one parity: kStages is even)
+          continue;
+        }
         const int st = i % Lay::kStages;
-        const int seq = w.G.sub_seq[w.s];
+        const int seq = pick4(w.G.sub_seq, w.s);
         const int64_t blk0 = 2 * (int64_t)w.t;
         if (seq != cache_seq || blk0 < cache_blk0 || blk0 + 1 >= cache_blk0 + 32) {   // warp-uniform
           cache_seq = seq;
@@ -323,42 +393,28 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane == 0) {
         uint8_t* sb = stage + st * kStageStride;
-        int64_t src[2];
-        int nv = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int32_t page = h ? pg1 : pg0;
-          src[h] = -1;
-          int status = -1;                              // no page
-          if (page >= p.idx.n_pages) status = -2;       // page id outside the pool
-          if (page >= 0 && page < p.idx.n_pages) {
-            src[h] = page;
-            status = 0;
-            ++nv;
+        const int32_t page = ph ? pg1 : pg0;
+        bool copied = false;
+        if (lane == 0) {
+          const bool valid = page >= 0 && page < p.idx.n_pages;
+          reinterpret_cast<int*>(sb + kStageMetaOff)[ph] = valid ? page : (page >= p.idx.n_pages ? -2 : -1);
+          if (valid) {
+            tc::mbar_arrive_tx(full + st, kPageBytes);
+            tma_load_2d(sb + ph * kPageBytes, &pages, 0, page * 64, full + st);
+            copied = true;
+          } else {
+            tc::mbar_arrive(full + st);
           }
-          reinterpret_cast<int*>(sb + kStageMetaOff)[h] = status;
         }
-        if (nv) {
-          tc::mbar_arrive_tx(full + st, (uint32_t)(nv * (64 * kDI + 64 * 4)));
-          for (int h = 0; h < 2; ++h)
-            if (src[h] >= 0) {
-              tc::bulk_g2s(sb + h * 64 * kDI, idx_data + src[h] * 64 * kDI, 64 * kDI, full + st);
-              tc::bulk_g2s(sb + kStageScaleOff + h * 256, p.idx.scale + src[h] * 64, 256, full + st);
-            }
-          had_copy |= 1u << st;
-        } else {
-          tc::mbar_arrive(full + st);
-          had_copy &= ~(1u << st);
-        }
-        }
+        if (copied) had_copy |= 1u << st;
+        else had_copy &= ~(1u << st);
         issued = i + 1;
         w.next(p, n_groups);
       }
-      if (lane == 0 && *abort_flag) {   // drain copies still in flight
+      if (lane == 0 && *abort_flag) {   // drain this warp's copies still in flight
         for (int i = issued > Lay::kStages ? issued - Lay::kStages : 0; i < issued; ++i)
-          if (had_copy & (1u << (i % Lay::kStages)))
+          if ((i & 1) == parity && (had_copy & (1u << (i % Lay::kStages))))
             tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
       }
     }
@@ -366,154 +422,188 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_units > 0) {
       Walk<NQ> w = start;
-      int prev_g = -1, gc = 0;
-      const uint32_t a0 = tc::smem_u32(abuf), b0 = tc::smem_u32(bbuf);
+      int prev_g = -1, gc = -1;
+      const uint32_t s0 = tc::smem_u32(stage), b0 = tc::smem_u32(bbuf);
       for (int i = 0; i < n_units; ++i) {
         if (w.g >= n_groups) break;
         if (w.g != prev_g) {
-          if (!tc::mbar_wait(bfull, gc & 1, abort_flag, p.err)) break;
           ++gc;
+          if (!tc::mbar_wait(bfull + (gc & 1), (gc >> 1) & 1, abort_flag, p.err)) break;
           prev_g = w.g;
         }
-        const int ab = i & 1;
-        if (!tc::mbar_wait(afull + ab, (i >> 1) & 1, abort_flag, p.err)) break;
-        if (!tc::mbar_wait(tempty + ab, ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+        const int st = i % Lay::kStages, tb = i % Lay::kAcc;
+        if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
+        if (!tc::mbar_wait(tempty + tb, ((i / Lay::kAcc) & 1) ^ 1, abort_flag, p.err)) break;
         tc::fence_after_sync();
-        const uint32_t d = tmem + ab * N;
+        const uint32_t d = tmem + tb * N;
+        const uint32_t a_base = s0 + st * kStageStride, b_base = b0 + (gc & 1) * Lay::kBBytes;
 #pragma unroll
-        for (int k = 0; k < kDI / 16; ++k) {
-          const uint32_t koff = (k & 3) * 32u;   // 16 bf16 = 32 bytes inside the swizzle row
-          const uint64_t ad = tc::sdesc_sw128(a0 + ab * kABytes + (k >> 2) * (kTile * 128) + koff, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(b0 + (k >> 2) * (N * 128) + koff, 16, 1024);
-          tc::mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+        for (int k = 0; k < kDI / 32; ++k) {   // K = 32 codes = 32 bytes inside the swizzle row
+          const uint64_t ad = tc::sdesc_sw128(a_base + k * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(b_base + k * 32, 16, 1024);
+          mma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(aempty + ab);
-        tc::mma_commit(tfull + ab);
+        tc::mma_commit(empty + st);
+        tc::mma_commit(tfull + tb);
         const int g_here = w.g;
         w.next(p, n_groups);
-        if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty);
+        if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty + (gc & 1));
       }
       tc::mma_commit(done);
       tc::mbar_wait_drain(done, 0);
     }
     __syncwarp();
-  } else if (warp >= kConv0 && warp < kEpi0) {
-    // ------------------------------------------------------------------ converters
-    const int ct = tid - kConv0 * 32;
+  } else if (warp >= kPrep0 && warp < kProd1) {
+    // ------------------------------------------------------------------ query preparation
+    // Per group: B rows qq*128 + h (hi) and qq*128 + 64 + h (lo), 128 bytes each, K-major
+    // 128B-swizzled; wsm = w_h / s_h. Warp pw prepares heads pw*16 .. pw*16+15 of every
+    // query of the group: lane l takes head pw*16 + l/2, dims 64*(l&1) .. +63 (the head's
+    // max needs one exchange with the neighbouring lane).
+    const int pw = warp - kPrep0;
+    const int h = pw * 16 + (lane >> 1), dh = lane & 1;
     Walk<NQ> w = start;
-    int prev_g = -1, gc = 0;
+    int prev_g = -1, gc = -1;
+    const __nv_bfloat16* qsrc = reinterpret_cast<const __nv_bfloat16*>(p.q_idx);
     for (int i = 0; i < n_units; ++i) {
       if (w.g >= n_groups) break;
       if (w.g != prev_g) {
-        if (gc > 0 && !tc::mbar_wait(bempty, (gc - 1) & 1, abort_flag, p.err)) break;
-        // the group's queries -> B operand [N rows = query*64 + head][128 dims]
-        const __nv_bfloat16* qsrc = reinterpret_cast<const __nv_bfloat16*>(p.q_idx);
+        ++gc;
+        prev_g = w.g;
+        const int b = gc & 1;
+        if (gc >= 2) {   // the buffer's previous group: its products and epilogue are done
+          const uint32_t par = ((gc >> 1) - 1) & 1;
+          if (!tc::mbar_wait(bempty + b, par, abort_flag, p.err)) break;
+          if (!tc::mbar_wait(egone + b, par, abort_flag, p.err)) break;
+        }
+        uint8_t* bb = bbuf + b * Lay::kBBytes;
 #pragma unroll 1
-        for (int base = 0; base < N * 16; base += kConvThreads * 8) {   // 8 loads in flight per thread
-          uint4 v[8];
+        for (int qq = 0; qq < NQ; ++qq) {
+          const int qi = w.g * NQ + qq;
+          uint4 v[8];                                  // 64 bf16
+          const uint4* src = reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + h) * kDI + dh * 64);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int item = base + k * kConvThreads + ct;
-            const int n = item >> 4, c = item & 15;
-            const int qi = w.g * NQ + n / kHI;
-            v[k] = (item < N * 16 && qi < p.n_q)
-                       ? __ldg(reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + (n % kHI)) * kDI) + c)
-                       : make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < 8; ++c) v[c] = qi < p.n_q ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          const float wh = qi < p.n_q ? __ldg(p.w + (int64_t)qi * kHI + h) : 0.f;
+          float amax = 0.f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int item = base + k * kConvThreads + ct;
-            const int n = item >> 4, c = item & 15;
-            if (item < N * 16)                           // N rows x 16 chunks of 16 bytes
-              *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + tc::sw128_off(n, c & 7)) = v[k];
+          for (int c = 0; c < 8; ++c) {
+            const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[c]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __bfloat1622float2(e[j]);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
           }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          // s = 2^(7 - ex) with amax = f * 2^ex, f in [1, 2): max |q * s| < 256 <= 448
+          int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+          if (!(amax > 0.f) || ex < -100 || ex > 100) ex = 7;   // zero, tiny or huge row: s = 1
+          const float sc = __uint_as_float((uint32_t)(127 + 7 - ex) << 23);
+          const float inv_s = __uint_as_float((uint32_t)(127 - 7 + ex) << 23);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {               // 16 dims -> one 16-byte chunk each
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[2 * c + (k >> 1)]);
+              uint32_t hp = 0, lp = 0;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float2 f = __bfloat1622float2(e[2 * (k & 1) + j]);
+                const float a0 = f.x * sc, a1 = f.y * sc;   // exact (power of two)
+                const __nv_fp8x2_storage_t h2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+                const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3);
+                const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+                const __nv_fp8x2_storage_t l2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(a0 - hf.x, a1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+                hp |= (uint32_t)h2 << (16 * j);
+                lp |= (uint32_t)l2 << (16 * j);
+              }
+              hw[k] = hp;
+              lw[k] = lp;
+            }
+            const int chunk = dh * 4 + c;               // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(bb + tc::sw128_off(qq * 128 + h, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(bb + tc::sw128_off(qq * 128 + 64 + h, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+          if (dh == 0) wsm[b * NQ * kHI + qq * kHI + h] = wh * inv_s;
         }
         tc::fence_proxy_async();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bfull);
-        ++gc;
-        prev_g = w.g;
-      }
-      const int st = i % Lay::kStages, ab = i & 1;
-      if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
-      if (!tc::mbar_wait(aempty + ab, ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-      const uint8_t* src = stage + st * kStageStride;
-      uint8_t* dst = abuf + ab * kABytes;
-      uint4 raw[kTile * 8 / kConvThreads];
-#pragma unroll
-      for (int k = 0; k < kTile * 8 / kConvThreads; ++k)
-        raw[k] = *reinterpret_cast<const uint4*>(src + (ct + k * kConvThreads) * 16);
-#pragma unroll
-      for (int k = 0; k < kTile * 8 / kConvThreads; ++k) {
-        const int item = ct + k * kConvThreads;
-        const int r = item >> 3, v = item & 7;      // 16 codes = dims 16v .. 16v+15
-        uint4 lo, hi;
-        e4m3x16_to_bf16x16(raw[k], lo, hi);
-        const int c0 = 2 * v;                        // bf16 chunk index over 128 dims
-        *reinterpret_cast<uint4*>(dst + (c0 >> 3) * (kTile * 128) + tc::sw128_off(r, c0 & 7)) = lo;
-        *reinterpret_cast<uint4*>(dst + ((c0 + 1) >> 3) * (kTile * 128) + tc::sw128_off(r, (c0 + 1) & 7)) = hi;
-      }
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(afull + ab);
-        tc::mbar_arrive(empty + st);
+        if (lane == 0) tc::mbar_arrive(bfull + b);
       }
       w.next(p, n_groups);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    const int es = (warp - kEpi0) >> 2;         // set: tiles i % 2 == es
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     Walk<NQ> w = start;
+    int prev_g = -1, gc = -1;
     for (int i = 0; i < n_units; ++i) {
       if (w.g >= n_groups) break;
-      const int ab = i & 1, st = i % Lay::kStages;
-      // the tile's page status and row scales arrive with its codes in the stage
+      if (w.g != prev_g) {
+        if (gc >= 0 && lane == 0) tc::mbar_arrive(egone + (gc & 1));   // left the previous group
+        ++gc;
+        prev_g = w.g;
+      }
+      if ((i & 1) != es) {
+        w.next(p, n_groups);
+        continue;
+      }
+      const int tb = i % Lay::kAcc, st = i % Lay::kStages, b = gc & 1;
+      // the tile's page ids arrive with its codes; the row scale load is issued now and
+      // used after the product
       if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
       const uint8_t* sb = stage + st * kStageStride;
-      const int status = reinterpret_cast<const int*>(sb + kStageMetaOff)[row >> 6];
-      const float sc = status == 0 ? reinterpret_cast<const float*>(sb + kStageScaleOff)[row] : 0.f;
-      if (!tc::mbar_wait(tfull + ab, (i >> 1) & 1, abort_flag, p.err)) break;
+      const int page = reinterpret_cast<const int*>(sb + kStageMetaOff)[row >> 6];
+      const float sc = page >= 0 ? __ldg(p.idx.scale + (int64_t)page * 64 + (row & 63)) : 0.f;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty + st);
+      if (!tc::mbar_wait(bfull + b, (gc >> 1) & 1, abort_flag, p.err)) break;   // w / s of the group
+      if (!tc::mbar_wait(tfull + tb, (i / Lay::kAcc) & 1, abort_flag, p.err)) break;
       tc::fence_after_sync();
-      const int seq = w.G.sub_seq[w.s];
+      const int seq = pick4(w.G.sub_seq, w.s);
       const int64_t j = (int64_t)w.t * kTile + row;
+      const float* wq = wsm + b * NQ * kHI;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        if (w.G.seq[q] != seq) continue;            // warp-uniform
-        float s = 0.f;
+      for (int qq = 0; qq < NQ; ++qq) {
+        if (w.G.seq[qq] != seq) continue;           // warp-uniform
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};       // four chains instead of one
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float acc[32];
-          tc::tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + ab * N + q * kHI + half * 32, acc);
+          float hi[32], lo[32];
+          const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + tb * N + qq * 128 + half * 32;
+          tc::tmem_ld32(col, hi);
+          tc::tmem_ld32(col + 64, lo);
           tc::tmem_wait_ld();
-          const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)(w.g * NQ + q) * kHI + half * 32);
+          const float4* w4 = reinterpret_cast<const float4*>(wq + qq * kHI + half * 32);
 #pragma unroll
           for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 ww = __ldg(wv + h4);
-            s = fmaf(ww.x, fmaxf(acc[4 * h4], 0.f), s);
-            s = fmaf(ww.y, fmaxf(acc[4 * h4 + 1], 0.f), s);
-            s = fmaf(ww.z, fmaxf(acc[4 * h4 + 2], 0.f), s);
-            s = fmaf(ww.w, fmaxf(acc[4 * h4 + 3], 0.f), s);
+            const float4 ww = w4[h4];
+            s4[0] = fmaf(ww.x, fmaxf(hi[4 * h4] + lo[4 * h4], 0.f), s4[0]);
+            s4[1] = fmaf(ww.y, fmaxf(hi[4 * h4 + 1] + lo[4 * h4 + 1], 0.f), s4[1]);
+            s4[2] = fmaf(ww.z, fmaxf(hi[4 * h4 + 2] + lo[4 * h4 + 2], 0.f), s4[2]);
+            s4[3] = fmaf(ww.w, fmaxf(hi[4 * h4 + 3] + lo[4 * h4 + 3], 0.f), s4[3]);
           }
         }
-        if (j < w.G.nvis[q] && w.g * NQ + q < p.n_q) {
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (j < w.G.nvis[qq] && w.g * NQ + qq < p.n_q) {
           float out;
-          if (status == 0) {
+          if (page >= 0) {
             out = s * sc + 0.0f;
           } else {
-            raise_err(p.err, status == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+            raise_err(p.err, page == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
             out = -INFINITY;
           }
-          p.scores[(int64_t)(w.g * NQ + q) * p.row_stride + j] = out;
+          p.scores[(int64_t)(w.g * NQ + qq) * p.row_stride + j] = out;
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(tempty + ab);
-        tc::mbar_arrive(empty + st);
-      }
+      if (lane == 0) tc::mbar_arrive(tempty + tb);
       w.next(p, n_groups);
     }
   }
@@ -526,28 +616,54 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (looked up once).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
 template <int NQ>
 cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   using Lay = Layout<NQ>;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // the pool as a 2-D byte tensor [n_pages * 64 rows][128], one page per box, 128B swizzle
+  CUtensorMap map;
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDI, (cuuint64_t)p.idx.n_pages * 64};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDI};
+  const cuuint32_t box[2] = {(cuuint32_t)kDI, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.idx.data, dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const int64_t n_groups = (p.n_q + NQ - 1) / NQ;
   const int64_t max_units = n_groups * NQ * ((max_vis + kTile - 1) / kTile);
   const int grid = (int)(max_units < sms ? (max_units > 0 ? max_units : 1) : sms);
   cudaError_t e = cudaFuncSetAttribute(index_scores_tc<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Lay::bytes);
   if (e != cudaSuccess) return e;
-  index_scores_tc<NQ><<<grid, kThreads, Lay::bytes, st>>>(p);
+  index_scores_tc<NQ><<<grid, kThreads, Lay::bytes, st>>>(p, map);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // Tensor-core path for bf16 queries and fp8 keys with 64 heads of dim 128. Many queries
-// (prefill) are taken four at a time (N = 256) so each key tile feeds four queries.
+// (prefill) are taken two at a time (N = 256) so each key tile feeds two queries.
 cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
-  if (p.n_q >= 1024) return launch_tc<4>(p, max_vis, st);
+  if (p.idx.n_pages <= 0 || p.idx.n_pages * 64 > INT32_MAX) return cudaErrorInvalidValue;
+  if (p.n_q >= 1024) return launch_tc<2>(p, max_vis, st);
   return launch_tc<1>(p, max_vis, st);
 }
 
