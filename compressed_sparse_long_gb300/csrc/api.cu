@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 2;
+constexpr int32_t kVersion = 3;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -319,6 +319,8 @@ namespace v4a {
 namespace {
 __global__ void slot_mapping_kernel(CacheView c, int32_t n, const int32_t* seq, const int64_t* row,
                                     int32_t* slots, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int64_t s = slot_of(c, __ldg(seq + i), __ldg(row + i));
@@ -329,7 +331,9 @@ __global__ void slot_mapping_kernel(CacheView c, int32_t n, const int32_t* seq, 
 
 int launch_slot_mapping(const CacheView& c, int32_t n, const int32_t* seq, const int64_t* row,
                         int32_t* slots, int32_t* err, cudaStream_t st) {
-  slot_mapping_kernel<<<(n + 255) / 256, 256, 0, st>>>(c, n, seq, row, slots, err);
+  if (launch_pdl(slot_mapping_kernel, dim3((n + 255) / 256), dim3(256), 0, st, c, n, seq, row, slots, err) !=
+      cudaSuccess)
+    return V4A_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

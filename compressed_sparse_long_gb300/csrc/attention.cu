@@ -52,6 +52,8 @@ __device__ __forceinline__ KeyRef key_ref(const AttnParams& p, int qi, int seq, 
 // Warp w owns heads w*HPW .. w*HPW+HPW-1; lane l owns dims l, l+32, ... of every head.
 template <typename QT, bool kFp8, typename OT, int H, int D>
 __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int HPW = H / 8;
   constexpr int DPL = D / 32;
   constexpr int KS = D + 1;                      // padded key row (conflict-free columns)
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
 // group of splits are issued before they are used.
 template <typename OT, int kPairs>
 __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x, h = blockIdx.y * 8 + warp;
   if (h >= p.H) return;
@@ -301,11 +305,11 @@ cudaError_t launch_simt(const AttnParams& p, cudaStream_t st) {
   cudaFuncSetAttribute(attn_simt<QT, kFp8, OT, H, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   dim3 grid((unsigned)p.n_split, (unsigned)p.n_q);
-  attn_simt<QT, kFp8, OT, H, D><<<grid, kThreads, smem, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_simt<QT, kFp8, OT, H, D>, grid, dim3(kThreads), smem, st, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split == 1) return e;
-  attn_merge<OT, D / 64><<<dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(attn_merge<OT, D / 64>, dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), dim3(256), 0, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -317,8 +321,8 @@ int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
   {
     e = launch_attention_tc(p, st);
     if (e == cudaSuccess && p.n_split > 1) {
-      attn_merge<__nv_bfloat16, 8><<<dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), 256, 0, st>>>(p);
-      e = cudaGetLastError();
+      e = launch_pdl(attn_merge<__nv_bfloat16, 8>, dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), dim3(256), 0, st, p);
+      if (e == cudaSuccess) e = cudaGetLastError();
     }
   }
   else if (dtype == V4A_FP32 && p.H == 8 && p.D == 128)

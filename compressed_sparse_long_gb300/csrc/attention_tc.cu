@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = p.n_q * p.n_split;
+  // On-chip setup and the first query's Q~ read only this call's inputs and overlap the
+  // previous kernel; the key gathers (top-k lists, pools) and every global write wait.
+  pdl_trigger();
 
   if (tid == 0) {
     for (int b = 0; b < 4; ++b) {
@@ -268,10 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
                         : make_uint4(0, 0, 0, 0);
       }
     };
+    bool waited = false;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = make_item(p, it);
       if (I.n_tiles == 0) continue;
-      issue(I, 0);                                  // tile 0 of the item in flight
+      if (waited) issue(I, 0);                      // tile 0 of the item in flight
       // Q~ = RoPE(q, p) * scale * log2(e), bf16, K-major 128B-swizzled [64 heads][512]
       if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
       {
@@ -320,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(qfull);
       }
+      if (!waited) {                                // first item: Q~ was built meanwhile
+        pdl_wait();
+        waited = true;
+        issue(I, 0);
+      }
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
         for (int b = 0; b < 4; ++b) {
           if (!tc::mbar_wait(kempty + b, (gi & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     }
   } else if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
+    pdl_wait();
     // ------------------------------------------------------------ softmax + epilogue
     // Every lane keeps the running max of heads `lane` and `lane + 32` in registers (all
     // four warps hold the same copy); the owner of head h (thread row h) keeps its
@@ -614,11 +624,13 @@ cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st) {
   if (p.n_split > 1) {
     e = cudaFuncSetAttribute(attn_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_tc<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+    e = launch_pdl(attn_tc<true>, dim3(grid), dim3(kThreads), kSmemBytes, st, p);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_tc<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+    e = launch_pdl(attn_tc<false>, dim3(grid), dim3(kThreads), kSmemBytes, st, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

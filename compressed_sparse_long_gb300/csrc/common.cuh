@@ -2,6 +2,8 @@
 // fp8 e4m3 <-> fp32/bf16 conversion, warp reductions, the device error word.
 #pragma once
 
+#include <utility>
+
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -210,6 +212,31 @@ __device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4& u, uint4& lo, ui
 }
 
 __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch. Every kernel of the library lets the next kernel of its
+// stream start early (pdl_trigger, at its start) and, in each thread, waits for the kernels
+// before it (pdl_wait: they have completed and their memory is visible) before it reads
+// memory one of them may write or writes memory one of them may read. Work on the call's
+// own inputs (queries, positions, block tables, weights) and on-chip setup may run before
+// the wait, overlapping the previous kernel. Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Number of entries visible to a query at p: entry j qualifies iff its last covered
 // position S*j + win_off + W - 1 is < p.

@@ -261,6 +261,8 @@ struct CompressKernel {
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_constant__ CompressParams p) {
+  pdl_trigger();
+  pdl_wait();
   CompressKernel<TIn, CPL, ICPL, kFp8>::run(p);
 }
 
@@ -268,8 +270,8 @@ template <typename TIn, int CPL, int ICPL, bool kFp8>
 cudaError_t launch(const CompressParams& p, cudaStream_t st) {
   const int threads = 256;
   const int64_t blocks = (p.n_tokens * 32 + threads - 1) / threads;
-  compress_insert_kernel<TIn, CPL, ICPL, kFp8><<<(unsigned)blocks, threads, 0, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(compress_insert_kernel<TIn, CPL, ICPL, kFp8>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -24,6 +24,8 @@ namespace {
 // One thread per entry, the query's heads in shared memory (broadcast reads).
 template <typename T, bool kFp8, int HI, int DI>
 __global__ void __launch_bounds__(128) index_scores_simt(const __grid_constant__ IndexParams p) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float qs[HI * DI];
   __shared__ float ws[HI];
   const int qi = blockIdx.y;
@@ -118,6 +120,8 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* warp_to
 
 template <bool kSmem>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ IndexParams p) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t row_keys[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t whist[kTopkWarps][256];   // per-warp histograms (no cross-warp contention)
@@ -236,6 +240,8 @@ __device__ __forceinline__ float key_value(uint32_t u) {   // inverse of order_k
 // (above, equal) ballot counts.
 template <int ITEMS, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_constant__ IndexParams p) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kWarps = THREADS / 32;
   constexpr int kCnt = ITEMS * kWarps;
   static_assert(kCnt % 32 == 0, "count table splits over one warp");
@@ -466,8 +472,8 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
 template <typename T, bool kFp8, int HI, int DI>
 cudaError_t launch_simt(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   dim3 grid((unsigned)((max_vis + 127) / 128), (unsigned)p.n_q);
-  index_scores_simt<T, kFp8, HI, DI><<<grid, 128, 0, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(index_scores_simt<T, kFp8, HI, DI>, grid, dim3(128), 0, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -490,9 +496,9 @@ int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.n_q == 0) return V4A_OK;
   cudaError_t e;
   if (max_vis <= 16 * 512) {
-    topk_reg_kernel<16, 512><<<p.n_q, 512, 0, st>>>(p);
+    e = launch_pdl(topk_reg_kernel<16, 512>, dim3(p.n_q), dim3(512), 0, st, p);
   } else if (max_vis <= 32 * 1024) {
-    topk_reg_kernel<32, 1024><<<p.n_q, 1024, 0, st>>>(p);
+    e = launch_pdl(topk_reg_kernel<32, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
   } else if (max_vis <= kTopkSmemMax) {
     const size_t smem = (size_t)max_vis * sizeof(uint32_t);
     static bool attr_set = false;
@@ -501,11 +507,11 @@ int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
                            kTopkSmemMax * (int)sizeof(uint32_t));
       attr_set = true;
     }
-    topk_kernel<true><<<p.n_q, kTopkThreads, smem, st>>>(p);
+    e = launch_pdl(topk_kernel<true>, dim3(p.n_q), dim3(kTopkThreads), smem, st, p);
   } else {
-    topk_kernel<false><<<p.n_q, kTopkThreads, 0, st>>>(p);
+    e = launch_pdl(topk_kernel<false>, dim3(p.n_q), dim3(kTopkThreads), 0, st, p);
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

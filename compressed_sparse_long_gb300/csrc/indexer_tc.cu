@@ -20,16 +20,16 @@
 // products and the head sum is a per-thread loop in the epilogue.
 //
 // One persistent CTA per SM, warp-specialised, every hand-off an mbarrier:
-//   warps 0,14-16 producers: a tile's two pages are copied into one ring stage by two
-//               warps, one per page; even tiles go to warps 0 and 14, odd tiles to 15 and
-//               16 (a warp serialises its bulk copies, ~0.3 us each). Each warp arms the
+//   warps 0,12-14 producers: a tile's two pages are copied into one ring stage by two
+//               warps, one per page; even tiles go to warps 0 and 12, odd tiles to 13 and
+//               14 (a warp serialises its bulk copies, ~0.3 us each). Each warp arms the
 //               stage barrier with its own bytes and leaves its page id (or status) there.
 //   warp 1      MMA: allocates TMEM, one thread issues 4 tcgen05.mma per tile into one of
 //               four accumulators (two for two queries per group); commits release the
 //               stage and hand the tile over
 //   warps 2-9   epilogue, two sets of four (one per TMEM lane quadrant) taking even and
 //               odd tiles: tcgen05.ld, hi + lo, ReLU, weighted head sum, row scale, store
-//   warps 10-13 query preparation: the hi/lo B operand and w/s of each query group, double
+//   warps 10-11 query preparation: the hi/lo B operand and w/s of each query group, double
 //               buffered across groups
 // Work: units = (query group, sequence sub-pass, tile); each CTA takes a contiguous slice
 // of the units of all groups (found with a block scan), so long and short rows balance.
@@ -55,9 +55,9 @@ constexpr int kStageBytes = kTile * kDI;    // codes of one tile (two pages)
 // stay 1 KB aligned for the swizzled copies
 constexpr int kStageMetaOff = kStageBytes;
 constexpr int kStageStride = kStageBytes + 1024;
-constexpr int kThreads = 544;              // 17 warps
+constexpr int kThreads = 480;              // 15 warps (128 registers a thread)
 constexpr int kEpi0 = 2, kPrep0 = 10;       // first epilogue / query-preparation warp
-constexpr int kProd1 = 14;                  // producers: warp 0 and warps 14-16
+constexpr int kProd1 = 12;                  // producers: warp 0 and warps 12-14
 
 template <int NQ>
 struct Layout {
@@ -173,25 +173,33 @@ __device__ __forceinline__ Group load_group(const IndexParams& p, int g, bool fl
 
 // Position in the CTA's unit sequence: group, sub-pass, tile.
 template <int NQ>
+// The sub-pass's tile count and sequence are cached so that the per-tile step is one
+// increment and compare; the group state is consulted only when a sub-pass ends.
 struct Walk {
   int g, s, t;
+  int t_lim;   // tiles of sub-pass s
+  int seq;     // sequence of sub-pass s
   Group G;
-  __device__ void settle(const IndexParams& p, int n_groups) {
+  __device__ __forceinline__ void settle(const IndexParams& p, int n_groups) {
     // move forward to the first existing unit at or after (g, s, t)
     while (g < n_groups) {
       while (s < G.n_sub && t >= pick4(G.sub_tiles, s)) {
         ++s;
         t = 0;
       }
-      if (s < G.n_sub) return;
+      if (s < G.n_sub) {
+        t_lim = pick4(G.sub_tiles, s);
+        seq = pick4(G.sub_seq, s);
+        return;
+      }
       ++g;
       s = 0;
       t = 0;
       if (g < n_groups) G = load_group<NQ>(p, g, false);
     }
   }
-  __device__ void next(const IndexParams& p, int n_groups) {
-    ++t;
+  __device__ __forceinline__ void next(const IndexParams& p, int n_groups) {
+    if (++t < t_lim) return;
     settle(p, n_groups);
   }
 };
@@ -254,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_groups = (p.n_q + NQ - 1) / NQ;
+  // The setup, the work partition and the query preparation read only this call's inputs
+  // and run while the previous kernel finishes; the producers (pages the insert writes)
+  // and the epilogue (row scales, scores) wait for it first.
+  pdl_trigger();
 
   if (tid == 0) {
     for (int i = 0; i < Lay::kStages; ++i) {
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       tc::mbar_init(tempty + i, 4);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(bfull + i, 4);
+      tc::mbar_init(bfull + i, kProd1 - kPrep0);   // the preparation warps
       tc::mbar_init(bempty + i, 1);
       tc::mbar_init(egone + i, 8);
     }
@@ -363,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     const int ph = pw & 1, parity = pw >> 1;            // page of the tile, tiles i % 2 == parity
     // The whole warp keeps the page ids of 32 consecutive blocks (16 tiles) of the current
     // sequence in registers, one per lane; lane 0 waits on the ring and issues the copy.
+    pdl_wait();
     if (n_units > 0) {
       Walk<NQ> w = start;
       int issued = 0;
@@ -378,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
           continue;
         }
         const int st = i % Lay::kStages;
-        const int seq = pick4(w.G.sub_seq, w.s);
+        const int seq = w.seq;
         const int64_t blk0 = 2 * (int64_t)w.t;
         if (seq != cache_seq || blk0 < cache_blk0 || blk0 + 1 >= cache_blk0 + 32) {   // warp-uniform
           cache_seq = seq;
@@ -420,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_units > 0) {
+    // The whole warp walks the units and waits (a converged warp); lane 0 issues.
+    if (n_units > 0) {
       Walk<NQ> w = start;
       int prev_g = -1, gc = -1;
       const uint32_t s0 = tc::smem_u32(stage), b0 = tc::smem_u32(bbuf);
@@ -428,39 +442,42 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         if (w.g >= n_groups) break;
         if (w.g != prev_g) {
           ++gc;
-          if (!tc::mbar_wait(bfull + (gc & 1), (gc >> 1) & 1, abort_flag, p.err)) break;
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(bfull + (gc & 1), (gc >> 1) & 1, abort_flag, p.err))) break;
           prev_g = w.g;
         }
         const int st = i % Lay::kStages, tb = i % Lay::kAcc;
-        if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
-        if (!tc::mbar_wait(tempty + tb, ((i / Lay::kAcc) & 1) ^ 1, abort_flag, p.err)) break;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err))) break;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(tempty + tb, ((i / Lay::kAcc) & 1) ^ 1, abort_flag, p.err))) break;
         tc::fence_after_sync();
-        const uint32_t d = tmem + tb * N;
-        const uint32_t a_base = s0 + st * kStageStride, b_base = b0 + (gc & 1) * Lay::kBBytes;
-#pragma unroll
-        for (int k = 0; k < kDI / 32; ++k) {   // K = 32 codes = 32 bytes inside the swizzle row
-          const uint64_t ad = tc::sdesc_sw128(a_base + k * 32, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(b_base + k * 32, 16, 1024);
-          mma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(empty + st);
-        tc::mma_commit(tfull + tb);
         const int g_here = w.g;
         w.next(p, n_groups);
-        if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty + (gc & 1));
+        if (lane == 0) {
+          const uint32_t d = tmem + tb * N;
+          const uint64_t ad0 = tc::sdesc_sw128(s0 + st * kStageStride, 16, 1024);
+          const uint64_t bd0 = tc::sdesc_sw128(b0 + (gc & 1) * Lay::kBBytes, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < kDI / 32; ++k)   // K = 32 codes = 32 bytes = 2 descriptor units
+            mma_e4m3(d, ad0 + (uint64_t)(2 * k), bd0 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+          tc::mma_commit(empty + st);
+          tc::mma_commit(tfull + tb);
+          if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty + (gc & 1));
+        }
+        __syncwarp();
       }
-      tc::mma_commit(done);
-      tc::mbar_wait_drain(done, 0);
+      if (lane == 0) {
+        tc::mma_commit(done);
+        tc::mbar_wait_drain(done, 0);
+      }
     }
     __syncwarp();
   } else if (warp >= kPrep0 && warp < kProd1) {
     // ------------------------------------------------------------------ query preparation
     // Per group: B rows qq*128 + h (hi) and qq*128 + 64 + h (lo), 128 bytes each, K-major
-    // 128B-swizzled; wsm = w_h / s_h. Warp pw prepares heads pw*16 .. pw*16+15 of every
-    // query of the group: lane l takes head pw*16 + l/2, dims 64*(l&1) .. +63 (the head's
-    // max needs one exchange with the neighbouring lane).
+    // 128B-swizzled; wsm = w_h / s_h. Warp pw prepares heads pw*32 .. pw*32+31 of every
+    // query of the group, 16 at a time: lane l takes head pw*32 + 16*pass + l/2, dims
+    // 64*(l&1) .. +63 (the head's max needs one exchange with the neighbouring lane).
     const int pw = warp - kPrep0;
-    const int h = pw * 16 + (lane >> 1), dh = lane & 1;
+    const int dh = lane & 1;
     Walk<NQ> w = start;
     int prev_g = -1, gc = -1;
     const __nv_bfloat16* qsrc = reinterpret_cast<const __nv_bfloat16*>(p.q_idx);
@@ -477,7 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         }
         uint8_t* bb = bbuf + b * Lay::kBBytes;
 #pragma unroll 1
-        for (int qq = 0; qq < NQ; ++qq) {
+        for (int pass = 0; pass < 2 * NQ; ++pass) {
+          const int qq = pass >> 1;
+          const int h = pw * 32 + (pass & 1) * 16 + (lane >> 1);
           const int qi = w.g * NQ + qq;
           uint4 v[8];                                  // 64 bf16
           const uint4* src = reinterpret_cast<const uint4*>(qsrc + ((int64_t)qi * kHI + h) * kDI + dh * 64);
@@ -537,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    pdl_wait();
     const int es = (warp - kEpi0) >> 2;         // set: tiles i % 2 == es
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -565,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       if (!tc::mbar_wait(bfull + b, (gc >> 1) & 1, abort_flag, p.err)) break;   // w / s of the group
       if (!tc::mbar_wait(tfull + tb, (i / Lay::kAcc) & 1, abort_flag, p.err)) break;
       tc::fence_after_sync();
-      const int seq = pick4(w.G.sub_seq, w.s);
+      const int seq = w.seq;
       const int64_t j = (int64_t)w.t * kTile + row;
       const float* wq = wsm + b * NQ * kHI;
 #pragma unroll
@@ -573,15 +593,15 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         if (w.G.seq[qq] != seq) continue;           // warp-uniform
         float s4[4] = {0.f, 0.f, 0.f, 0.f};       // four chains instead of one
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float hi[32], lo[32];
-          const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + tb * N + qq * 128 + half * 32;
-          tc::tmem_ld32(col, hi);
-          tc::tmem_ld32(col + 64, lo);
+        for (int qt = 0; qt < 4; ++qt) {          // 16 heads at a time (fewer live registers)
+          float hi[16], lo[16];
+          const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + tb * N + qq * 128 + qt * 16;
+          tc::tmem_ld16(col, hi);
+          tc::tmem_ld16(col + 64, lo);
           tc::tmem_wait_ld();
-          const float4* w4 = reinterpret_cast<const float4*>(wq + qq * kHI + half * 32);
+          const float4* w4 = reinterpret_cast<const float4*>(wq + qq * kHI + qt * 16);
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
+          for (int h4 = 0; h4 < 4; ++h4) {
             const float4 ww = w4[h4];
             s4[0] = fmaf(ww.x, fmaxf(hi[4 * h4] + lo[4 * h4], 0.f), s4[0]);
             s4[1] = fmaf(ww.y, fmaxf(hi[4 * h4 + 1] + lo[4 * h4 + 1], 0.f), s4[1]);
@@ -653,7 +673,8 @@ cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(index_scores_tc<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Lay::bytes);
   if (e != cudaSuccess) return e;
-  index_scores_tc<NQ><<<grid, kThreads, Lay::bytes, st>>>(p, map);
+  e = launch_pdl(index_scores_tc<NQ>, dim3(grid), dim3(kThreads), Lay::bytes, st, p, map);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
