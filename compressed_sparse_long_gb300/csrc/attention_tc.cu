@@ -17,9 +17,10 @@
 // second product, so keys stay exact codes. Q~ = RoPE(q, p) * softmax_scale * log2(e) in
 // bf16; logits are in log2 units.
 //
-// Warpgroups (setmaxnreg splits the registers): 0 = softmax and epilogue (warp w reads
-// TMEM lanes 32w..32w+31), 1-2 = eight gather/convert warps that also build Q~,
-// 3 = warp 12 allocates TMEM and issues the MMAs (warps 13-15 idle).
+// Warpgroups (setmaxnreg splits the 512 x 128 launch registers as 152 / 128 / 128 / 104):
+// 0 = softmax and epilogue (warp w reads TMEM lanes 32w..32w+31), 1-2 = eight
+// gather/convert warps that also build Q~, 3 = warp 12 allocates TMEM, walks the items
+// converged and issues the MMAs from lane 0 (warps 13-15 idle).
 // Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
 #include "common.cuh"
 #include "kernels.h"
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       ++ni;
     }
   } else if (warp < 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     pdl_wait();
     // ------------------------------------------------------------ softmax + epilogue
     // Every lane keeps the running max of heads `lane` and `lane + 32` in registers (all
@@ -544,9 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       ++ni;
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
     // ------------------------------------------------------------ MMA issuer (warp 12)
-    if (warp == 12 && lane == 0) {
+    // The whole warp walks the items and waits (a converged warp); lane 0 issues.
+    if (warp == 12) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kTile, kH);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, kH, true, true);
       const uint32_t k0 = tc::smem_u32(kbuf), q0 = tc::smem_u32(qbuf), p0 = tc::smem_u32(pbuf);
@@ -559,47 +561,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const Item I = make_item(p, it);
         if (I.n_tiles == 0) continue;
-        if (!tc::mbar_wait(qfull, ni & 1, abort_flag, p.err)) break;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(qfull, ni & 1, abort_flag, p.err))) break;
         for (int t = 0; t < I.n_tiles; ++t, ++gi) {
           // S^T = K Q~^T over the 8 K-blocks, block pair b as soon as it is converted
           for (int b = 0; b < 4; ++b) {
-            if (!tc::mbar_wait(kfull + b, gi & 1, abort_flag, p.err)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(kfull + b, gi & 1, abort_flag, p.err))) { ok = false; break; }
             tc::fence_after_sync();
+            if (lane == 0) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int kb = 2 * b + kk;
+              for (int kk = 0; kk < 2; ++kk) {
+                const int kb = 2 * b + kk;
 #pragma unroll
-              for (int s4 = 0; s4 < 4; ++s4) {
-                // descriptor start address field counts 16-byte units
-                const uint64_t ad = dk_k + (uint64_t)((kb * 16384 + s4 * 32) >> 4);
-                const uint64_t bd = dq_k + (uint64_t)((kb * 8192 + s4 * 32) >> 4);
-                tc::mma_bf16(tmem + kSCol, ad, bd, idesc_qk, (kb | s4) ? 1u : 0u);
+                for (int s4 = 0; s4 < 4; ++s4) {
+                  // descriptor start address field counts 16-byte units
+                  const uint64_t ad = dk_k + (uint64_t)((kb * 16384 + s4 * 32) >> 4);
+                  const uint64_t bd = dq_k + (uint64_t)((kb * 8192 + s4 * 32) >> 4);
+                  tc::mma_bf16(tmem + kSCol, ad, bd, idesc_qk, (kb | s4) ? 1u : 0u);
+                }
               }
             }
+            __syncwarp();
           }
           if (!ok) break;
-          tc::mma_commit(sfull);
-          if (t == I.n_tiles - 1) tc::mma_commit(qempty);
-          if (!tc::mbar_wait(pfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
-          if (t == 0 && ni > 0 && !tc::mbar_wait(oempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-          tc::fence_after_sync();
-          // O^T[dims of block b] += V^T P'^T; V^T is the key tile read MN-major
-          for (int b = 0; b < 4; ++b) {
-#pragma unroll
-            for (int s8 = 0; s8 < 8; ++s8) {
-              const uint64_t ad = dk_mn + (uint64_t)(((2 * b) * 16384 + s8 * 2048) >> 4);
-              const uint64_t bd = dp_mn + (uint64_t)((s8 * 2048) >> 4);
-              tc::mma_bf16(tmem + kOCol + b * 64, ad, bd, idesc_pv, (t > 0 || s8 > 0) ? 1u : 0u);
-            }
-            tc::mma_commit(kempty + b);
+          if (lane == 0) {
+            tc::mma_commit(sfull);
+            if (t == I.n_tiles - 1) tc::mma_commit(qempty);
           }
-          tc::mma_commit(pvdone);
-          if (t == I.n_tiles - 1) tc::mma_commit(ofull);
+          __syncwarp();
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(pfull, gi & 1, abort_flag, p.err))) { ok = false; break; }
+          if (t == 0 && ni > 0 &&
+              !__all_sync(0xffffffffu, tc::mbar_wait(oempty, (ni - 1) & 1, abort_flag, p.err))) { ok = false; break; }
+          tc::fence_after_sync();
+          if (lane == 0) {
+            // O^T[dims of block b] += V^T P'^T; V^T is the key tile read MN-major
+            for (int b = 0; b < 4; ++b) {
+#pragma unroll
+              for (int s8 = 0; s8 < 8; ++s8) {
+                const uint64_t ad = dk_mn + (uint64_t)(((2 * b) * 16384 + s8 * 2048) >> 4);
+                const uint64_t bd = dp_mn + (uint64_t)((s8 * 2048) >> 4);
+                tc::mma_bf16(tmem + kOCol + b * 64, ad, bd, idesc_pv, (t > 0 || s8 > 0) ? 1u : 0u);
+              }
+              tc::mma_commit(kempty + b);
+            }
+            tc::mma_commit(pvdone);
+            if (t == I.n_tiles - 1) tc::mma_commit(ofull);
+          }
+          __syncwarp();
         }
         ++ni;
       }
-      tc::mma_commit(done);
-      tc::mbar_wait_drain(done, 0);
+      if (lane == 0) {
+        tc::mma_commit(done);
+        tc::mbar_wait_drain(done, 0);
+      }
     }
     __syncwarp();
   }
