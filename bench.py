@@ -277,7 +277,7 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     if args.only == "prefill":          # profiling aid: the prefill chunk alone
         print(json.dumps({"prefill": _prefill(dev, tf_peak, tf_sus)}), flush=True)
         return
-    w = wl.c4a_decode(seed=1 + 1000 * rank, B=B, L=L)
+    w = wl.c4a_decode(seed=rank_seed(rank), B=B, L=L)
     base = Layer.from_host(w.layers[0], dev)
     r0 = DecodeReplica(base, w, dev, clone=False)
     per_step = r0.touched_bytes()
@@ -328,8 +328,7 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     ms_max = _max_over_ranks(ms, world, dev)
-    queries = world * B * args.steps
-    value = queries / (ms_max / 1e3)
+    value = whole_job_rate(B * args.steps, world, ms_max)
     ms_per_step = ms_max / args.steps
     algo_bytes_step = per_step
     hbm_gbs = algo_bytes_step / (ms_per_step / 1e3) / 1e9
@@ -384,6 +383,17 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         print(json.dumps(line), flush=True)
     if err_bits:
         raise SystemExit("device error bits 0x%x raised during the decode steps" % err_bits)
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes the same units; the job takes the slowest rank's
+    time, so the whole-job rate is all ranks' units over that time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank's decode replica draws its own inputs (no data-path collective)."""
+    return 1 + 1000 * rank
 
 
 def _max_over_ranks(ms, world, dev):
