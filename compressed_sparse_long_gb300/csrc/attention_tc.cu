@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   uint8_t* kbuf = sm + kOffK;
   uint8_t* qbuf = sm + kOffQ;
   uint8_t* pbuf = sm + kOffP;
-  float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] by item parity
+  float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] 1 / l by item parity
   float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
   float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
   float* sscale = red_sum + 512;                          // [2][128] row scales by tile parity
@@ -492,10 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       }
       if (!ok) break;
       // ---- publish the denominators, then read O^T (lanes: dims 128b + row; cols: heads)
-      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg;
+      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg > 0.f ? 1.f / l_reg : 0.f;   // 1 / l
       const float m_final = quad == 0 ? mc0 : mc1;   // used by the owners (row < 64)
       if (!group_sync()) { ok = false; break; }
-      const float* lden = l_fin + (ni & 1) * 64;
+      const float* linv = l_fin + (ni & 1) * 64;
       if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }
       tc::fence_after_sync();
       if (kSplit) {
@@ -530,8 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
             tc::tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
-              const float L = lden[half * 32 + h];
-              float v = L > 0.f ? o[h] / L : 0.f;
+              float v = o[h] * linv[half * 32 + h];
               const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
               if (tail) v = (d & 1) ? (-partner * sn + v * c) : (v * c + partner * sn);
               out[(int64_t)(half * 32 + h) * kD + d] = __float2bfloat16_rn(v);
