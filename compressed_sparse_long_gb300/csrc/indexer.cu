@@ -495,8 +495,8 @@ int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaSt
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.n_q == 0) return V4A_OK;
   cudaError_t e;
-  if (max_vis <= 16 * 512) {
-    e = launch_pdl(topk_reg_kernel<16, 512>, dim3(p.n_q), dim3(512), 0, st, p);
+  if (max_vis <= 8 * 1024) {
+    e = launch_pdl(topk_reg_kernel<8, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
   } else if (max_vis <= 32 * 1024) {
     e = launch_pdl(topk_reg_kernel<32, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
   } else if (max_vis <= kTopkSmemMax) {
