@@ -239,18 +239,38 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
 template <typename OT, int kPairs>
 __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
   pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x, h = blockIdx.y * 8 + warp;
   if (h >= p.H) return;
   const int H = p.H, D = p.D, tail0 = D - p.rope.d_r;
   const int64_t pos = __ldg(p.q_pos + qi);
   const int64_t row0 = (int64_t)qi * p.n_split * H + h;          // (qi, split 0, h)
-  float mx = -INFINITY;
-  for (int s = lane; s < p.n_split; s += 32) mx = fmaxf(mx, p.part_ml[(row0 + (int64_t)s * H) * 2]);
+  pdl_wait();
+  // One round of loads: every split's (m, l) (lane s holds split s, s < 32) and the first
+  // four splits' partial rows; the weights are formed from registers afterwards.
+  float m_l = -INFINITY, l_l = 0.f;
+  if (lane < p.n_split) {
+    m_l = p.part_ml[(row0 + (int64_t)lane * H) * 2];
+    l_l = p.part_ml[(row0 + (int64_t)lane * H) * 2 + 1];
+  }
+  float2 v[4][kPairs];
+  auto load4 = [&](int s0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u;
+      const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i)
+        v[u][i] = s < p.n_split ? *reinterpret_cast<const float2*>(src + 2 * lane + 64 * i)
+                                : make_float2(0.f, 0.f);
+    }
+  };
+  load4(0);
+  float mx = m_l;
+  for (int s = lane + 32; s < p.n_split; s += 32) mx = fmaxf(mx, p.part_ml[(row0 + (int64_t)s * H) * 2]);
   mx = warp_max(mx);
-  float L = 0.f;
-  for (int s = lane; s < p.n_split; s += 32) {
+  float L = (mx != -INFINITY && m_l != -INFINITY) ? l_l * exp2f(m_l - mx) : 0.f;
+  for (int s = lane + 32; s < p.n_split; s += 32) {
     const float ms = p.part_ml[(row0 + (int64_t)s * H) * 2];
     if (mx != -INFINITY && ms != -INFINITY) L += p.part_ml[(row0 + (int64_t)s * H) * 2 + 1] * exp2f(ms - mx);
   }
@@ -260,19 +280,14 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) a[i] = b[i] = 0.f;
   for (int s0 = 0; s0 < p.n_split; s0 += 4) {
-    float2 v[4][kPairs];
+    if (s0 > 0) load4(s0);
     float wg[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int s = s0 + u;
       float ms = -INFINITY;
-      if (s < p.n_split) ms = p.part_ml[(row0 + (int64_t)s * H) * 2];
+      if (s < p.n_split) ms = s < 32 ? __shfl_sync(0xffffffffu, m_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2];
       wg[u] = (s < p.n_split && mx != -INFINITY && ms != -INFINITY) ? exp2f(ms - mx) : 0.f;
-      const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
-#pragma unroll
-      for (int i = 0; i < kPairs; ++i)
-        v[u][i] = s < p.n_split ? *reinterpret_cast<const float2*>(src + 2 * lane + 64 * i)
-                                : make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)

@@ -129,9 +129,16 @@ struct CompressKernel {
       }
     }
 
+    // Everything above read only this call's inputs (and so did the slot lookups below):
+    // it ran while the previous kernel finished. Pool writes, and the residual reads of
+    // the window loop, wait for it.
+    const int64_t swa_slot = slot_of(p.swa, b, t);
+    const int64_t state_slot = keep_state ? slot_of(p.state, b, t) : -1;
+    pdl_wait();
+
     // (1) sliding-window row: RoPE(kv_t, t)
     {
-      int64_t s = slot_of(p.swa, b, t);
+      const int64_t s = swa_slot;
       if (s >= 0) {
         float y[CPL];
 #pragma unroll
@@ -145,7 +152,7 @@ struct CompressKernel {
 
     // (2) raw residual row for the last W new positions
     if (keep_state) {
-      int64_t s = slot_of(p.state, b, t);
+      const int64_t s = state_slot;
       if (s >= 0) {
         TIn* dst = reinterpret_cast<TIn*>(p.state.data) + s * (int64_t)p.state.width;
         store_f<TIn, CPL>(dst + lane * CPL, x);
@@ -261,8 +268,7 @@ struct CompressKernel {
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_constant__ CompressParams p) {
-  pdl_trigger();
-  pdl_wait();
+  pdl_trigger();   // the kernel waits (pdl_wait) after loading its inputs
   CompressKernel<TIn, CPL, ICPL, kFp8>::run(p);
 }
 
