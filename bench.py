@@ -414,6 +414,8 @@ def _per_call_times(reps, steps, stream):
         "compress_insert": lambda r: r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_),
         "index_topk": lambda r: r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk),
         "attention": lambda r: r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out),
+        # the same attention with the fp8 output epilogue (e4m3 codes + per-row scales)
+        "attention_q8": lambda r: r.lay.attention_q8(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk),
     }
     out = {}
     for name, fn in calls.items():

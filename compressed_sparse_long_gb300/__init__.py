@@ -17,6 +17,7 @@ __all__ = [
     "V4AError", "LayerCfg", "Cache", "library", "layer_cfg", "cache",
     "v4a_compress_insert", "v4a_index_topk", "v4a_index_topk_workspace_size",
     "v4a_attn_decode", "v4a_attn_prefill", "v4a_attn_workspace_size", "v4a_slot_mapping",
+    "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size",
     "v4a_get_error", "v4a_version",
     "C4A", "C128A", "FP32", "BF16_FP8", "DEV_MISSING_PAGE", "DEV_BAD_PAGE", "DEV_BAD_INDEX", "DEV_BAD_POS",
 ]
@@ -72,6 +73,9 @@ _SIGS = {
     "v4a_attn_prefill": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
                                         _P, _P, _SZ, _P, _P]),
     "v4a_slot_mapping": (ctypes.c_int, [_CACHE, _I32, _P, _P, _P, _P, _P]),
+    "v4a_attn_q8_workspace_size": (_SZ, [_CFG, _I32, _I64, _I32]),
+    "v4a_attn_decode_q8": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
+                                          _P, _P, _P, _SZ, _P, _P]),
     "v4a_index_topk_noalloc_capacity": (_SZ, []),
     "v4a_index_topk_noalloc": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _I32,
                                               _P, _P, _P]),
@@ -192,6 +196,19 @@ def v4a_attn_decode(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out,
                     dev_err=None, stream=None):
     _attn("v4a_attn_decode", cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out,
           workspace, dev_err, stream)
+
+
+def v4a_attn_q8_workspace_size(cfg, n_q, max_pos, k) -> int:
+    return library().v4a_attn_q8_workspace_size(ctypes.byref(cfg), n_q, max_pos, k)
+
+
+def v4a_attn_decode_q8(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out_codes,
+                       out_scale, workspace, dev_err=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("v4a_attn_decode_q8", library().v4a_attn_decode_q8(
+        ctypes.byref(cfg), n_q, _ptr(q_seq), _ptr(q_pos), max_pos, _ptr(q), _ptr(topk), k,
+        ctypes.byref(attn), ctypes.byref(swa), _ptr(out_codes), _ptr(out_scale), _ptr(workspace),
+        ws_bytes, _ptr(dev_err), _stream(stream)))
 
 
 def v4a_attn_prefill(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out, workspace,

@@ -176,7 +176,7 @@ struct SplitPlan {
 };
 
 SplitPlan plan_split(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int32_t k,
-                     bool dense, bool prefill) {
+                     bool dense, bool prefill, bool at_least_two = false) {
   const int64_t max_keys =
       (dense ? visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off) : k) + cfg->swa;
   SplitPlan s{1, (int32_t)max_keys};
@@ -201,9 +201,11 @@ SplitPlan plan_split(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int
       best_k = k;
     }
   }
+  if (at_least_two && best_k < 2) best_k = 2;
   const int64_t per = ((tiles + best_k - 1) / best_k) * tile;
   s.keys_per_split = (int32_t)per;
   s.n_split = (int32_t)((max_keys + per - 1) / per);
+  if (at_least_two && s.n_split < 2) s.n_split = 2;   // the second range may hold no key
   return s;
 }
 
@@ -217,7 +219,8 @@ size_t attn_ws(const v4a_layer_cfg* cfg, int32_t n_q, const SplitPlan& s) {
 int attn_common(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq, const int64_t* q_pos,
                 int64_t max_pos, const void* q, const int32_t* topk, int32_t k,
                 const v4a_cache* attn, const v4a_cache* swa, void* out, void* workspace,
-                size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream, bool prefill) {
+                size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream, bool prefill,
+                float* out_scale = nullptr) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if (n_q < 0 || max_pos < 0) return V4A_ERR_ARG;
@@ -228,7 +231,8 @@ int attn_common(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq, con
   const bool fp8 = cfg->dtype == V4A_BF16_FP8;
   if ((rc = check_cache(attn, kBlock / cfg->stride, cfg->head_dim, fp8))) return rc;
   if ((rc = check_cache(swa, kBlock, cfg->head_dim, fp8))) return rc;
-  const SplitPlan s = plan_split(cfg, n_q, max_pos, topk ? k : 0, topk == nullptr, prefill);
+  const SplitPlan s = plan_split(cfg, n_q, max_pos, topk ? k : 0, topk == nullptr, prefill,
+                                 out_scale != nullptr);
   const size_t need = attn_ws(cfg, n_q, s);
   if (s.n_split > 1) {
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return V4A_ERR_ARG;
@@ -244,6 +248,7 @@ int attn_common(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq, con
   p.k = topk ? k : 0;
   p.n_split = s.n_split;
   p.keys_per_split = s.keys_per_split;
+  p.out_scale = out_scale;
   p.scale = cfg->softmax_scale;
   p.q_seq = q_seq;
   p.q_pos = q_pos;
@@ -278,6 +283,25 @@ int v4a_attn_decode(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                     v4a_stream_t stream) {
   return attn_common(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out, workspace,
                      workspace_bytes, dev_err, stream, false);
+}
+
+size_t v4a_attn_q8_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int32_t k) {
+  if (check_cfg(cfg) || n_q < 0 || max_pos < 0) return 0;
+  const SplitPlan s = plan_split(cfg, n_q, max_pos, k, k <= 0, false, true);
+  return attn_ws(cfg, n_q, s);
+}
+
+int v4a_attn_decode_q8(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                       const int64_t* q_pos, int64_t max_pos, const void* q, const int32_t* topk,
+                       int32_t k, const v4a_cache* attn, const v4a_cache* swa, uint8_t* out_codes,
+                       float* out_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                       v4a_stream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (cfg->dtype != V4A_BF16_FP8) return V4A_ERR_UNSUPPORTED;
+  if (n_q > 0 && (!out_scale || !aligned(out_scale, 4))) return V4A_ERR_ARG;
+  return attn_common(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out_codes, workspace,
+                     workspace_bytes, dev_err, stream, false, out_scale);
 }
 
 int v4a_attn_prefill(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,

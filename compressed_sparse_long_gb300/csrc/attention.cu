@@ -290,27 +290,51 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
       wg[u] = (s < p.n_split && mx != -INFINITY && ms != -INFINITY) ? exp2f(ms - mx) : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 4; ++u) {
+      if (wg[u] == 0.f) continue;   // a range without keys wrote no partial: never multiply it
 #pragma unroll
       for (int i = 0; i < kPairs; ++i) {
         a[i] = fmaf(v[u][i].x, wg[u], a[i]);
         b[i] = fmaf(v[u][i].y, wg[u], b[i]);
       }
+    }
+  }
+  float x[kPairs], y[kPairs];
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) {
+    const int d = 2 * lane + 64 * i;
+    x[i] = a[i] * inv;
+    y[i] = b[i] * inv;
+    if (d >= tail0) {
+      float c, sn;
+      rope_cs(p.rope, pos, (d - tail0) >> 1, c, sn);
+      const float rx = x[i] * c + y[i] * sn, ry = -x[i] * sn + y[i] * c;
+      x[i] = rx;
+      y[i] = ry;
+    }
+  }
+  if (p.out_scale) {
+    // fp8 output ([notes] 融合 2：Inverse RoPE + FP8 Quant): per (query, head) row,
+    // scale = amax/448 (1 for a zero row), code = e4m3 RNE satfinite of value/scale
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[i]), fabsf(y[i])));
+    amax = warp_max(amax);
+    const float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+    uint8_t* codes = reinterpret_cast<uint8_t*>(p.out) + ((int64_t)qi * H + h) * D;
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i)
+      *reinterpret_cast<uint16_t*>(codes + 2 * lane + 64 * i) =
+          e4m3x2_encode(__fdiv_rn(x[i], scale), __fdiv_rn(y[i], scale));
+    if (lane == 0) p.out_scale[(int64_t)qi * H + h] = scale;
+    return;
   }
   OT* out = reinterpret_cast<OT*>(p.out) + ((int64_t)qi * H + h) * D;
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) {
     const int d = 2 * lane + 64 * i;
-    float x = a[i] * inv, y = b[i] * inv;
-    if (d >= tail0) {
-      float c, sn;
-      rope_cs(p.rope, pos, (d - tail0) >> 1, c, sn);
-      const float rx = x * c + y * sn, ry = -x * sn + y * c;
-      x = rx;
-      y = ry;
-    }
-    out[d] = Elem<OT>::from_f(x);
-    out[d + 1] = Elem<OT>::from_f(y);
+    out[d] = Elem<OT>::from_f(x[i]);
+    out[d + 1] = Elem<OT>::from_f(y[i]);
   }
 }
 

@@ -55,7 +55,8 @@ struct AttnParams {
   const void* q;
   const int32_t* topk;
   CacheView attn, swa;
-  void* out;
+  void* out;                   // bf16 / fp32 [n_q, H, D], or e4m3 codes when out_scale is set
+  float* out_scale;            // [n_q, H] row scales of an fp8 output (nullptr: no quantisation)
   float* part_o;               // [n_q, n_split, H, D]   (n_split > 1)
   float* part_ml;              // [n_q, n_split, H, 2]   (n_split > 1)
   Rope rope;

@@ -12,6 +12,7 @@ import numpy as np
 import torch
 
 from . import (BF16_FP8, C4A, C128A, FP32, cache, layer_cfg, v4a_attn_decode,
+               v4a_attn_decode_q8, v4a_attn_q8_workspace_size,
                v4a_attn_prefill, v4a_attn_workspace_size, v4a_compress_insert,
                v4a_index_topk, v4a_index_topk_workspace_size)
 
@@ -117,6 +118,18 @@ class Layer:
         fn(self.cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, self.attn.c, self.swa.c, out, ws,
            dev_err, stream)
         return out
+
+    def attention_q8(self, q_seq, q_pos, max_pos, q, topk=None, k=0, dev_err=None, stream=None):
+        """Decode attention with an fp8 output: (e4m3 codes [n_q, H, D] uint8, scales [n_q, H])."""
+        n_q = q_seq.numel()
+        k = k if topk is None else topk.shape[1]
+        codes = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+        scale = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        nb = v4a_attn_q8_workspace_size(self.cfg, n_q, max_pos, k if topk is not None else 0)
+        ws = self.workspace("attn_q8", nb, q_seq.device)
+        v4a_attn_decode_q8(self.cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, self.attn.c,
+                           self.swa.c, codes, scale, ws, dev_err, stream)
+        return codes, scale
 
     def step(self, cu, start, kv, s, ik, is_, q_seq, q_pos, max_pos, q, q_idx=None, w=None,
              out=None, prefill=False, dev_err=None, stream=None):

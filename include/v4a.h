@@ -209,6 +209,23 @@ int v4a_attn_decode(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                     int32_t k, const v4a_cache* attn, const v4a_cache* swa, void* out,
                     void* workspace, size_t workspace_bytes, int32_t* dev_err,
                     v4a_stream_t stream);
+/* v4a_attn_decode_q8 — v4a_attn_decode whose epilogue also quantises the output for an fp8
+ * output projection ([notes] 优化一, 融合 2：Inverse RoPE + FP8 Quant: the attention output goes
+ * through the inverse RoPE and straight into an fp8 batched matmul; [blog] GPU 計算飽和度).
+ *   out_codes  [n_q, H, D] e4m3 bytes, 16-byte aligned (caller-owned)
+ *   out_scale  [n_q, H] fp32 (caller-owned)
+ * Per (query, head) row y of R^-1(p) o_h: scale = max|y| / 448 (1 for a zero row) and
+ * code = e4m3 round-to-nearest-even, saturating, of y / scale: the rule of the fp8 caches.
+ * bf16 layers (V4A_BF16_FP8) only, else V4A_ERR_UNSUPPORTED. The keys of a query are always
+ * split into at least two ranges (the quantisation runs where the ranges are merged), so the
+ * workspace is v4a_attn_q8_workspace_size(cfg, n_q, max_pos, k), 256-byte aligned. Other
+ * arguments, errors and the device error word as for v4a_attn_decode. */
+size_t v4a_attn_q8_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int32_t k);
+int v4a_attn_decode_q8(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                       const int64_t* q_pos, int64_t max_pos, const void* q, const int32_t* topk,
+                       int32_t k, const v4a_cache* attn, const v4a_cache* swa, uint8_t* out_codes,
+                       float* out_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                       v4a_stream_t stream);
 int v4a_attn_prefill(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                      const int64_t* q_pos, int64_t max_pos, const void* q,
                      const int32_t* topk, int32_t k, const v4a_cache* attn,

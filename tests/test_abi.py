@@ -88,6 +88,14 @@ def test_host_validation_rejects_bad_arguments(lib):
                               ctypes.byref(c), 1, 16, None, 0, None, None) == v4a.ERR_UNSUPPORTED
     assert lib.v4a_index_topk(ctypes.byref(_cfg(win_off=1)), 1, 8, 8, 0, 16, 16, ctypes.byref(c),
                               1, 16, None, 0, None, None) == v4a.ERR_ARG
+    # fp8 output: bf16 layers only, and it needs the scale array
+    assert lib.v4a_attn_decode_q8(ctypes.byref(_cfg(dtype=v4a.FP32)), 4, 8, 8, 100, 16, 16, 512,
+                                  ctypes.byref(c), ctypes.byref(c), 16, 16, None, 0, None,
+                                  None) == v4a.ERR_UNSUPPORTED
+    assert lib.v4a_attn_decode_q8(ctypes.byref(_cfg(dtype=v4a.BF16_FP8)), 4, 8, 8, 100, 16, 16,
+                                  512, ctypes.byref(c), ctypes.byref(c), 16, None, None, 0, None,
+                                  None) == v4a.ERR_ARG
+    assert v4a.v4a_attn_q8_workspace_size(_cfg(dtype=v4a.BF16_FP8), 4, 1000, 512) > 256
     # the indexer exists only for c4a layers
     assert lib.v4a_index_topk(ctypes.byref(_cfg(kind=v4a.C128A, window=128, stride=128)), 1, 8,
                               8, 0, 16, 16, ctypes.byref(c), 1, 16, None, 0, None,

@@ -277,6 +277,52 @@ def test_attention_fp8_c4a_lists(prefill):
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
 
+def _e4m3_step(v):
+    """Grid step of the e4m3 value nearest |v| (the spacing a rounding error is bounded by)."""
+    g = O.e4m3_values()
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(g, a, side="left"), 1, len(g) - 1)
+    return g[hi] - g[hi - 1]
+
+
+@pytest.mark.parametrize("B,L,width", [(8, 8192, 512), (4, 48, 64)])
+def test_attention_q8_output(B, L, width):
+    """fp8 output epilogue ([notes] 融合 2：Inverse RoPE + FP8 Quant): per (query, head) row the
+    scale is amax/448 and the codes are e4m3 RNE of out/scale. The rule is checked against the
+    same attention's bf16 output, the values against the oracle. The short contexts leave the
+    second key range empty (the merge must skip it)."""
+    w = wl.c4a_decode(seed=21, B=B, L=L)
+    h = w.layers[0]
+    q = w.queries
+    lists = _random_lists(np.random.default_rng(5), q.pos, h.spec, width)
+    _fill_query_window_row(h, w)
+    lay, x = device_layer(h), DevInputs(w)
+    tk = torch.from_numpy(lists).cuda()
+    err = _err()
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, tk, dev_err=err)
+    codes, scale = lay.attention_q8(x.q_seq, x.q_pos, x.max_pos, x.q, tk, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    out = out.float().cpu().numpy()
+    codes, scale = codes.cpu().numpy(), scale.cpu().numpy().astype(np.float64)
+    assert np.isfinite(scale).all() and (scale > 0).all()
+    # the rule, against the same call's output (bf16 rounds the fp32 values by <= 2^-9)
+    amax = np.abs(out).max(axis=-1)
+    assert np.allclose(scale, np.where(amax > 0, amax / 448.0, 1.0), rtol=2.0 ** -8)
+    deq = O.e4m3_decode(codes) * scale[..., None]
+    half = 0.5 * _e4m3_step(out / scale[..., None]) * scale[..., None]
+    assert (np.abs(deq - out) <= half * 1.05 + np.abs(out) * 2.0 ** -8 + 1e-12).all()
+    # against the oracle: its quantised rows, within the attention tolerance plus one step
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
+    codes_o, scale_o = O.quantize(ref)
+    assert np.allclose(scale, scale_o, rtol=3e-2, atol=1e-6)
+    deq_o = O.e4m3_decode(codes_o) * scale_o[..., None]
+    step_o = _e4m3_step(ref / scale_o[..., None]) * scale_o[..., None]
+    assert (np.abs(deq - deq_o) <= step_o * 1.05 + 3e-2).all()
+    # fp8 rounding itself (half a step, ~3% of a value) is in both: compare the quantised
+    # outputs with the bf16 output's mean tolerance
+    assert np.abs(deq - deq_o).mean() <= 3e-3
+
+
 def test_attention_fp8_c128a_dense():
     w = wl.c128a_decode(seed=2, B=4, L=65536)
     h = w.layers[0]
