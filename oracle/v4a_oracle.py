@@ -30,6 +30,8 @@ the design notes of the repository):
   R8  attention: one softmax over the selected entries and the window, logits
       scaled by 1/sqrt(D); the same stored vector is key and value; inverse RoPE at
       the query position on the output.
+  R13 query norm: RMSNorm of each (query, head) row over its D dims, one gamma [D]
+      shared by the heads, the entries' epsilon.
 """
 from __future__ import annotations
 
@@ -168,6 +170,21 @@ def compress_window(kv_win: np.ndarray, s_win: np.ndarray, b_win: np.ndarray) ->
 def rmsnorm(c: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """y = gamma * c / sqrt(mean(c^2) + eps) ([notes] 融合 1: 压缩后的 K 经过 RMSNorm)."""
     return gamma * c / np.sqrt(np.mean(c * c) + eps)
+
+
+def q_norm(q: np.ndarray, gamma_q: np.ndarray, eps: float) -> np.ndarray:
+    """Per-head query RMSNorm (R13): every (query, head) row of q [n_q, H, D] becomes
+    gamma_q * q_h / sqrt(mean(q_h^2) + eps), gamma_q [D] shared by the heads.
+
+    [notes] 优化一：三大内核融合, fusion 3 (Q Norm + KV RoPE + K Insert): each Q head is
+    normalised on its own, with no communication between heads.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    out = np.empty_like(q)
+    for i in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            out[i, h] = rmsnorm(q[i, h], np.asarray(gamma_q, dtype=np.float64), eps)
+    return out
 
 
 def visible_entries(S: int, W: int, win_off: int, p: int) -> int:

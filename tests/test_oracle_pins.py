@@ -136,6 +136,34 @@ def test_rmsnorm_closed_form():
     assert abs(math.sqrt(np.mean(y * y)) - 1.0) < 1e-6
 
 
+def test_q_norm_by_hand_per_head():
+    """Two heads of D=2 worked out by hand: each head is divided by its own RMS and
+    multiplied by the per-dim gamma (R13)."""
+    q = np.array([[[3.0, 4.0], [1.0, 0.0]]])
+    g = np.array([2.0, -1.0])
+    y = O.q_norm(q, g, 0.0)
+    r0, r1 = math.sqrt(12.5), math.sqrt(0.5)
+    assert np.allclose(y, [[[6 / r0, -4 / r0], [2 / r1, 0.0]]])
+
+
+def test_q_norm_heads_are_independent_and_unit_rms():
+    """Heads at scales 1e-2 .. 1e3 each come out with RMS 1 (gamma = 1), and scaling one
+    head leaves every row unchanged (eps = 0): a norm taken over all heads jointly, or over
+    the wrong axis, fails here."""
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((3, 6, 64)) * (10.0 ** np.arange(-2, 4))[None, :, None]
+    y = O.q_norm(q, np.ones(64), 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, atol=1e-12)
+    q2 = q.copy()
+    q2[1, 4] *= 37.0
+    assert np.allclose(O.q_norm(q2, np.ones(64), 0.0), y, atol=1e-12)
+    # eps enters inside the root: a zero row stays zero, a row of RMS sqrt(eps) shrinks by 1/sqrt(2)
+    z = np.zeros((1, 2, 4))
+    z[0, 1] = math.sqrt(1e-6)
+    yz = O.q_norm(z, np.ones(4), 1e-6)
+    assert np.all(yz[0, 0] == 0.0) and np.allclose(yz[0, 1], 1 / math.sqrt(2))
+
+
 def _fresh_pools(w):
     L = w.layers[0]
     return O.Pools(L.spec, L.attn, L.idx, L.swa, L.state)
