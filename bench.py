@@ -247,6 +247,10 @@ class DecodeReplica:
         self.topk = torch.empty((len(q.pos), self.lay.top_k), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)   # device error bits
+        # query-norm weight and output of the fused insert + query RMSNorm call
+        self.q_gamma = _dev(np.random.default_rng(7).normal(1.0, 0.1, self.q.shape[-1]),
+                            torch.float32, dev)
+        self.qn = torch.empty_like(self.q)
 
     def step(self):
         self.lay.compress_insert(self.cu, self.start, self.kv, self.s, self.ik, self.is_,
@@ -416,6 +420,12 @@ def _per_call_times(reps, steps, stream):
         "attention": lambda r: r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out),
         # the same attention with the fp8 output epilogue (e4m3 codes + per-row scales)
         "attention_q8": lambda r: r.lay.attention_q8(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk),
+        # the insert with the per-head query RMSNorm in the same launch, and the norm alone
+        "compress_insert_qnorm": lambda r: r.lay.compress_insert_qnorm(
+            r.cu, r.start, r.kv, r.s, r.ik, r.is_, r.q, r.q_gamma, q_out=r.qn),
+        "q_norm_alone": lambda r: r.lay.compress_insert_qnorm(
+            r.cu[:1], r.start[:0], r.kv[:0], r.s[:0], r.ik[:0], r.is_[:0], r.q, r.q_gamma,
+            q_out=r.qn),
     }
     out = {}
     for name, fn in calls.items():

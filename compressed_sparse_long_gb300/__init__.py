@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "V4AError", "LayerCfg", "Cache", "library", "layer_cfg", "cache",
-    "v4a_compress_insert", "v4a_index_topk", "v4a_index_topk_workspace_size",
+    "v4a_compress_insert", "v4a_compress_insert_qnorm", "v4a_index_topk", "v4a_index_topk_workspace_size",
     "v4a_attn_decode", "v4a_attn_prefill", "v4a_attn_workspace_size", "v4a_slot_mapping",
     "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size",
     "v4a_get_error", "v4a_version",
@@ -64,6 +64,9 @@ _SIGS = {
     "v4a_version": (_I32, []),
     "v4a_compress_insert": (ctypes.c_int, [_CFG, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            _CACHE, _CACHE, _CACHE, _CACHE, _P, _P]),
+    "v4a_compress_insert_qnorm": (ctypes.c_int, [_CFG, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _CACHE, _CACHE, _CACHE, _CACHE, _I32,
+                                                 _P, _P, _P, _P, _P]),
     "v4a_index_topk_workspace_size": (_SZ, [_CFG, _I32, _I64]),
     "v4a_index_topk": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _I32, _P, _P,
                                       _SZ, _P, _P]),
@@ -151,6 +154,20 @@ def v4a_compress_insert(cfg, n_seq, n_tokens, cu_tokens, start_pos, kv, score, b
         _ptr(score), _ptr(bias), _ptr(gamma), _ptr(ikv), _ptr(iscore), _ptr(ibias),
         ctypes.byref(attn), None if idx is None else ctypes.byref(idx), ctypes.byref(swa),
         ctypes.byref(state), _ptr(dev_err), _stream(stream)))
+
+
+def _cref(c):
+    return None if c is None else ctypes.byref(c)
+
+
+def v4a_compress_insert_qnorm(cfg, n_seq, n_tokens, cu_tokens, start_pos, kv, score, bias,
+                              gamma, ikv, iscore, ibias, attn, idx, swa, state, n_q, q, q_gamma,
+                              q_out, dev_err=None, stream=None):
+    _check("v4a_compress_insert_qnorm", library().v4a_compress_insert_qnorm(
+        ctypes.byref(cfg), n_seq, n_tokens, _ptr(cu_tokens), _ptr(start_pos), _ptr(kv),
+        _ptr(score), _ptr(bias), _ptr(gamma), _ptr(ikv), _ptr(iscore), _ptr(ibias),
+        _cref(attn), _cref(idx), _cref(swa), _cref(state), n_q, _ptr(q), _ptr(q_gamma),
+        _ptr(q_out), _ptr(dev_err), _stream(stream)))
 
 
 def v4a_index_topk_workspace_size(cfg, n_q, max_pos) -> int:

@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 4;
+constexpr int32_t kVersion = 5;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -69,31 +69,49 @@ extern "C" {
 
 int32_t v4a_version(void) { return kVersion; }
 
-int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
-                        const int32_t* cu_tokens, const int64_t* start_pos, const void* kv,
-                        const void* score, const float* bias, const float* gamma,
-                        const void* ikv, const void* iscore, const float* ibias,
-                        const v4a_cache* attn, const v4a_cache* idx, const v4a_cache* swa,
-                        const v4a_cache* state, int32_t* dev_err, v4a_stream_t stream) {
+namespace {
+
+// v4a_compress_insert and v4a_compress_insert_qnorm: one launch, n_tokens insert warps
+// followed by n_q * H query-norm warps.
+int compress_common(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
+                    const int32_t* cu_tokens, const int64_t* start_pos, const void* kv,
+                    const void* score, const float* bias, const float* gamma, const void* ikv,
+                    const void* iscore, const float* ibias, const v4a_cache* attn,
+                    const v4a_cache* idx, const v4a_cache* swa, const v4a_cache* state,
+                    int32_t n_q, const void* q, const float* q_gamma, void* q_out,
+                    int32_t* dev_err, v4a_stream_t stream) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
-  if (n_seq < 0 || n_tokens < 0) return V4A_ERR_ARG;
-  if (n_tokens == 0) return V4A_OK;
-  if (n_seq == 0) return V4A_ERR_ARG;
-  if (!cu_tokens || !start_pos || !kv || !score || !bias || !gamma) return V4A_ERR_ARG;
+  if (n_seq < 0 || n_tokens < 0 || n_q < 0) return V4A_ERR_ARG;
   const bool fp8 = cfg->dtype == V4A_BF16_FP8;
   const bool c4a = cfg->kind == V4A_C4A;
   const int D = cfg->head_dim, DI = c4a ? cfg->idx_dim : 0;
   const size_t es = fp8 ? 2 : 4;
-  if (!aligned(kv, 16) || !aligned(score, 16)) return V4A_ERR_ARG;
-  if (c4a && (!ikv || !iscore || !ibias || !aligned(ikv, 16) || !aligned(iscore, 16)))
-    return V4A_ERR_ARG;
-  const int R = kBlock / cfg->stride;
-  if ((rc = check_cache(attn, R, D, fp8))) return rc;
-  if (c4a && (rc = check_cache(idx, R, DI, fp8))) return rc;
-  if ((rc = check_cache(swa, kBlock, D, fp8))) return rc;
-  if ((rc = check_cache(state, kBlock, 2 * D + 2 * DI, false))) return rc;
-  (void)es;
+  const int64_t n_qrows = (int64_t)n_q * cfg->n_heads;
+  if (n_q > 0) {
+    if (!q || !q_gamma || !q_out || !aligned(q, 16) || !aligned(q_gamma, 16) ||
+        !aligned(q_out, 16))
+      return V4A_ERR_ARG;
+    // q_out is q itself or does not overlap it
+    const uintptr_t a = (uintptr_t)q, b = (uintptr_t)q_out, n = (uintptr_t)(n_qrows * D * es);
+    if (a != b && a < b + n && b < a + n) return V4A_ERR_ARG;
+    if ((int64_t)n_tokens + n_qrows > ((int64_t)1 << 33)) return V4A_ERR_ARG;   // grid limit
+  }
+  if (n_tokens > 0) {
+    if (n_seq == 0) return V4A_ERR_ARG;
+    if (!cu_tokens || !start_pos || !kv || !score || !bias || !gamma) return V4A_ERR_ARG;
+    if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(bias, 16) || !aligned(gamma, 16))
+      return V4A_ERR_ARG;
+    if (c4a && (!ikv || !iscore || !ibias || !aligned(ikv, 16) || !aligned(iscore, 16) ||
+                !aligned(ibias, 16)))
+      return V4A_ERR_ARG;
+    const int R = kBlock / cfg->stride;
+    if ((rc = check_cache(attn, R, D, fp8))) return rc;
+    if (c4a && (rc = check_cache(idx, R, DI, fp8))) return rc;
+    if ((rc = check_cache(swa, kBlock, D, fp8))) return rc;
+    if ((rc = check_cache(state, kBlock, 2 * D + 2 * DI, false))) return rc;
+  }
+  if (n_tokens == 0 && n_qrows == 0) return V4A_OK;
 
   CompressParams p{};
   p.n_tokens = n_tokens;
@@ -113,13 +131,45 @@ int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_token
   p.bias = bias;
   p.gamma = gamma;
   p.ibias = c4a ? ibias : nullptr;
-  p.attn = view_of(attn);
-  p.idx = c4a ? view_of(idx) : CacheView{};
-  p.swa = view_of(swa);
-  p.state = view_of(state);
+  if (n_tokens > 0) {
+    p.attn = view_of(attn);
+    p.idx = c4a ? view_of(idx) : CacheView{};
+    p.swa = view_of(swa);
+    p.state = view_of(state);
+  }
   p.rope = make_rope(cfg);
   p.err = dev_err;
+  p.n_qrows = n_qrows;
+  p.q = n_q > 0 ? q : nullptr;
+  p.q_gamma = n_q > 0 ? q_gamma : nullptr;
+  p.q_out = n_q > 0 ? q_out : nullptr;
   return launch_compress_insert(p, cfg->dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
+                        const int32_t* cu_tokens, const int64_t* start_pos, const void* kv,
+                        const void* score, const float* bias, const float* gamma,
+                        const void* ikv, const void* iscore, const float* ibias,
+                        const v4a_cache* attn, const v4a_cache* idx, const v4a_cache* swa,
+                        const v4a_cache* state, int32_t* dev_err, v4a_stream_t stream) {
+  return compress_common(cfg, n_seq, n_tokens, cu_tokens, start_pos, kv, score, bias, gamma,
+                         ikv, iscore, ibias, attn, idx, swa, state, 0, nullptr, nullptr,
+                         nullptr, dev_err, stream);
+}
+
+int v4a_compress_insert_qnorm(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
+                              const int32_t* cu_tokens, const int64_t* start_pos,
+                              const void* kv, const void* score, const float* bias,
+                              const float* gamma, const void* ikv, const void* iscore,
+                              const float* ibias, const v4a_cache* attn, const v4a_cache* idx,
+                              const v4a_cache* swa, const v4a_cache* state, int32_t n_q,
+                              const void* q, const float* q_gamma, void* q_out,
+                              int32_t* dev_err, v4a_stream_t stream) {
+  return compress_common(cfg, n_seq, n_tokens, cu_tokens, start_pos, kv, score, bias, gamma,
+                         ikv, iscore, ibias, attn, idx, swa, state, n_q, q, q_gamma, q_out,
+                         dev_err, stream);
 }
 
 size_t v4a_index_topk_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos) {

@@ -6,7 +6,8 @@
 // RMSNorm + RoPE + cache insert; the K RoPE + K insert half of fusion 3) and 解决方案二
 // (compressor state kept as sliding-window KV); 数学附录精要 for the window positions.
 //
-// Work decomposition: one warp per new token. The warp writes the token's sliding-window
+// Work decomposition: one warp per new token (and, in the call with the query norm, one
+// warp per query head row after them: fusion 3's static warp dispatch). The warp writes the token's sliding-window
 // row and, if the token is among the last W of its sequence's new tokens, its raw residual
 // row. If the token is the last position of entry j's window, the same warp also builds
 // entry j (attention row and, for c4a, indexer row). Lane l owns channels
@@ -95,24 +96,55 @@ struct CompressKernel {
     }
   }
 
+  // One (query, head) row of the query RMSNorm: y = gamma_q * q / sqrt(mean(q^2) + eps),
+  // stored in the input type. The row is in registers before the first store, so q_out may
+  // be q itself.
+  static __device__ void q_norm_row(const CompressParams& p, int64_t r, int lane) {
+    float x[CPL], g[CPL];
+    load_f<TIn, CPL>(reinterpret_cast<const TIn*>(p.q) + r * D + lane * CPL, x);
+    load_f<float, CPL>(p.q_gamma + lane * CPL, g);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) ss = fmaf(x[k], x[k], ss);
+    ss = warp_sum(ss);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)D) + p.eps));
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) x[k] = x[k] * inv * g[k];
+    pdl_wait();   // q_out may still be read by the kernel before this one
+    store_f<TIn, CPL>(reinterpret_cast<TIn*>(p.q_out) + r * D + lane * CPL, x);
+  }
+
   static __device__ void run(const CompressParams& p) {
     const int lane = threadIdx.x & 31;
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (i >= p.n_tokens) return;
+    // static warp dispatch: warps [0, n_tokens) insert tokens, the next n_qrows warps
+    // normalise query head rows; no warp depends on another
+    if (i >= p.n_tokens) {
+      if (i < p.n_tokens + p.n_qrows) q_norm_row(p, i - p.n_tokens, lane);
+      return;
+    }
 
-    // sequence of row i: the largest b with cu[b] <= i, 32 candidates per warp load
+    // sequence of row i: the largest b with cu[b] <= i, 32 candidates per warp load; the
+    // candidates' cu[k], cu[k+1] and start[k] come in the same round and the hit's values
+    // are taken by shuffle
     int b = -1;
+    int64_t row0 = 0, n_new = 0, P0 = 0;
     for (int base = 0; base < p.n_seq && b < 0; base += 32) {
       const int k = base + lane;
-      const bool le = k < p.n_seq && __ldg(p.cu + k) <= i;
-      const bool nxt_le = k + 1 < p.n_seq && __ldg(p.cu + k + 1) <= i;
-      const uint32_t hit = __ballot_sync(0xffffffffu, le && !nxt_le);
-      if (hit) b = base + __ffs(hit) - 1;
+      const int64_t c0 = k < p.n_seq ? (int64_t)__ldg(p.cu + k) : INT64_MAX;
+      const int64_t c1 = k < p.n_seq ? (int64_t)__ldg(p.cu + k + 1) : INT64_MAX;
+      const int64_t st = k < p.n_seq ? __ldg(p.start + k) : 0;
+      const bool hit_k = c0 <= i && !(k + 1 < p.n_seq && c1 <= i);
+      const uint32_t hit = __ballot_sync(0xffffffffu, k < p.n_seq && hit_k);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        b = base + src;
+        row0 = __shfl_sync(0xffffffffu, c0, src);
+        n_new = __shfl_sync(0xffffffffu, c1, src) - row0;
+        P0 = __shfl_sync(0xffffffffu, st, src);
+      }
     }
     if (b < 0) return;
-    const int64_t row0 = __ldg(p.cu + b);
-    const int64_t n_new = __ldg(p.cu + b + 1) - row0;
-    const int64_t P0 = __ldg(p.start + b);
     const int64_t P1 = P0 + n_new;
     const int64_t t = P0 + (i - row0);
 
@@ -274,8 +306,11 @@ __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_const
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 cudaError_t launch(const CompressParams& p, cudaStream_t st) {
-  const int threads = 256;
-  const int64_t blocks = (p.n_tokens * 32 + threads - 1) / threads;
+  // One warp per block (the c4a bf16 kernel compiles to 128 registers a thread): such a
+  // block fits on an SM beside a persistent indexer CTA, so a small insert never holds
+  // an SM the indexer is waiting for.
+  const int threads = 32;
+  const int64_t blocks = p.n_tokens + p.n_qrows;
   const cudaError_t e = launch_pdl(compress_insert_kernel<TIn, CPL, ICPL, kFp8>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -283,7 +318,7 @@ cudaError_t launch(const CompressParams& p, cudaStream_t st) {
 }  // namespace
 
 int launch_compress_insert(const CompressParams& p, int dtype, cudaStream_t st) {
-  if (p.n_tokens == 0) return V4A_OK;
+  if (p.n_tokens == 0 && p.n_qrows == 0) return V4A_OK;
   const int D = p.D, DI = p.DI;
   cudaError_t e = cudaErrorInvalidValue;
   bool done = false;

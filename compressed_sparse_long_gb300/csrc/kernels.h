@@ -26,6 +26,11 @@ struct CompressParams {
   CacheView attn, idx, swa, state;
   Rope rope;
   int32_t* err;
+  // query RMSNorm rows handled by the warps after the n_tokens insert warps (0: none)
+  int64_t n_qrows;             // n_q * H rows of D elements
+  const void* q;               // [n_qrows, D] input type
+  const float* q_gamma;        // [D]
+  void* q_out;                 // [n_qrows, D] input type; equal to q or disjoint from it
 };
 
 struct IndexParams {

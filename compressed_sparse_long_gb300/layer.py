@@ -14,6 +14,7 @@ import torch
 from . import (BF16_FP8, C4A, C128A, FP32, cache, layer_cfg, v4a_attn_decode,
                v4a_attn_decode_q8, v4a_attn_q8_workspace_size,
                v4a_attn_prefill, v4a_attn_workspace_size, v4a_compress_insert,
+               v4a_compress_insert_qnorm,
                v4a_index_topk, v4a_index_topk_workspace_size)
 
 
@@ -92,6 +93,19 @@ class Layer:
         v4a_compress_insert(self.cfg, cu.numel() - 1, kv.shape[0], cu, start, kv, s, self.bias,
                             self.gamma, ik, is_, self.ibias, self.attn.c, idx_c, self.swa.c,
                             self.state.c, dev_err, stream)
+
+    def compress_insert_qnorm(self, cu, start, kv, s, ik, is_, q, q_gamma, q_out=None,
+                              dev_err=None, stream=None):
+        """Insert the new tokens and RMSNorm every query head row of q [n_q, H, D] in the
+        same launch; returns q_out (a new tensor unless given; q itself normalises in place)."""
+        if q_out is None:
+            q_out = torch.empty_like(q)
+        idx_c = None if self.idx is None else self.idx.c
+        v4a_compress_insert_qnorm(self.cfg, cu.numel() - 1, kv.shape[0], cu, start, kv, s,
+                                  self.bias, self.gamma, ik, is_, self.ibias, self.attn.c, idx_c,
+                                  self.swa.c, self.state.c, q.shape[0], q, q_gamma, q_out,
+                                  dev_err, stream)
+        return q_out
 
     def index_topk(self, q_seq, q_pos, max_pos, q_idx, w, out=None, k=None, dev_err=None,
                    stream=None):

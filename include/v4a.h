@@ -125,7 +125,8 @@ typedef struct v4a_cache {
  * swa:   token cache (rows_per_block 256, row_width D)
  * state: token cache of raw rows (rows_per_block 256, row_width 2D (+2 d_I for c4a)),
  *        element type of the inputs.
- * Pool data pointers must be 16-byte aligned.
+ * Pool data pointers and kv, score, ikv, iscore, bias, gamma, ibias must be 16-byte
+ * aligned (V4A_ERR_ARG otherwise).
  */
 int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
                         const int32_t* cu_tokens, const int64_t* start_pos,
@@ -134,6 +135,35 @@ int v4a_compress_insert(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_token
                         const float* ibias, const v4a_cache* attn, const v4a_cache* idx,
                         const v4a_cache* swa, const v4a_cache* state, int32_t* dev_err,
                         v4a_stream_t stream);
+
+/*
+ * v4a_compress_insert_qnorm — v4a_compress_insert plus the per-head query RMSNorm of the
+ * step's queries, in the same launch.
+ *
+ * [notes] 优化一：三大内核融合, fusion 3 (Q Norm + KV RoPE + K Insert, static warp-ID
+ * dispatch: every warp handles one Q head or one K row on its own). The launch's first
+ * n_tokens warps do exactly what v4a_compress_insert does; each of the next n_q * H warps
+ * takes one (query, head) row:
+ *   q_out[i, h, :] = q_gamma * q[i, h, :] / sqrt(mean(q[i, h, :]^2) + cfg->rms_eps),
+ * computed in fp32 and stored in the input type (bf16 round-to-nearest-even or fp32).
+ *
+ * n_q:      queries (>= 0); n_q = 0 makes the call v4a_compress_insert
+ * q:        device [n_q, H, D] (fp32 or bf16 per cfg->dtype), 16-byte aligned
+ * q_gamma:  device fp32 [D], 16-byte aligned, shared by the heads
+ * q_out:    device [n_q, H, D], same type, 16-byte aligned; q_out == q normalises in place,
+ *           any other overlap with q returns V4A_ERR_ARG
+ * The insert arguments are checked only when n_tokens > 0, so n_tokens = 0 runs the norm
+ * alone. Errors: as v4a_compress_insert, plus V4A_ERR_ARG for a NULL, misaligned or
+ * partially overlapping query buffer.
+ */
+int v4a_compress_insert_qnorm(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
+                              const int32_t* cu_tokens, const int64_t* start_pos,
+                              const void* kv, const void* score, const float* bias,
+                              const float* gamma, const void* ikv, const void* iscore,
+                              const float* ibias, const v4a_cache* attn, const v4a_cache* idx,
+                              const v4a_cache* swa, const v4a_cache* state, int32_t n_q,
+                              const void* q, const float* q_gamma, void* q_out,
+                              int32_t* dev_err, v4a_stream_t stream);
 
 /*
  * v4a_index_topk — indexer scores and top-k selection of c4a entries (steps a6, a7).

@@ -96,6 +96,17 @@ def test_host_validation_rejects_bad_arguments(lib):
                                   512, ctypes.byref(c), ctypes.byref(c), 16, None, None, 0, None,
                                   None) == v4a.ERR_ARG
     assert v4a.v4a_attn_q8_workspace_size(_cfg(dtype=v4a.BF16_FP8), 4, 1000, 512) > 256
+    # query norm: negative count, missing or misaligned buffers, partial overlap of q_out
+    # and q (every case returns before anything is enqueued)
+    qn = lib.v4a_compress_insert_qnorm
+    n13 = [None] * 13
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, -1, 4096, 4096, 4096, None, None) == v4a.ERR_ARG
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, 1, None, 4096, 4096, None, None) == v4a.ERR_ARG
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, 1, 4104, 4096, 4104, None, None) == v4a.ERR_ARG
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, 1, 4096, 4100, 4096, None, None) == v4a.ERR_ARG
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, 1, 1 << 20, 4096, (1 << 20) + 1024, None,
+              None) == v4a.ERR_ARG
+    assert qn(ctypes.byref(cfg), 0, 0, *n13, 0, None, None, None, None, None) == v4a.OK
     # the indexer exists only for c4a layers
     assert lib.v4a_index_topk(ctypes.byref(_cfg(kind=v4a.C128A, window=128, stride=128)), 1, 8,
                               8, 0, 16, 16, ctypes.byref(c), 1, 16, None, 0, None,

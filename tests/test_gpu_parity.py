@@ -159,6 +159,64 @@ def test_compress_chunking_invariance_gpu():
 
 
 # -------------------------------------------------------------------- indexer / top-k
+def _pools_equal(a, b):
+    for kind in ("attn", "idx", "swa", "state"):
+        pa, pb = getattr(a, kind), getattr(b, kind)
+        if pa is None:
+            continue
+        assert torch.equal(pa.data, pb.data), kind
+        if pa.scale is not None:
+            assert torch.equal(pa.scale, pb.scale), kind
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_compress_insert_qnorm(fp8):
+    """Fusion 3 (static warp dispatch): the insert warps of v4a_compress_insert_qnorm write
+    the same bytes as v4a_compress_insert; every (query, head) row of q_out is the oracle's
+    per-head RMSNorm to within one rounding to the output type (bf16: 2^-8 relative; fp32:
+    1e-5 relative), and within the layer tolerances; q_out == q gives the same rows in
+    place; n_tokens = 0 runs the norm alone and leaves the pools untouched."""
+    w = wl.c4a_decode(seed=31, B=8, L=4096) if fp8 else wl.tiny_prefill(seed=32, L=300)
+    h = w.layers[0]
+    rng = np.random.default_rng(33)
+    dt = torch.bfloat16 if fp8 else torch.float32
+    q_gamma = rng.normal(1.0, 0.1, h.spec.D)
+    # heads at very different scales, as a joint or wrong-axis norm would not survive
+    q_host = np.asarray(w.queries.q, dtype=np.float64) * \
+        (2.0 ** ((np.arange(h.spec.H) % 9) - 4.0))[None, :, None]
+    q_host = T(q_host, dt).float().cpu().numpy().astype(np.float64)   # what the kernel reads
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    ref_lay = lay.clone_pools()
+    qd, gd = T(q_host, dt), T(q_gamma, torch.float32)
+    q_out = lay.compress_insert_qnorm(x.cu, x.start, x.kv, x.s, x.ik, x.is_, qd, gd,
+                                      dev_err=err)
+    ref_lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_, dev_err=err)
+    torch.cuda.synchronize()
+    assert v4a.v4a_get_error(err) == 0
+    _pools_equal(lay, ref_lay)
+
+    o = O.q_norm(q_host, q_gamma, h.spec.eps)
+    g = q_out.float().cpu().numpy()
+    d = np.abs(g - o)
+    rel = 2.0 ** -8 * 1.001 if fp8 else 1e-5
+    assert np.all(d <= rel * np.abs(o) + 1e-6), d.max()
+    if fp8:
+        assert d.max() <= 3e-2 and d.mean() <= 3e-3
+    else:
+        assert d.max() <= 1e-4
+
+    # in place, and the norm alone
+    q_in = qd.clone()
+    before = lay.clone_pools()
+    lay.compress_insert_qnorm(x.cu[:1], x.start[:0], x.kv[:0], x.s[:0],
+                              None if x.ik is None else x.ik[:0],
+                              None if x.is_ is None else x.is_[:0], q_in, gd, q_out=q_in,
+                              dev_err=err)
+    torch.cuda.synchronize()
+    assert torch.equal(q_in, q_out)
+    _pools_equal(lay, before)
+
+
 def _inject_subnormal_keys(h, rng, n=200):
     """Give some indexer rows only subnormal e4m3 codes and a large scale, so a wrong
     decoding of subnormal codes changes the scores."""
