@@ -231,9 +231,11 @@ def _dev(x, dt, dev):
 class DecodeReplica:
     """One copy of the decode workload's device state (pools + step inputs/outputs)."""
 
-    def __init__(self, base_layer, w, dev, clone: bool):
+    def __init__(self, base_layer, w, dev, clone: bool, side: bool = False):
         import torch
         self.lay = base_layer.clone_pools() if clone else base_layer
+        # decode: the insert runs on a side stream beside the indexer (Layer.step)
+        self.side = torch.cuda.Stream(device=dev) if side else None
         b, q = w.batch, w.queries
         bf = torch.bfloat16
         self.cu = _dev(b.cu, torch.int32, dev)
@@ -253,12 +255,9 @@ class DecodeReplica:
         self.qn = torch.empty_like(self.q)
 
     def step(self):
-        self.lay.compress_insert(self.cu, self.start, self.kv, self.s, self.ik, self.is_,
-                                 dev_err=self.err)
-        self.lay.index_topk(self.q_seq, self.q_pos, self.max_pos, self.q_idx, self.w, self.topk,
-                            dev_err=self.err)
-        self.lay.attention(self.q_seq, self.q_pos, self.max_pos, self.q, self.topk, out=self.out,
-                           dev_err=self.err)
+        self.lay.step(self.cu, self.start, self.kv, self.s, self.ik, self.is_, self.q_seq,
+                      self.q_pos, self.max_pos, self.q, self.q_idx, self.w, out=self.out,
+                      dev_err=self.err, side_stream=self.side, topk_out=self.topk)
 
     def touched_bytes(self):
         n_vis = (self.max_pos - 8) // 4 + 1
@@ -283,10 +282,11 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         return
     w = wl.c4a_decode(seed=rank_seed(rank), B=B, L=L)
     base = Layer.from_host(w.layers[0], dev)
-    r0 = DecodeReplica(base, w, dev, clone=False)
+    side = args.side_stream
+    r0 = DecodeReplica(base, w, dev, clone=False, side=side)
     per_step = r0.touched_bytes()
     n_rep = args.replicas or max(2, int(math.ceil(4.0 * l2 / per_step)))
-    reps = [r0] + [DecodeReplica(base, w, dev, clone=True) for _ in range(n_rep - 1)]
+    reps = [r0] + [DecodeReplica(base, w, dev, clone=True, side=side) for _ in range(n_rep - 1)]
     stream = torch.cuda.current_stream()
 
     # warm-up (also allocates the workspaces), then one graph per replica
@@ -337,6 +337,32 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     algo_bytes_step = per_step
     hbm_gbs = algo_bytes_step / (ms_per_step / 1e3) / 1e9
 
+    # the other variant of the step: the insert on a side stream beside the indexer (or,
+    # when that is the headline, serialised before it), timed the same way
+    for r in reps:
+        r.side = None if side else torch.cuda.Stream(device=dev)
+    alt = []
+    for r in reps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            r.step()
+        alt.append(g)
+    for i in range(args.warmup):
+        alt[i % n_rep].replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        alt[i % n_rep].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_alt = _max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    ms_side, ms_ser = (ms_per_step, ms_alt) if side else (ms_alt, ms_per_step)
+    overlap = {"ms_per_step_side_stream": ms_side, "ms_per_step_serial": ms_ser,
+               "latency_saving": 1.0 - ms_side / ms_ser}
+    del alt
+    for r in reps:
+        r.side = torch.cuda.Stream(device=dev) if side else None
+
     # per-call timing over the same rotating replicas; the roofline line is the slower of
     # the two large calls (both HBM-bound by arithmetic intensity)
     calls = _per_call_times(reps, args.steps, stream)
@@ -367,10 +393,13 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
                    "top_k": 512, "swa": 128, "cache": "fp8 e4m3 + fp32 row scale",
                    "l2": "inputs larger than L2: %d rotating pool replicas, %.1f MB touched per "
                          "step, %.0f MB L2" % (n_rep, per_step / 1e6, l2 / 2 ** 20),
-                   "launch": "one CUDA graph per replica, replayed"},
+                   "launch": "one CUDA graph per replica, replayed; the insert on a side "
+                             "stream beside the indexer" if side else
+                             "one CUDA graph per replica, replayed; serial step"},
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / hbm_peak,
         "per_call_ms": calls,
+        "side_stream": overlap,
         "roofline": roof[dominant],
         "roofline_other": roof["attention" if dominant == "index_topk" else "index_topk"],
         "device_error_bits": err_bits,
@@ -496,7 +525,8 @@ def _e2e(r, w, steps, dev, world):
     def one():
         dev_buf.copy_(host_buf, non_blocking=True)
         kv, s, ik, is_, qq, qi, ww, cu, st, qs, qp = views
-        r.lay.step(cu, st, kv, s, ik, is_, qs, qp, r.max_pos, qq, qi, ww, out=r.out)
+        r.lay.step(cu, st, kv, s, ik, is_, qs, qp, r.max_pos, qq, qi, ww, out=r.out,
+                   side_stream=r.side)
         host_out.copy_(r.out, non_blocking=True)
 
     for _ in range(3):
@@ -568,6 +598,9 @@ def main():
     ap.add_argument("--load-s", type=float, default=1.5, dest="load_s")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, dest="cpu_budget_s")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--side-stream", action="store_true", dest="side_stream",
+                    help="time the step with the decode insert on a side stream as the headline "
+                         "(default: the serial step; the other variant is reported beside it)")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0: enough to exceed 4x L2)")

@@ -146,12 +146,29 @@ class Layer:
         return codes, scale
 
     def step(self, cu, start, kv, s, ik, is_, q_seq, q_pos, max_pos, q, q_idx=None, w=None,
-             out=None, prefill=False, dev_err=None, stream=None):
-        """One pass of the layer: insert the new tokens, select (c4a), attend."""
-        self.compress_insert(cu, start, kv, s, ik, is_, dev_err, stream)
+             out=None, prefill=False, dev_err=None, stream=None, side_stream=None,
+             topk_out=None):
+        """One pass of the layer: insert the new tokens, select (c4a), attend.
+
+        side_stream (c4a decode): the insert runs there while the indexer and top-k run on
+        `stream`; attention waits for both. This is valid only when no query of the call can
+        see an entry completed by the call's own tokens, i.e. every new token of a sequence
+        sits at or after the positions of that sequence's queries (decode: one token at the
+        query's own position). An entry completed by the token at t covers t, and a query
+        at p sees only entries whose positions are all below p.
+        """
+        main = stream if stream is not None else torch.cuda.current_stream()
         topk = None
-        if self.cfg.kind == C4A:
-            topk = self.index_topk(q_seq, q_pos, max_pos, q_idx, w, dev_err=dev_err,
-                                   stream=stream)
+        if side_stream is not None and self.cfg.kind == C4A and not prefill:
+            side_stream.wait_stream(main)
+            topk = self.index_topk(q_seq, q_pos, max_pos, q_idx, w, out=topk_out,
+                                   dev_err=dev_err, stream=main)
+            self.compress_insert(cu, start, kv, s, ik, is_, dev_err, side_stream)
+            main.wait_stream(side_stream)
+        else:
+            self.compress_insert(cu, start, kv, s, ik, is_, dev_err, main)
+            if self.cfg.kind == C4A:
+                topk = self.index_topk(q_seq, q_pos, max_pos, q_idx, w, out=topk_out,
+                                       dev_err=dev_err, stream=main)
         return self.attention(q_seq, q_pos, max_pos, q, topk, out=out, prefill=prefill,
-                              dev_err=dev_err, stream=stream), topk
+                              dev_err=dev_err, stream=main), topk

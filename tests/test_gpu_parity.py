@@ -455,11 +455,13 @@ def test_empty_calls_are_noops():
 
 
 # ------------------------------------------------------------- full-size workloads
-def _full_step(w, li=0, prefill=False):
+def _full_step(w, li=0, prefill=False, side=False):
     h = w.layers[li]
     lay, x, err = device_layer(h), DevInputs(w), _err()
     out, topk = lay.step(x.cu, x.start, x.kv, x.s, x.ik, x.is_, x.q_seq, x.q_pos, x.max_pos,
-                         x.q, x.q_idx, x.w, prefill=prefill, dev_err=err)
+                         x.q, x.q_idx, x.w, prefill=prefill, dev_err=err,
+                         side_stream=torch.cuda.Stream() if side else None)
+    torch.cuda.synchronize()
     assert v4a.v4a_get_error(err) == 0
     return h, out.float().cpu().numpy(), None if topk is None else topk.cpu().numpy()
 
@@ -488,6 +490,34 @@ def test_c4a_decode_full_size_sampled():
     keep, ref = _oracle_sampled(w, h, [0, 7, 19, 31], topk)
     assert len(keep) >= 3
     check_out(out[keep], ref, fp8=True)
+
+
+def test_side_stream_step_equals_serial_step():
+    """The decode step with the insert on a side stream, run eagerly and replayed from a
+    CUDA graph, writes the same bytes (pools, top-k lists, outputs) as the serial step."""
+    w = wl.c4a_decode(seed=41, B=8, L=8192)
+    h = w.layers[0]
+    x, err = DevInputs(w), _err()
+    ser, side_e, side_g = device_layer(h), device_layer(h), device_layer(h)
+    args = (x.cu, x.start, x.kv, x.s, x.ik, x.is_, x.q_seq, x.q_pos, x.max_pos, x.q, x.q_idx,
+            x.w)
+    o_ser, t_ser = ser.step(*args, dev_err=err)
+    side = torch.cuda.Stream()
+    o_e, t_e = side_e.step(*args, dev_err=err, side_stream=side)
+    torch.cuda.synchronize()
+    # graph: warm the workspaces on a scratch copy, capture on the third layer, replay once
+    side_g.clone_pools().step(*args, dev_err=err, side_stream=side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        o_g, t_g = side_g.step(*args, dev_err=err, side_stream=side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert v4a.v4a_get_error(err) == 0
+    for o, t, lay in ((o_e, t_e, side_e), (o_g, t_g, side_g)):
+        assert torch.equal(t, t_ser)
+        assert torch.equal(o, o_ser)
+        _pools_equal(lay, ser)
 
 
 def test_c128a_decode_full_size_sampled():
