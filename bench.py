@@ -300,9 +300,10 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
             r.step()
         graphs.append(g)
     torch.cuda.synchronize()
-    # compress (1) + indexer scores (1) + top-k (1) + attention (1) + split merge (0/1)
-    split = v4a.v4a_attn_workspace_size(base.cfg, B, L, 512, 0) > 256
-    launches_per_step = 4 + int(split)
+    # compress (1) + indexer scores (1) + top-k (1) + attention (1, or 2 with a separate
+    # split merge), as the library plans the call
+    _, attn_kernels = v4a.v4a_attn_plan(base.cfg, B, L, 512, False)
+    launches_per_step = 3 + attn_kernels
 
     def barrier():
         if world > 1:

@@ -17,7 +17,7 @@ __all__ = [
     "V4AError", "LayerCfg", "Cache", "library", "layer_cfg", "cache",
     "v4a_compress_insert", "v4a_compress_insert_qnorm", "v4a_index_topk", "v4a_index_topk_workspace_size",
     "v4a_attn_decode", "v4a_attn_prefill", "v4a_attn_workspace_size", "v4a_slot_mapping",
-    "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size",
+    "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size", "v4a_attn_plan",
     "v4a_get_error", "v4a_version",
     "C4A", "C128A", "FP32", "BF16_FP8", "DEV_MISSING_PAGE", "DEV_BAD_PAGE", "DEV_BAD_INDEX", "DEV_BAD_POS",
 ]
@@ -71,6 +71,8 @@ _SIGS = {
     "v4a_index_topk": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _I32, _P, _P,
                                       _SZ, _P, _P]),
     "v4a_attn_workspace_size": (_SZ, [_CFG, _I32, _I64, _I32, _I32]),
+    "v4a_attn_plan": (ctypes.c_int, [_CFG, _I32, _I64, _I32, _I32, ctypes.POINTER(_I32),
+                                     ctypes.POINTER(_I32)]),
     "v4a_attn_decode": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
                                        _P, _P, _SZ, _P, _P]),
     "v4a_attn_prefill": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
@@ -217,6 +219,15 @@ def v4a_attn_decode(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out,
 
 def v4a_attn_q8_workspace_size(cfg, n_q, max_pos, k) -> int:
     return library().v4a_attn_q8_workspace_size(ctypes.byref(cfg), n_q, max_pos, k)
+
+
+def v4a_attn_plan(cfg, n_q, max_pos, k, prefill=False):
+    """(key ranges per query, kernels per call) of an attention call of this shape."""
+    ns, nk = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("v4a_attn_plan", library().v4a_attn_plan(ctypes.byref(cfg), n_q, max_pos, k,
+                                                     int(prefill), ctypes.byref(ns),
+                                                     ctypes.byref(nk)))
+    return ns.value, nk.value
 
 
 def v4a_attn_decode_q8(cfg, n_q, q_seq, q_pos, max_pos, q, topk, k, attn, swa, out_codes,

@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 5;
+constexpr int32_t kVersion = 6;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -324,6 +324,17 @@ size_t v4a_attn_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t ma
   if (check_cfg(cfg) || n_q < 0 || max_pos < 0) return 0;
   const SplitPlan s = plan_split(cfg, n_q, max_pos, k, k <= 0, prefill != 0);
   return attn_ws(cfg, n_q, s);
+}
+
+int v4a_attn_plan(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int32_t k,
+                  int32_t prefill, int32_t* n_split, int32_t* n_kernels) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (n_q < 0 || max_pos < 0 || !n_split || !n_kernels) return V4A_ERR_ARG;
+  const SplitPlan s = plan_split(cfg, n_q, max_pos, k, k <= 0, prefill != 0);
+  *n_split = s.n_split;
+  *n_kernels = n_q == 0 ? 0 : (s.n_split > 1 ? 2 : 1);   // attention (+ the split merge)
+  return V4A_OK;
 }
 
 int v4a_attn_decode(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,

@@ -236,7 +236,9 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
 // lanes first reduce the split maxima and denominators (split s on lane s % 32), then lane
 // l owns the rotation pairs (d, d+1), d = 2l + 64i, of that head; all partial loads of a
 // group of splits are issued before they are used.
-template <typename OT, int kPairs>
+// kNorm: the partials are o / l in bf16 (the tensor-core kernel's), else o in fp32; the
+// combine is sum_s w_s o_s / sum_s w_s l_s, with o_s = l_s * (o / l)_s in the first case.
+template <typename OT, int kPairs, bool kNorm = false>
 __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -258,11 +260,20 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int s = s0 + u;
-      const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
+      if constexpr (kNorm) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.part_o) + ((row0 + (int64_t)s * H) * D >> 1);
 #pragma unroll
-      for (int i = 0; i < kPairs; ++i)
-        v[u][i] = s < p.n_split ? *reinterpret_cast<const float2*>(src + 2 * lane + 64 * i)
-                                : make_float2(0.f, 0.f);
+        for (int i = 0; i < kPairs; ++i) {
+          const uint32_t w = s < p.n_split ? src[lane + 32 * i] : 0u;
+          v[u][i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        }
+      } else {
+        const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
+#pragma unroll
+        for (int i = 0; i < kPairs; ++i)
+          v[u][i] = s < p.n_split ? *reinterpret_cast<const float2*>(src + 2 * lane + 64 * i)
+                                  : make_float2(0.f, 0.f);
+      }
     }
   };
   load4(0);
@@ -285,9 +296,13 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int s = s0 + u;
-      float ms = -INFINITY;
-      if (s < p.n_split) ms = s < 32 ? __shfl_sync(0xffffffffu, m_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2];
+      float ms = -INFINITY, ls = 0.f;
+      if (s < p.n_split) {
+        ms = s < 32 ? __shfl_sync(0xffffffffu, m_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2];
+        if (kNorm) ls = s < 32 ? __shfl_sync(0xffffffffu, l_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2 + 1];
+      }
       wg[u] = (s < p.n_split && mx != -INFINITY && ms != -INFINITY) ? exp2f(ms - mx) : 0.f;
+      if (kNorm) wg[u] *= ls;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -360,7 +375,7 @@ int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
   {
     e = launch_attention_tc(p, st);
     if (e == cudaSuccess && p.n_split > 1) {
-      e = launch_pdl(attn_merge<__nv_bfloat16, 8>, dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), dim3(256), 0, st, p);
+      e = launch_pdl(attn_merge<__nv_bfloat16, 8, true>, dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), dim3(256), 0, st, p);
       if (e == cudaSuccess) e = cudaGetLastError();
     }
   }

@@ -22,6 +22,8 @@
 // gather/convert warps that also build Q~, 3 = warp 12 allocates TMEM, walks the items
 // converged and issues the MMAs from lane 0 (warps 13-15 idle).
 // Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
+// Decode split: each key range's CTA writes its partial as o / l in bf16 plus (m, l) in
+// fp32; the merge kernel combines the ranges and applies R^-1.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -499,7 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }
       tc::fence_after_sync();
       if (kSplit) {
+        // partial o / l in bf16 (the range's max and denominator go out in fp32): lanes 2i
+        // and 2i+1 hold dims d, d+1; for heads (h, h+1) the even lane stores head h's pair
+        // and the odd lane head h+1's, one 32-bit store each
         const int64_t base = ((int64_t)I.qi * p.n_split + I.split) * kH;
+        uint32_t* part = reinterpret_cast<uint32_t*>(p.part_o);
+        const bool even = (lane & 1) == 0;
         for (int b = 0; b < 4; ++b) {
           const int d = b * 128 + row;
 #pragma unroll
@@ -508,7 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
             tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + half * 32, o);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; ++h) p.part_o[(base + half * 32 + h) * kD + d] = o[h];
+            for (int h = 0; h < 32; h += 2) {
+              const int hh = half * 32 + h;
+              const float a = o[h] * linv[hh], bb = o[h + 1] * linv[hh + 1];
+              const float recv = __shfl_xor_sync(0xffffffffu, even ? bb : a, 1);
+              const uint32_t w = even ? pack_bf16(a, recv) : pack_bf16(recv, bb);
+              const int head = even ? hh : hh + 1, d0 = even ? d : d - 1;
+              part[((base + head) * kD + d0) >> 1] = w;
+            }
           }
         }
         if (row < 64) {

@@ -239,6 +239,14 @@ int v4a_attn_decode(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                     int32_t k, const v4a_cache* attn, const v4a_cache* swa, void* out,
                     void* workspace, size_t workspace_bytes, int32_t* dev_err,
                     v4a_stream_t stream);
+/* v4a_attn_plan — how v4a_attn_decode (prefill = 0) or v4a_attn_prefill (prefill = 1) of
+ * this shape runs on the current device: *n_split = key ranges per query (1 = no split),
+ * *n_kernels = kernels the call launches (0 for n_q = 0; 1, or 2 when a split is combined
+ * by the merge kernel). Host only, enqueues nothing. Returns V4A_ERR_ARG for NULL outputs
+ * or negative sizes. */
+int v4a_attn_plan(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos, int32_t k,
+                  int32_t prefill, int32_t* n_split, int32_t* n_kernels);
+
 /* v4a_attn_decode_q8 — v4a_attn_decode whose epilogue also quantises the output for an fp8
  * output projection ([notes] 优化一, 融合 2：Inverse RoPE + FP8 Quant: the attention output goes
  * through the inverse RoPE and straight into an fp8 batched matmul; [blog] GPU 計算飽和度).

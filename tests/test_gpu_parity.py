@@ -335,6 +335,25 @@ def test_attention_fp8_c4a_lists(prefill):
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
 
+@pytest.mark.parametrize("B,L,plan", [(32, 4096, (3, 2)), (64, 4096, (2, 2)), (16, 4096, (5, 2)),
+                                      (32, 600, (3, 2)), (160, 4096, (1, 1))])
+def test_attention_split_merge_modes(B, L, plan):
+    """Decode attention with 3, 2 or 5 key ranges per query (bf16 o / l partials combined by
+    the merge kernel) and without a split; at L=600 a query sees 149 entries, so its third
+    range holds no key and must not enter the combine."""
+    w = wl.c4a_decode(seed=17, B=B, L=L)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lists = _random_lists(np.random.default_rng(5), q.pos, h.spec, 512)
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    assert v4a.v4a_attn_plan(lay.cfg, B, x.max_pos, 512) == plan
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32), dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
+    check_out(out.float().cpu().numpy(), ref, fp8=True)
+
+
 def _e4m3_step(v):
     """Grid step of the e4m3 value nearest |v| (the spacing a rounding error is bounded by)."""
     g = O.e4m3_values()
@@ -484,8 +503,11 @@ def _oracle_sampled(w, h, sample, topk_gpu):
 
 
 def test_c4a_decode_full_size_sampled():
-    """B=32 sequences of 32768 tokens, one new token and query each (full layer step)."""
+    """B=32 sequences of 32768 tokens, one new token and query each (full layer step; on a
+    152-SM GB300 the attention call splits each query's keys into 3 ranges)."""
     w = wl.c4a_decode()
+    cfg = device_layer(w.layers[0]).cfg
+    assert v4a.v4a_attn_plan(cfg, 32, 32768, 512) == (3, 2)
     h, out, topk = _full_step(w)
     keep, ref = _oracle_sampled(w, h, [0, 7, 19, 31], topk)
     assert len(keep) >= 3
