@@ -175,7 +175,7 @@ int v4a_compress_insert_qnorm(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n
 size_t v4a_index_topk_workspace_size(const v4a_layer_cfg* cfg, int32_t n_q, int64_t max_pos) {
   if (check_cfg(cfg) || n_q < 0 || max_pos < 0) return 0;
   const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
-  return align_up((size_t)n_q * (size_t)max_vis * sizeof(float), 256) + 256;
+  return align_up((size_t)n_q * (size_t)score_row_stride(max_vis) * sizeof(float), 256) + 256;
 }
 
 int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
@@ -204,7 +204,7 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
   p.S = cfg->stride;
   p.win_off = cfg->win_off;
   p.k = k;
-  p.row_stride = max_vis;
+  p.row_stride = score_row_stride(max_vis);
   p.q_seq = q_seq;
   p.q_pos = q_pos;
   p.q_idx = q_idx;

@@ -238,6 +238,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Floats between consecutive indexer score rows: rows start on 16-byte boundaries.
+__host__ __device__ __forceinline__ int64_t score_row_stride(int64_t max_vis) {
+  return (max_vis + 3) & ~(int64_t)3;
+}
+
 // Number of entries visible to a query at p: entry j qualifies iff its last covered
 // position S*j + win_off + W - 1 is < p.
 __host__ __device__ __forceinline__ int64_t visible_entries(int64_t p, int S, int W, int win_off) {

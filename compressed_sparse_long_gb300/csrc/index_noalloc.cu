@@ -76,7 +76,8 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
       (fp8 && (!idx->scale || reinterpret_cast<uintptr_t>(idx->scale) % 16 != 0)))
     return V4A_ERR_ARG;
   const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
-  if ((uint64_t)n_q * (uint64_t)max_vis > kNoallocScoreFloats) return V4A_ERR_TOO_LARGE;
+  if ((uint64_t)n_q * (uint64_t)score_row_stride(max_vis) > kNoallocScoreFloats)
+    return V4A_ERR_TOO_LARGE;
 
   float* scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
@@ -90,7 +91,7 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
   p.S = cfg->stride;
   p.win_off = cfg->win_off;
   p.k = k;
-  p.row_stride = max_vis;
+  p.row_stride = score_row_stride(max_vis);
   p.q_seq = q_seq;
   p.q_pos = q_pos;
   p.q_idx = q_idx;

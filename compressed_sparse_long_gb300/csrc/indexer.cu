@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
   pdl_trigger();
   pdl_wait();
   constexpr int kWarps = THREADS / 32;
-  constexpr int kCnt = ITEMS * kWarps;
-  static_assert(kCnt % 32 == 0, "count table splits over one warp");
+  constexpr int kCnt = kWarps;      // per-warp scan totals
+  static_assert(kWarps <= 32, "one scan total per lane");
   static_assert(ITEMS * THREADS <= 65535, "packed 16-bit counts");
   constexpr int kBuckets = 1024, kCandMax = 512;
   __shared__ uint32_t hist[2][256];
@@ -264,11 +264,19 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
   }
   const float* row = p.scores + (int64_t)qi * p.row_stride;
   const int nn = (int)n;   // <= ITEMS * THREADS (the launcher's choice)
+  // thread t holds entries t*ITEMS .. t*ITEMS + ITEMS-1 (rows start on 16-byte boundaries
+  // and their stride is a multiple of 4, so a group of 4 starting below nn is in the row)
+  static_assert(ITEMS % 4 == 0, "whole float4 groups");
+  const int i0 = tid * ITEMS;
   uint32_t u[ITEMS];
 #pragma unroll
-  for (int r = 0; r < ITEMS; ++r) {
-    const int i = r * THREADS + tid;
-    u[r] = i < nn ? order_key(__ldg(row + i)) : 0u;
+  for (int r = 0; r < ITEMS; r += 4) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i0 + r < nn) x = __ldg(reinterpret_cast<const float4*>(row + i0 + r));
+    u[r] = i0 + r < nn ? order_key(x.x) : 0u;
+    u[r + 1] = i0 + r + 1 < nn ? order_key(x.y) : 0u;
+    u[r + 2] = i0 + r + 2 < nn ? order_key(x.z) : 0u;
+    u[r + 3] = i0 + r + 3 < nn ? order_key(x.w) : 0u;
   }
   for (int i = tid; i < 512; i += THREADS) (&hist[0][0])[i] = 0u;
   for (int i = tid; i < kBuckets; i += THREADS) bhist[i] = 0u;
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
     float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
     for (int r = 0; r < ITEMS; ++r) {
-      if (r * THREADS + tid < nn) {
+      if (i0 + r < nn) {
         const float x = key_value(u[r]);
         lo = fminf(lo, x);
         hi = x != x ? INFINITY : fmaxf(hi, x);   // a NaN score sends the row to the radix path
@@ -294,11 +302,12 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
     }
   }
   __syncthreads();
-  float lo = s_min[0], hi = s_max[0];
+  // every warp reduces the per-warp extremes itself (lane l reads warp l's)
+  float lo = lane < kWarps ? s_min[lane] : INFINITY, hi = lane < kWarps ? s_max[lane] : -INFINITY;
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
-    lo = fminf(lo, s_min[w]);
-    hi = fmaxf(hi, s_max[w]);
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
   uint32_t kth = 0, remaining = 0;
   bool found = false;
@@ -310,31 +319,31 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
     };
 #pragma unroll
     for (int r = 0; r < ITEMS; ++r)
-      if (r * THREADS + tid < nn) atomicAdd(&bhist[bucket(u[r])], 1u);
+      if (i0 + r < nn) atomicAdd(&bhist[bucket(u[r])], 1u);
     __syncthreads();
-    if (warp == 0) {
-      // lane l owns buckets 1023-32l-31 .. 1023-32l, scanned from the top
-      uint32_t sum = 0;
-      for (int j = 0; j < 32; ++j) sum += bhist[kBuckets - 1 - 32 * lane - j];
-      uint32_t incl = sum;
+    // block-wide scan from the top bucket down: thread t owns bucket 1023 - t, a warp scan,
+    // then each warp adds the totals of the warps before it; exactly one thread holds the
+    // bucket where the running count reaches k
+    {
+      static_assert(THREADS == kBuckets, "one bucket per thread");
+      uint32_t* wsum = cnt;   // free until the compaction below
+      const uint32_t c = bhist[kBuckets - 1 - tid];
+      uint32_t incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const uint32_t before = incl - sum, kk = (uint32_t)p.k;
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      uint32_t off = lane < warp ? wsum[lane] : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
+      incl += off;
+      const uint32_t before = incl - c, kk = (uint32_t)p.k;
       if (before < kk && incl >= kk) {
-        uint32_t cum = before;
-        for (int j = 0; j < 32; ++j) {
-          const int b = kBuckets - 1 - 32 * lane - j;
-          const uint32_t c = bhist[b];
-          if (cum + c >= kk) {
-            s_bucket = (uint32_t)b;
-            s_above = cum;
-            break;
-          }
-          cum += c;
-        }
+        s_bucket = (uint32_t)(kBuckets - 1 - tid);
+        s_above = before;
       }
     }
     __syncthreads();
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
     if (bhist[bstar] <= (uint32_t)kCandMax) {          // block-uniform
 #pragma unroll
       for (int r = 0; r < ITEMS; ++r)
-        if (r * THREADS + tid < nn && bucket(u[r]) == bstar) cand[atomicAdd(&s_ncand, 1u)] = u[r];
+        if (i0 + r < nn && bucket(u[r]) == bstar) cand[atomicAdd(&s_ncand, 1u)] = u[r];
       __syncthreads();
       const int nc = (int)s_ncand;
       // the candidate whose key has fewer than r_need keys above it and at least r_need at
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
         for (int i = tid; i < 256; i += THREADS) hist[(pass + 1) & 1][i] = 0u;
 #pragma unroll
       for (int r = 0; r < ITEMS; ++r) {
-        const bool in = r * THREADS + tid < nn && (u[r] & mask) == prefix;
+        const bool in = i0 + r < nn && (u[r] & mask) == prefix;
         const uint32_t bin = in ? (u[r] >> shift) & 0xFFu : 0x100u;
         const uint32_t peers = __match_any_sync(0xffffffffu, bin);
         if (in && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
@@ -423,49 +432,40 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
   }
 
   // kth is the key of the k-th largest score: take every key above it and the first
-  // `remaining` keys equal to it, in index order
-  const uint32_t lt = (1u << lane) - 1u;
+  // `remaining` keys equal to it, in index order. A block-wide exclusive scan of each
+  // thread's (above, equal) counts, packed 16 | 16 bits, gives its first output position.
+  uint32_t g = 0, e = 0;
 #pragma unroll
   for (int r = 0; r < ITEMS; ++r) {
-    const bool v = r * THREADS + tid < nn;
-    const uint32_t bg = __ballot_sync(0xffffffffu, v && u[r] > kth);
-    const uint32_t be = __ballot_sync(0xffffffffu, v && u[r] == kth);
-    if (lane == 0) cnt[r * kWarps + warp] = ((uint32_t)__popc(bg) << 16) | (uint32_t)__popc(be);
+    const bool v = i0 + r < nn;
+    g += (v && u[r] > kth) ? 1u : 0u;
+    e += (v && u[r] == kth) ? 1u : 0u;
   }
-  __syncthreads();
-  if (warp == 0) {
-    constexpr int kPer = kCnt / 32;
-    uint32_t c[kPer], sum = 0;
+  const uint32_t packed = (g << 16) | e;
+  uint32_t incl = packed;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      c[j] = cnt[lane * kPer + j];
-      sum += c[j];
-    }
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    uint32_t ex = incl - sum;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      cnt[lane * kPer + j] = ex;
-      ex += c[j];
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
+  if (lane == 31) cnt[warp] = incl;
   __syncthreads();
+  uint32_t off = lane < kWarps && lane < warp ? cnt[lane] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
+  const uint32_t ex = off + incl - packed;
+  uint32_t n_gt = ex >> 16, n_eq = ex & 0xFFFFu;
 #pragma unroll
   for (int r = 0; r < ITEMS; ++r) {
-    const bool v = r * THREADS + tid < nn;
-    const bool gt = v && u[r] > kth, eq = v && u[r] == kth;
-    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
-    const uint32_t be = __ballot_sync(0xffffffffu, eq);
-    const uint32_t base = cnt[r * kWarps + warp];
-    const uint32_t n_gt = (base >> 16) + (uint32_t)__popc(bg & lt);
-    const uint32_t n_eq = (base & 0xFFFFu) + (uint32_t)__popc(be & lt);
-    const uint32_t at = n_gt + min(n_eq, remaining);
-    if ((gt || (eq && n_eq < remaining)) && at < (uint32_t)p.k) out[at] = r * THREADS + tid;
+    if (i0 + r >= nn) continue;
+    if (u[r] > kth) {
+      const uint32_t at = n_gt + min(n_eq, remaining);
+      if (at < (uint32_t)p.k) out[at] = i0 + r;
+      ++n_gt;
+    } else if (u[r] == kth) {
+      if (n_eq < remaining && n_gt + n_eq < (uint32_t)p.k) out[n_gt + n_eq] = i0 + r;
+      ++n_eq;
+    }
   }
 }
 

@@ -38,6 +38,7 @@ struct IndexParams {
   int32_t H_I, d_I, W, S, win_off;
   int32_t k;
   int64_t row_stride;          // floats between consecutive score rows in the workspace
+                               // (the visible count rounded up to a multiple of 4)
   const int32_t* q_seq;
   const int64_t* q_pos;
   const void* q_idx;

@@ -199,7 +199,8 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
  * Same arguments, meaning and results as v4a_index_topk, minus workspace and
  * workspace_bytes. The score rows live in a fixed 8 MiB array inside the library's device
  * image (held by every GPU that loads the library until the process exits), so
- * n_q * visible(max_pos) must not exceed v4a_index_topk_noalloc_capacity() floats
+ * n_q * visible(max_pos), with visible(max_pos) rounded up to a multiple of 4 (score rows
+ * start on 16-byte boundaries), must not exceed v4a_index_topk_noalloc_capacity() floats
  * (2,097,152; e.g. 64 queries at positions up to 131,072); larger requests return
  * V4A_ERR_TOO_LARGE without enqueuing anything. The call itself allocates nothing.
  * The first call on each device looks up the array's device address while that device
