@@ -282,23 +282,37 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         return
     w = wl.c4a_decode(seed=rank_seed(rank), B=B, L=L)
     base = Layer.from_host(w.layers[0], dev)
-    side = args.side_stream
+    side = not args.serial_step
     r0 = DecodeReplica(base, w, dev, clone=False, side=side)
     per_step = r0.touched_bytes()
     n_rep = args.replicas or max(2, int(math.ceil(4.0 * l2 / per_step)))
     reps = [r0] + [DecodeReplica(base, w, dev, clone=True, side=side) for _ in range(n_rep - 1)]
     stream = torch.cuda.current_stream()
 
-    # warm-up (also allocates the workspaces), then one graph per replica
+    # warm-up (also allocates the workspaces). The timed graphs chain the replicas' steps
+    # the way a model's layers run back to back in one graph: one graph holds one step of
+    # every replica (different batches and pools), consecutive steps linked by
+    # programmatic dependent launch; a tail graph makes the count exactly --steps.
     for r in reps:
         r.step()
     torch.cuda.synchronize()
-    graphs = []
-    for r in reps:
+
+    def capture(rs):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            r.step()
-        graphs.append(g)
+            for r in rs:
+                r.step()
+        return g
+
+    def run_steps(chain, tail, k):
+        for _ in range(k // n_rep):
+            chain.replay()
+        if k % n_rep:
+            tail[k % n_rep].replay()
+
+    chain = capture(reps)
+    tails = {args.steps % n_rep: capture(reps[:args.steps % n_rep])} if args.steps % n_rep else {}
+    graphs = [capture([r]) for r in reps]          # one graph per step, reported beside
     torch.cuda.synchronize()
     # compress (1) + indexer scores (1) + top-k (1) + attention (1, or 2 with a separate
     # split merge), as the library plans the call
@@ -311,22 +325,21 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
 
     # load phase so the clock sampler sees the GPU busy, then the timed region
     with ClockSampler(local_rank) as clk:
-        for i in range(args.warmup):
-            graphs[i % n_rep].replay()
+        for i in range(-(-args.warmup // n_rep)):
+            chain.replay()
         t_end = time.perf_counter() + args.load_s
         i = 0
         while time.perf_counter() < t_end:
-            graphs[i % n_rep].replay()
+            chain.replay()
             i += 1
-            if i % 64 == 0:
+            if i % 8 == 0:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(args.steps):
-            graphs[i % n_rep].replay()
+        run_steps(chain, tails, args.steps)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -338,29 +351,36 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     algo_bytes_step = per_step
     hbm_gbs = algo_bytes_step / (ms_per_step / 1e3) / 1e9
 
+    # the same steps with one graph launch per step (no overlap between steps)
+    for i in range(args.warmup):
+        graphs[i % n_rep].replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i % n_rep].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_one = _max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    del graphs
+
     # the other variant of the step: the insert on a side stream beside the indexer (or,
     # when that is the headline, serialised before it), timed the same way
     for r in reps:
         r.side = None if side else torch.cuda.Stream(device=dev)
-    alt = []
-    for r in reps:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            r.step()
-        alt.append(g)
-    for i in range(args.warmup):
-        alt[i % n_rep].replay()
+    alt_chain = capture(reps)
+    alt_tails = {args.steps % n_rep: capture(reps[:args.steps % n_rep])} if args.steps % n_rep else {}
+    for _ in range(-(-args.warmup // n_rep)):
+        alt_chain.replay()
     torch.cuda.synchronize()
     e0.record(stream)
-    for i in range(args.steps):
-        alt[i % n_rep].replay()
+    run_steps(alt_chain, alt_tails, args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_alt = _max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
     ms_side, ms_ser = (ms_per_step, ms_alt) if side else (ms_alt, ms_per_step)
     overlap = {"ms_per_step_side_stream": ms_side, "ms_per_step_serial": ms_ser,
                "latency_saving": 1.0 - ms_side / ms_ser}
-    del alt
+    del alt_chain, alt_tails
     for r in reps:
         r.side = torch.cuda.Stream(device=dev) if side else None
 
@@ -394,11 +414,13 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
                    "top_k": 512, "swa": 128, "cache": "fp8 e4m3 + fp32 row scale",
                    "l2": "inputs larger than L2: %d rotating pool replicas, %.1f MB touched per "
                          "step, %.0f MB L2" % (n_rep, per_step / 1e6, l2 / 2 ** 20),
-                   "launch": "one CUDA graph per replica, replayed; the insert on a side "
-                             "stream beside the indexer" if side else
-                             "one CUDA graph per replica, replayed; serial step"},
+                   "launch": "one CUDA graph holds one step of each replica (%d steps, linked "
+                             "by programmatic dependent launch, as a model's layers run in one "
+                             "graph), replayed; %s" % (n_rep, "the insert on a side stream beside "
+                             "the indexer" if side else "serial step")},
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / hbm_peak,
+        "ms_per_step_one_graph_per_step": ms_one,
         "per_call_ms": calls,
         "side_stream": overlap,
         "roofline": roof[dominant],
@@ -599,9 +621,9 @@ def main():
     ap.add_argument("--load-s", type=float, default=1.5, dest="load_s")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, dest="cpu_budget_s")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--side-stream", action="store_true", dest="side_stream",
-                    help="time the step with the decode insert on a side stream as the headline "
-                         "(default: the serial step; the other variant is reported beside it)")
+    ap.add_argument("--serial-step", action="store_true", dest="serial_step",
+                    help="time the serial step as the headline (default: the decode insert on a "
+                         "side stream beside the indexer; the other variant is reported beside it)")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0: enough to exceed 4x L2)")

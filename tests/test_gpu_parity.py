@@ -503,12 +503,13 @@ def _oracle_sampled(w, h, sample, topk_gpu):
 
 
 def test_c4a_decode_full_size_sampled():
-    """B=32 sequences of 32768 tokens, one new token and query each (full layer step; on a
-    152-SM GB300 the attention call splits each query's keys into 3 ranges)."""
+    """B=32 sequences of 32768 tokens, one new token and query each: the full layer step as
+    the benchmark runs it (the insert on a side stream beside the indexer; on a 152-SM GB300
+    the attention call splits each query's keys into 3 ranges)."""
     w = wl.c4a_decode()
     cfg = device_layer(w.layers[0]).cfg
     assert v4a.v4a_attn_plan(cfg, 32, 32768, 512) == (3, 2)
-    h, out, topk = _full_step(w)
+    h, out, topk = _full_step(w, side=True)
     keep, ref = _oracle_sampled(w, h, [0, 7, 19, 31], topk)
     assert len(keep) >= 3
     check_out(out[keep], ref, fp8=True)
