@@ -430,7 +430,7 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         "clocks": clk.summary(),
     }
     if not args.skip_e2e:
-        line["e2e"] = _e2e(reps[0], w, args.steps, dev, world)
+        line["e2e"] = _e2e(reps, w, args.steps, dev, world)
     if not args.skip_prefill:
         line["prefill"] = _prefill(dev, tf_peak, tf_sus)
     if rank == 0 and not args.skip_cpu:
@@ -517,11 +517,15 @@ def _profile_traffic(call: str):
     return traffic if ver == v4a.v4a_version() else None
 
 
-def _e2e(r, w, steps, dev, world):
-    """Same step through the public API with host buffers: per step the new tokens and
-    queries go host->device from one pinned buffer (one copy) and the output comes back
-    (one copy). The copies and the step's calls are captured once in a CUDA graph, the way
-    a serving engine drives decode, and the graph is replayed every step."""
+def _e2e(reps, w, steps, dev, world):
+    """Same steps through the public API with host buffers: per step the new tokens and
+    queries go host->device from a pinned buffer (one copy) and the output comes back to
+    pinned memory (one copy). As on the device, one CUDA graph holds one step of every
+    replica. Inputs are double-buffered the way a serving engine overlaps the next batch's
+    upload with the current batch: graph X computes on device buffers X while a copy stream
+    uploads the next graph's inputs into buffers Y, and each step's read-back runs on a
+    second copy stream after its calls. Every step of the timed region thus pays one upload
+    and one read-back; the uploads for the first graph happen before the timed region."""
     import torch
     b, q = w.batch, w.queries
     bf = torch.bfloat16
@@ -533,44 +537,88 @@ def _e2e(r, w, steps, dev, world):
     for t in tensors:
         offs.append(total)
         total += (t.numel() * t.element_size() + 255) // 256 * 256
-    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for t, o in zip(tensors, offs):
-        n = t.numel() * t.element_size()
-        host_buf[o:o + n].copy_(t.reshape(-1).view(torch.uint8))
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = [dev_buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-             for t, o in zip(tensors, offs)]
-    host_out = torch.empty(r.out.shape, dtype=bf).pin_memory()
+    n = len(reps)
+    host_in, host_out = [], []
+    dev_in = [[], []]       # two device input sets
+    views = [[], []]
+    for _ in range(n):
+        hb = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            hb[o:o + nb].copy_(t.reshape(-1).view(torch.uint8))
+        host_in.append(hb)
+        host_out.append(torch.empty(reps[0].out.shape, dtype=bf).pin_memory())
+        for x in range(2):
+            db = torch.empty(total, dtype=torch.uint8, device=dev)
+            dev_in[x].append(db)
+            views[x].append([db[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                             for t, o in zip(tensors, offs)])
     h2d = sum(t.numel() * t.element_size() for t in tensors)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
     stream = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def one():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        kv, s, ik, is_, qq, qi, ww, cu, st, qs, qp = views
-        r.lay.step(cu, st, kv, s, ik, is_, qs, qp, r.max_pos, qq, qi, ww, out=r.out,
-                   side_stream=r.side)
-        host_out.copy_(r.out, non_blocking=True)
+    def steps_of(x, idx, up_idx):
+        """Steps `idx` on input set x; uploads of `up_idx` into set 1 - x beside them."""
+        main = torch.cuda.current_stream()
+        up.wait_stream(main)
+        down.wait_stream(main)
+        with torch.cuda.stream(up):
+            for i in up_idx:
+                dev_in[1 - x][i].copy_(host_in[i], non_blocking=True)
+        for i in idx:
+            r = reps[i]
+            kv, s_, ik, is_, qq, qi, ww, cu, st, qs, qp = views[x][i]
+            r.lay.step(cu, st, kv, s_, ik, is_, qs, qp, r.max_pos, qq, qi, ww, out=r.out,
+                       side_stream=r.side)
+            e_done = torch.cuda.Event()
+            e_done.record(main)
+            down.wait_event(e_done)
+            with torch.cuda.stream(down):
+                host_out[i].copy_(r.out, non_blocking=True)
+        main.wait_stream(up)
+        main.wait_stream(down)
 
-    for _ in range(3):
-        one()
+    def capture(x, idx, up_idx):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            steps_of(x, idx, up_idx)
+        return g
+
+    full = list(range(n))
+    for x in range(2):                      # both input sets filled once, untimed
+        for i in full:
+            dev_in[x][i].copy_(host_in[i])
+    steps_of(0, full, full)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        one()
-    for _ in range(3):
-        g.replay()
+    chains = [capture(0, full, full), capture(1, full, full)]
+    n_chain, rem = steps // n, steps % n
+    # the last graph uploads only what a following graph would need (nothing after it)
+    tail = [capture(0, range(rem), []), capture(1, range(rem), [])] if rem else None
+    for x in range(2):
+        chains[x].replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        g.replay()
+    for c in range(n_chain):
+        chains[c & 1].replay()
+    if tail is not None:
+        tail[n_chain & 1].replay()
     e1.record(stream)
     torch.cuda.synchronize()
+    # the read-back of the last graph holds each of its replicas' output
+    last = range(rem) if rem else range(n)
+    if not all(torch.equal(host_out[i], reps[i].out.cpu()) for i in last):
+        raise SystemExit("e2e: the read-back output differs from the device output")
     ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
+    uploads = n_chain * n            # copies in the timed region, one per step on average
     return {"value": whole_job_rate(B * steps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
-            "launch": "one pinned-buffer copy in, the step's calls, one copy out: one CUDA graph"}
+            "uploads_in_timed_region": uploads, "read_backs_in_timed_region": steps,
+            "launch": "double-buffered inputs: each graph holds one step of each of the %d "
+                      "replicas on one device input set while a copy stream uploads the next "
+                      "graph's inputs into the other; each step's read-back on a second copy "
+                      "stream" % n}
 
 
 def _prefill(dev, tf_peak, tf_sus):
