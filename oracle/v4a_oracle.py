@@ -32,6 +32,9 @@ the design notes of the repository):
       the query position on the output.
   R13 query norm: RMSNorm of each (query, head) row over its D dims, one gamma [D]
       shared by the heads, the entries' epsilon.
+  R16 fp4 indexer cache: e2m1 codes (2 exponent bits, bias 1, 1 mantissa bit), two per
+      byte with element 2i in the low nibble, one scale per 128-dim row = amax / 6 (1 if
+      the row is zero), code = round-to-nearest-even of y / scale saturated to +-6.
 """
 from __future__ import annotations
 
@@ -127,6 +130,77 @@ def quantize(y: np.ndarray):
     return e4m3_encode(y / scale[..., None]), scale
 
 
+# --------------------------------------------------------------------------- fp4
+E2M1_MAX = 6.0
+
+
+def e2m1_values() -> np.ndarray:
+    """Magnitudes of the e2m1 codes 0..7, from the format's definition: 2 exponent bits
+    (bias 1), 1 mantissa bit, exponent 0 subnormal, no infinities or NaN."""
+    out = np.empty(8, dtype=np.float64)
+    for code in range(8):
+        e, m = code >> 1, code & 1
+        out[code] = (m / 2.0) if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1)
+    return out
+
+
+_E2M1 = e2m1_values()
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of 4-bit codes (bit 3 the sign)."""
+    c = np.asarray(codes, dtype=np.int64)
+    mag = _E2M1[c & 7]
+    return np.where(c & 8, -mag, mag)
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Round-to-nearest-even onto the e2m1 grid, saturating at +-6 (R16)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(_E2M1, a, side="left"), 7)   # first grid value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E2M1[lo]
+    d_hi = _E2M1[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a == _E2M1[hi], hi, code)
+    return (code | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def e2m1_midpoint_distance(v) -> np.ndarray:
+    """Distance of |v| from the nearest rounding midpoint of the e2m1 grid, in units of the
+    local grid step (the tests allow a one-code difference only within a hair of a tie)."""
+    a = np.minimum(np.abs(np.asarray(v, dtype=np.float64)), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(_E2M1, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    step = np.maximum(_E2M1[hi] - _E2M1[lo], 1e-300)
+    return np.abs(a - 0.5 * (_E2M1[hi] + _E2M1[lo])) / step
+
+
+def pack_e2m1(codes) -> np.ndarray:
+    """Two codes per byte along the last axis: element 2i in the low nibble, 2i+1 high."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def quantize_fp4(y: np.ndarray):
+    """Row-wise fp4 storage of y (R16): one scale per row, amax / 6 (1 if the row is
+    zero); returns (packed codes uint8 [..., d/2], scale fp64)."""
+    y = np.asarray(y, dtype=np.float64)
+    amax = np.abs(y).max(axis=-1)
+    scale = np.where(amax > 0, amax / E2M1_MAX, 1.0)
+    return pack_e2m1(e2m1_encode(y / scale[..., None])), scale
+
+
 # --------------------------------------------------------------------- paged layout
 def slot(bt: np.ndarray, R: int, seq: int, r: int) -> int:
     """Pool row of logical row r (a token position or an entry index) of sequence seq.
@@ -204,15 +278,21 @@ class Pools:
     def __init__(self, spec, attn, idx, swa, state):
         self.spec = spec
         self.attn = _own(attn)
-        self.idx = _own(idx) if idx is not None else None
+        self.idx = _own(idx, getattr(spec, "idx_fp4", False)) if idx is not None else None
         self.swa = _own(swa)
         self.state = _own(state)
 
 
 class _Pool:
-    def __init__(self, data, scale, bt, R):
+    def __init__(self, data, scale, bt, R, fp4=False):
         self.data, self.scale, self.bt, self.R = data, scale, bt, R
+        self.fp4 = fp4         # packed e2m1 rows (R16) instead of fp8 / raw values
         self.raw = {}          # pool row -> value before fp8 rounding (for the tests)
+
+    def _decode(self, s):
+        if self.fp4:
+            return e2m1_decode(unpack_e2m1(self.data[s])) * np.asarray(self.scale[s])[..., None]
+        return e4m3_decode(self.data[s]) * np.asarray(self.scale[s])[..., None]
 
     def slots(self, seq, rows) -> np.ndarray:
         """slot() of many logical rows of one sequence."""
@@ -226,23 +306,27 @@ class _Pool:
         s = self.slots(seq, rows)
         if (s < 0).any():
             raise ValueError("a row of sequence %d has no page" % seq)
-        if fp8:
-            return e4m3_decode(self.data[s]) * self.scale[s][:, None]
+        if fp8 or self.fp4:
+            return self._decode(s)
         return self.data[s].astype(np.float64)
 
     def read(self, seq, r, fp8):
         s = slot(self.bt, self.R, seq, r)
         if s < 0:
             raise ValueError("row %d of sequence %d has no page" % (r, seq))
-        if fp8:
-            return e4m3_decode(self.data[s]) * float(self.scale[s])
+        if fp8 or self.fp4:
+            return self._decode(s)
         return self.data[s].astype(np.float64)
 
     def write(self, seq, r, y, fp8):
         s = slot(self.bt, self.R, seq, r)
         if s < 0:
             return -1
-        if fp8:
+        if self.fp4:
+            codes, sc = quantize_fp4(y[None, :])
+            self.data[s] = codes[0]
+            self.scale[s] = sc[0]
+        elif fp8:
             codes, sc = quantize(y[None, :])
             self.data[s] = codes[0]
             self.scale[s] = sc[0]
@@ -252,12 +336,12 @@ class _Pool:
         return s
 
 
-def _own(p):
+def _own(p, fp4=False):
     data = np.array(p.data, copy=True)
     if data.dtype != np.uint8:
         data = data.astype(np.float64)
     scale = None if p.scale is None else np.asarray(p.scale, dtype=np.float64).copy()
-    return _Pool(data, scale, np.array(p.bt, copy=True), p.rows_per_block)
+    return _Pool(data, scale, np.array(p.bt, copy=True), p.rows_per_block, fp4)
 
 
 def compress_insert(spec, bias, gamma, ibias, pools: Pools, cu, start, kv, s, ik=None, is_=None):

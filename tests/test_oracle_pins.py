@@ -64,6 +64,79 @@ def test_e4m3_encode_matches_torch_on_all_bf16_patterns():
     assert list(O.e4m3_encode([449.0, 1e6, -1e6])) == [0x7E, 0x7E, 0xFE]
 
 
+def test_e2m1_table_matches_the_published_format():
+    fmt = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_format.json")))
+    vals = O.e2m1_values()
+    assert np.array_equal(vals, fmt["magnitudes"])
+    assert vals.max() == fmt["max_normal"] and vals[2] == fmt["min_normal"]
+    assert vals[1] == fmt["max_subnormal"]
+    # every e2m1 value is an e4m3 value (so an exact e4m3 operand can carry it)
+    assert set(vals.tolist()) <= set(O.e4m3_values().tolist())
+    assert np.array_equal(O.e2m1_decode(np.arange(16)), np.concatenate([vals, -vals]))
+
+
+def test_e2m1_encode_is_nearest_even_by_brute_force():
+    """Against a brute-force search over the 16 codes: nearest value, ties to the code with
+    a zero mantissa bit, saturation at +-6, the sign kept for zero."""
+    vals = O.e2m1_decode(np.arange(16))
+    grid = np.unique(np.abs(vals))
+    mids = 0.5 * (grid[1:] + grid[:-1])
+    v = np.concatenate([grid, mids, mids + 1e-9, mids - 1e-9, np.linspace(-9, 9, 4001),
+                        np.random.default_rng(7).standard_normal(2000) * 3, [-0.0, 0.0, 1e-30]])
+    got = O.e2m1_encode(v)
+    for x, c in zip(v, got):
+        a = min(abs(x), 6.0)
+        d = np.abs(np.abs(vals[:8]) - a)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+        want |= 8 if np.signbit(x) else 0
+        assert c == want, (x, c, want)
+
+
+def test_e2m1_packing_and_row_quantisation():
+    codes = np.array([[1, 2, 3, 15, 8, 0]], dtype=np.uint8)
+    packed = O.pack_e2m1(codes)
+    assert packed.tolist() == [[0x21, 0xF3, 0x08]]          # element 2i in the low nibble
+    assert np.array_equal(O.unpack_e2m1(packed), codes)
+    rng = np.random.default_rng(11)
+    y = rng.standard_normal((64, 128)) * rng.uniform(0.1, 10, (64, 1))
+    p, sc = O.quantize_fp4(y)
+    assert p.shape == (64, 64) and p.dtype == np.uint8
+    assert np.allclose(sc, np.abs(y).max(axis=1) / 6.0)
+    deq = O.e2m1_decode(O.unpack_e2m1(p)) * sc[:, None]
+    # the largest element of each row is stored exactly; every other within half a step
+    i = np.abs(y).argmax(axis=1)
+    assert np.allclose(deq[np.arange(64), i], y[np.arange(64), i])
+    step = np.diff(np.concatenate([O.e2m1_values(), [8.0]]))
+    a = np.abs(y) / sc[:, None]
+    k = np.minimum(np.searchsorted(O.e2m1_values(), a, side="right") - 1, 7)
+    assert np.all(np.abs(deq - y) <= 0.5 * step[k] * sc[:, None] + 1e-12)
+    z, zs = O.quantize_fp4(np.zeros((1, 128)))
+    assert zs[0] == 1.0 and not z.any()
+
+
+def test_fp4_indexer_rows_written_by_the_compressor():
+    """With the fp4 indexer cache, the insert stores each indexer entry as packed e2m1
+    codes + row scale whose dequantised values are within half an e2m1 step (times the
+    row scale) of the exact compressed vector; the attention entries stay fp8."""
+    w = wl.c4a_prefill(seed=5, cached=64, chunk=96, idx_fp4=True)
+    pools = _fresh_pools(w)
+    assert pools.idx.fp4 and pools.idx.data.shape[1] == 64
+    writes = _run_compress(w, pools)
+    idx_slots = [sl for (k, _, _, sl) in writes if k == "idx" and sl >= 0]
+    assert len(idx_slots) >= 20
+    step = np.diff(np.concatenate([O.e2m1_values(), [8.0]]))
+    for sl in idx_slots:
+        y = pools.idx.raw[sl]
+        sc = pools.idx.scale[sl]
+        assert np.isclose(sc, np.abs(y).max() / 6.0)
+        deq = O.e2m1_decode(O.unpack_e2m1(pools.idx.data[sl])) * sc
+        k = np.minimum(np.searchsorted(O.e2m1_values(), np.abs(y) / sc, side="right") - 1, 7)
+        assert np.all(np.abs(deq - y) <= 0.5 * step[k] * sc + 1e-12)
+    a_sl = [sl for (k, _, _, sl) in writes if k == "attn" and sl >= 0]
+    assert pools.attn.data.shape[1] == 512 and len(a_sl) == len(idx_slots)
+
+
 def test_quantize_rows():
     y = np.array([[0.5, -3.0, 1.0], [0.0, 0.0, 0.0]])
     codes, scale = O.quantize(y)

@@ -49,6 +49,7 @@ class LayerSpec:
     eps: float = 1e-6
     win_off: int = 0          # entry j covers S*j+win_off .. S*j+win_off+W-1
     sm_scale: float = 0.0     # 0 -> 1/sqrt(D)
+    idx_fp4: bool = False     # indexer cache in packed 4-bit e2m1 codes + row scale (fp8 layers)
 
     @property
     def W(self) -> int:
@@ -159,6 +160,17 @@ def random_fp8_rows(rng: np.random.Generator, n: int, width: int):
     return codes, scale
 
 
+def random_fp4_rows(rng: np.random.Generator, n: int, width: int):
+    """n random rows of 4-bit codes, two per byte (element 2i in the low nibble):
+    (packed uint8 [n, width / 2], scales float32 [n]). Magnitude codes 0..7 are drawn
+    with weights that roughly follow a rounded normal, signs uniformly."""
+    scale = (rng.uniform(0.5, 1.5, size=n) / 3.0).astype(np.float32)
+    w = np.array([0.10, 0.18, 0.17, 0.15, 0.13, 0.14, 0.08, 0.05])
+    mag = rng.choice(8, size=(n, width), p=w / w.sum()).astype(np.uint8)
+    codes = mag | (rng.integers(0, 2, size=(n, width), dtype=np.uint8) << 3)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), scale
+
+
 def block_table(rng: np.random.Generator, need: list, max_blocks: int):
     """Assign physical pages to the logical blocks listed in need[b] (a set of block ids).
 
@@ -225,7 +237,8 @@ def make_layer(rng, spec: LayerSpec, ctx: list, new: list, prefill_cache: bool,
     attn_d, attn_s = _empty_pool(spec, np_e * R, spec.D, spec.fp8)
     idx_d = idx_s = None
     if spec.has_indexer:
-        idx_d, idx_s = _empty_pool(spec, np_e * R, spec.d_I, spec.fp8)
+        idx_d, idx_s = _empty_pool(spec, np_e * R, spec.d_I // 2 if spec.idx_fp4 else spec.d_I,
+                                   spec.fp8)
     swa_d, swa_s = _empty_pool(spec, np_t * BLOCK, spec.D, spec.fp8)
     st_d = np.zeros((np_t * BLOCK, spec.state_width), np.float32)
     bias, gamma, ibias = (None, None, None)
@@ -242,7 +255,7 @@ def make_layer(rng, spec: LayerSpec, ctx: list, new: list, prefill_cache: bool,
                 c, s = random_fp8_rows(rng, ne, spec.D)
                 layer.attn.data[rows], layer.attn.scale[rows] = c, s
                 if spec.has_indexer:
-                    c, s = random_fp8_rows(rng, ne, spec.d_I)
+                    c, s = (random_fp4_rows if spec.idx_fp4 else random_fp8_rows)(rng, ne, spec.d_I)
                     layer.idx.data[rows], layer.idx.scale[rows] = c, s
             else:
                 layer.attn.data[rows] = rng.standard_normal((ne, spec.D))
