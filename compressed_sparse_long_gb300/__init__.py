@@ -19,13 +19,14 @@ __all__ = [
     "v4a_attn_decode", "v4a_attn_prefill", "v4a_attn_workspace_size", "v4a_slot_mapping",
     "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size", "v4a_attn_plan",
     "v4a_get_error", "v4a_version",
-    "C4A", "C128A", "FP32", "BF16_FP8", "DEV_MISSING_PAGE", "DEV_BAD_PAGE", "DEV_BAD_INDEX", "DEV_BAD_POS",
+    "C4A", "C128A", "FP32", "BF16_FP8", "IDX_DEFAULT", "IDX_FP4", "DEV_MISSING_PAGE", "DEV_BAD_PAGE", "DEV_BAD_INDEX", "DEV_BAD_POS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libv4a.so")
 
 C4A, C128A = 0, 1
 FP32, BF16_FP8 = 0, 1
+IDX_DEFAULT, IDX_FP4 = 0, 1
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4
 DEV_MISSING_PAGE, DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_BAD_POS = 1, 2, 4, 8
 _NAMES = {ERR_ARG: "V4A_ERR_ARG", ERR_UNSUPPORTED: "V4A_ERR_UNSUPPORTED",
@@ -46,7 +47,8 @@ class LayerCfg(ctypes.Structure):
                 ("idx_dim", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("stride", ctypes.c_int32), ("win_off", ctypes.c_int32),
                 ("swa", ctypes.c_int32), ("rope_base", ctypes.c_float),
-                ("rms_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+                ("idx_format", ctypes.c_int32)]
 
 
 class Cache(ctypes.Structure):
@@ -130,19 +132,20 @@ def _check(fn: str, rc: int):
 def layer_cfg(kind: int, dtype: int, head_dim: int, rope_dim: int, n_heads: int,
               idx_heads: int, idx_dim: int, window: int, stride: int, win_off: int = 0,
               swa: int = 128, rope_base: float = 10000.0, rms_eps: float = 1e-6,
-              softmax_scale: float | None = None) -> LayerCfg:
+              softmax_scale: float | None = None, idx_format: int = 0) -> LayerCfg:
     return LayerCfg(kind, dtype, head_dim, rope_dim, n_heads, idx_heads, idx_dim, window,
                     stride, win_off, swa, rope_base, rms_eps,
-                    softmax_scale if softmax_scale else head_dim ** -0.5)
+                    softmax_scale if softmax_scale else head_dim ** -0.5, idx_format)
 
 
 def cache(data: torch.Tensor, scale: torch.Tensor | None, block_table: torch.Tensor,
-          rows_per_block: int) -> Cache:
-    """Describe a paged pool. The tensors must stay alive while the library uses them."""
+          rows_per_block: int, elems_per_byte: int = 1) -> Cache:
+    """Describe a paged pool. The tensors must stay alive while the library uses them.
+    elems_per_byte = 2 for a pool of packed fp4 rows (uint8 data, two elements a byte)."""
     assert data.dim() == 2 and block_table.dim() == 2 and block_table.dtype == torch.int32
     return Cache(data.data_ptr(), None if scale is None else scale.data_ptr(),
                  block_table.data_ptr(), block_table.shape[1], rows_per_block,
-                 data.shape[0] // rows_per_block, data.shape[1], 0)
+                 data.shape[0] // rows_per_block, data.shape[1] * elems_per_byte, 0)
 
 
 def v4a_version() -> int:

@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 6;
+constexpr int32_t kVersion = 7;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -47,8 +47,23 @@ int check_cfg(const v4a_layer_cfg* c) {
   if (c->win_off > 0 || c->win_off <= -c->window) return V4A_ERR_ARG;
   if (c->swa <= 0) return V4A_ERR_ARG;
   if (!(c->rms_eps >= 0.f) || !(c->softmax_scale > 0.f) || !(c->rope_base > 0.f)) return V4A_ERR_ARG;
+  if (c->idx_format != V4A_IDX_DEFAULT && c->idx_format != V4A_IDX_FP4) return V4A_ERR_UNSUPPORTED;
+  if (c->idx_format == V4A_IDX_FP4 &&
+      (c->dtype != V4A_BF16_FP8 || c->kind != V4A_C4A || c->idx_dim != 128))
+    return V4A_ERR_UNSUPPORTED;
   return V4A_OK;
 }
+
+}  // namespace
+
+// The indexer pool as the kernels see it: width in bytes for packed fp4 rows.
+CacheView v4a::idx_view(const v4a_layer_cfg* cfg, const v4a_cache* idx) {
+  CacheView v = view_of(idx);
+  if (cfg->idx_format == V4A_IDX_FP4) v.width = idx->row_width / 2;
+  return v;
+}
+
+namespace {
 
 int check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8) {
   if (!c || !c->data || !c->block_table) return V4A_ERR_ARG;
@@ -133,7 +148,8 @@ int compress_common(const v4a_layer_cfg* cfg, int32_t n_seq, int32_t n_tokens,
   p.ibias = c4a ? ibias : nullptr;
   if (n_tokens > 0) {
     p.attn = view_of(attn);
-    p.idx = c4a ? view_of(idx) : CacheView{};
+    p.idx = c4a ? idx_view(cfg, idx) : CacheView{};
+    p.idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
     p.swa = view_of(swa);
     p.state = view_of(state);
   }
@@ -209,7 +225,8 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
   p.q_pos = q_pos;
   p.q_idx = q_idx;
   p.w = w;
-  p.idx = view_of(idx);
+  p.idx = idx_view(cfg, idx);
+  p.idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
   p.scores = reinterpret_cast<float*>(workspace);
   p.topk = topk_out;
   p.err = dev_err;

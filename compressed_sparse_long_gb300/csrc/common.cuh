@@ -164,6 +164,31 @@ __device__ __forceinline__ uint16_t e4m3x2_encode(float lo, float hi) {
   return (uint16_t)r;
 }
 
+// ---------------------------------------------------------------- fp4 e2m1
+constexpr float kE2m1Max = 6.0f;
+
+// Encode: round-to-nearest-even onto the e2m1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6},
+// saturating to +-6; bit 3 is the sign. Each comparison is a rounding midpoint, strict
+// where the lower neighbour has the odd code (so a tie goes to the even code).
+__device__ __forceinline__ uint32_t e2m1_encode(float v) {
+  const float a = fminf(fabsf(v), kE2m1Max);
+  const uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                     (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+                     (uint32_t)(a > 5.0f);
+  return m | (signbit(v) ? 8u : 0u);
+}
+
+// Expand four e2m1 codes (one 16-bit group, code k in bits 4k..4k+3) into four e4m3 codes
+// (byte k of the result). Every e2m1 value is an e4m3 value: the magnitudes map to the
+// e4m3 codes 0x00 0x30 0x38 0x3C 0x40 0x44 0x48 0x4C (a byte permute looks them up) and
+// the sign bit moves to bit 7 of its byte.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t x) {
+  const uint32_t mag = __byte_perm(0x3C383000u, 0x4C484440u, x & 0x7777u);
+  const uint32_t sg = ((x & 0x8u) << 4) | ((x & 0x80u) << 8) | ((x & 0x800u) << 12) |
+                      ((x & 0x8000u) << 16);
+  return mag | sg;
+}
+
 // Decode 4 codes (one 32-bit word, code k in byte k) to fp32. e4m3 -> f16 is exact.
 __device__ __forceinline__ void e4m3x4_decode(uint32_t w, float (&f)[4]) {
   uint32_t h01, h23;

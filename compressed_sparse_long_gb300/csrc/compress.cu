@@ -78,6 +78,26 @@ struct CompressKernel {
     }
   }
 
+  // fp4 row store: per-row scale amax/6 (1 if the row is zero), e2m1 round-to-nearest-even
+  // of y/scale; lane l owns elements [N l, N l + N), i.e. bytes [N l / 2, N l / 2 + N / 2)
+  // of the packed row (element 2i in the low nibble).
+  template <int N>
+  static __device__ __forceinline__ void store_row_fp4(const CacheView& c, int64_t slot, float (&y)[N],
+                                                       int lane) {
+    static_assert(N == 4, "one 16-bit group of four codes per lane");
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < N; ++k) amax = fmaxf(amax, fabsf(y[k]));
+    amax = warp_max(amax);
+    const float scale = amax > 0.f ? __fdiv_rn(amax, kE2m1Max) : 1.0f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int k = 0; k < N; ++k) packed |= e2m1_encode(__fdiv_rn(y[k], scale)) << (4 * k);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(c.data) + slot * (int64_t)c.width + lane * (N / 2);
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+    if (lane == 0) c.scale[slot] = scale;
+  }
+
   // Rotate the lane's channels that fall in the rotated tail (adjacent pairs).
   template <int N>
   static __device__ __forceinline__ void rope_lane(const Rope& rp, float (&y)[N], int lane,
@@ -292,7 +312,12 @@ struct CompressKernel {
         float c[ICPL];
 #pragma unroll
         for (int k = 0; k < ICPL; ++k) c[k] = __fdiv_rn(iacc[k], il[k]);
-        store_row<ICPL>(p.idx, i_slot, c, lane);
+        if constexpr (kFp8 && ICPL == 4) {
+          if (p.idx_fp4) store_row_fp4<ICPL>(p.idx, i_slot, c, lane);
+          else store_row<ICPL>(p.idx, i_slot, c, lane);
+        } else {
+          store_row<ICPL>(p.idx, i_slot, c, lane);
+        }
       }
     }
   }

@@ -64,6 +64,9 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
   if (cfg->dtype != V4A_FP32 && cfg->dtype != V4A_BF16_FP8) return V4A_ERR_UNSUPPORTED;
   if (cfg->window <= 0 || cfg->stride <= 0 || kBlock % cfg->stride != 0) return V4A_ERR_UNSUPPORTED;
   if (cfg->win_off > 0 || cfg->win_off <= -cfg->window) return V4A_ERR_ARG;
+  if (cfg->idx_format != V4A_IDX_DEFAULT && cfg->idx_format != V4A_IDX_FP4) return V4A_ERR_UNSUPPORTED;
+  if (cfg->idx_format == V4A_IDX_FP4 && (cfg->dtype != V4A_BF16_FP8 || cfg->idx_dim != 128))
+    return V4A_ERR_UNSUPPORTED;
   if (n_q < 0 || k <= 0 || max_pos < 0) return V4A_ERR_ARG;
   if (n_q == 0) return V4A_OK;
   if (!q_seq || !q_pos || !q_idx || !w || !topk_out) return V4A_ERR_ARG;
@@ -96,7 +99,8 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
   p.q_pos = q_pos;
   p.q_idx = q_idx;
   p.w = w;
-  p.idx = view_of(idx);
+  p.idx = idx_view(cfg, idx);
+  p.idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
   p.scores = scratch;
   p.topk = topk_out;
   p.err = dev_err;

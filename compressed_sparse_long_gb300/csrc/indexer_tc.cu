@@ -35,6 +35,8 @@
 // of the units of all groups (found with a block scan), so long and short rows balance.
 // Every wait is bounded (~1 s): on expiry the CTA sets V4A_DEV_TIMEOUT, drains its copies
 // and MMAs, frees its TMEM and returns.
+#include <cstring>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
@@ -50,30 +52,43 @@ constexpr int kHI = 64;
 constexpr int kDI = 128;
 constexpr int kTile = 128;                  // entries per tile
 constexpr int kPageBytes = 64 * kDI;        // one 64-entry page of fp8 codes
-constexpr int kStageBytes = kTile * kDI;    // codes of one tile (two pages)
-// a stage: codes, then the two pages' ids (-1: no page, -2: id outside the pool); stages
-// stay 1 KB aligned for the swizzled copies
-constexpr int kStageMetaOff = kStageBytes;
-constexpr int kStageStride = kStageBytes + 1024;
-constexpr int kThreads = 480;              // 15 warps (128 registers a thread)
+constexpr int kPackedPageBytes = 64 * kDI / 2;   // one 64-entry page of packed fp4 codes
+constexpr int kStageBytes = kTile * kDI;    // e4m3 operand of one tile (two pages)
 constexpr int kEpi0 = 2, kPrep0 = 10;       // first epilogue / query-preparation warp
-constexpr int kProd1 = 12;                  // producers: warp 0 and warps 12-14
+constexpr int kProd1 = 12;                  // producers: warp 0 and warps 12-14 (fp8) or 12 (fp4)
+constexpr int kExp0 = 13;                   // fp4: expanders are warps 13-15
 
-template <int NQ>
+// Threads of the fp8 (15 warps) and fp4 (16 warps) kernels, 128 registers a thread.
+template <bool kFp4>
+constexpr int threads_of() { return kFp4 ? 512 : 480; }
+
+// A stage: the e4m3 operand of a tile (swizzled, fed to the product), for fp4 the two
+// packed pages it is expanded from, then the two pages' ids (-1: no page, -2: id outside
+// the pool). Stages stay 1 KB aligned for the swizzled layout.
+template <bool kFp4>
+struct StageGeo {
+  static constexpr int kPackOff = kStageBytes;                          // fp4 only
+  static constexpr int kMetaOff = kFp4 ? kStageBytes + 2 * kPackedPageBytes : kStageBytes;
+  static constexpr int kStride = kMetaOff + 1024;
+};
+
+template <int NQ, bool kFp4>
 struct Layout {
   static constexpr int N = NQ * 2 * kHI;    // hi and lo rows of each query
-  static constexpr int kStages = NQ == 1 ? 10 : 8;   // even: tiles alternate producer pairs
+  // fp8: even, tiles alternate producer pairs; fp4: the stage holds the packed pages too
+  static constexpr int kStages = kFp4 ? 6 : (NQ == 1 ? 10 : 8);
   static constexpr int kBBytes = N * kDI;   // fp8 B operand of one group
   static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators (512 columns)
   static constexpr int kTmemCols = kAcc * N;
   static constexpr int off_stage = 0;
-  static constexpr int off_b = kStages * kStageStride;            // 1 KB aligned
+  static constexpr int off_b = kStages * StageGeo<kFp4>::kStride;  // 1 KB aligned
   static constexpr int off_w = off_b + 2 * kBBytes;               // w_h / s_h [2][NQ * 64]
   static constexpr int off_bar = off_w + 2 * NQ * kHI * 4;
-  static constexpr int n_bar = 2 * kStages + 2 * kAcc + 6 + 1;
+  static constexpr int n_bar = (kFp4 ? 3 : 2) * kStages + 2 * kAcc + 6 + 1;
   static constexpr int off_misc = off_bar + n_bar * 8;
   static constexpr int bytes = off_misc + 128 + 1024;  // + alignment slack
   static_assert(off_b % 1024 == 0, "swizzled operands need 1 KB alignment");
+  static_assert(bytes <= 227 * 1024, "shared memory of one CTA");
 };
 
 // tcgen05.mma kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format
@@ -206,6 +221,7 @@ struct Walk {
 
 // Inclusive block-wide scan of one int per thread (kThreads threads); returns the
 // inclusive value, the chunk total in *total.
+template <int kThreads>
 __device__ __forceinline__ int block_scan(int v, int* warp_buf, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -233,10 +249,12 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int* total) {
   return r;
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_constant__ IndexParams p,
-                                                                const __grid_constant__ CUtensorMap pages) {
-  using Lay = Layout<NQ>;
+template <int NQ, bool kFp4>
+__global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const __grid_constant__ IndexParams p,
+                                                                          const __grid_constant__ CUtensorMap pages) {
+  using Lay = Layout<NQ, kFp4>;
+  using Geo = StageGeo<kFp4>;
+  constexpr int kThreads = threads_of<kFp4>();
   constexpr int N = Lay::N;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -253,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   uint64_t* bempty = bfull + 2;    // [2] products of the group done
   uint64_t* egone = bempty + 2;    // [2] epilogue left the group
   uint64_t* done = egone + 2;
+  uint64_t* xfull = done + 1;      // fp4: [kStages] the tile's operand expanded
   int* misc = reinterpret_cast<int*>(sm + Lay::off_misc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
@@ -282,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       tc::mbar_init(egone + i, 8);
     }
     tc::mbar_init(done, 1);
+    if (kFp4)
+      for (int i = 0; i < Lay::kStages; ++i) tc::mbar_init(xfull + i, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
   if (n_groups <= kThreads) {
     const int g = tid;
     const int u = g < n_groups ? load_group<NQ>(p, g, true).units : 0;
-    const int incl = block_scan(u, scan_buf, scan_tot);
+    const int incl = block_scan<kThreads>(u, scan_buf, scan_tot);
     total_units = *scan_tot;
     const int64_t ub = (int64_t)total_units * blockIdx.x / gridDim.x;
     if (tid == 0) { s_g0 = n_groups; s_off = 0; }
@@ -310,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     const int g = base + tid;
     const int u = g < n_groups ? load_group<NQ>(p, g, true).units : 0;
     int tot;
-    block_scan(u, scan_buf, scan_tot);
+    block_scan<kThreads>(u, scan_buf, scan_tot);
     tot = *scan_tot;
     total_units += tot;
     __syncthreads();
@@ -324,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
     for (int base = 0; base < n_groups; base += kThreads) {
       const int g = base + tid;
       const int u = g < n_groups ? load_group<NQ>(p, g, false).units : 0;
-      const int incl = block_scan(u, scan_buf, scan_tot) + run;
+      const int incl = block_scan<kThreads>(u, scan_buf, scan_tot) + run;
       const int excl = incl - u;
       if (u > 0 && excl <= u_begin && u_begin < incl) {
         s_g0 = g;
@@ -369,10 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
 
   constexpr uint32_t idesc = idesc_e4m3(kTile, N);
 
-  if (warp == 0 || warp >= kProd1) {
+  if (warp == 0 || (warp >= kProd1 && warp < (kFp4 ? kProd1 + 1 : kProd1 + 3))) {
     // ------------------------------------------------------------------ producers
+    // fp8: four warps, page ph of the tiles i % 2 == parity; fp4: two warps, page ph of
+    // every tile (a packed page is a 4 KB bulk copy into the stage's packed area)
     const int pw = warp == 0 ? 0 : warp - kProd1 + 1;
-    const int ph = pw & 1, parity = pw >> 1;            // page of the tile, tiles i % 2 == parity
+    const int ph = pw & 1, parity = kFp4 ? 0 : pw >> 1;
     // The whole warp keeps the page ids of 32 consecutive blocks (16 tiles) of the current
     // sequence in registers, one per lane; lane 0 waits on the ring and issues the copy.
     pdl_wait();
@@ -386,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         if (w.g >= n_groups) break;                    // every role stops at the same tile
-        if ((i & 1) != parity) {                       // the other pair's tile (stages of
+        if (!kFp4 && (i & 1) != parity) {              // the other pair's tile (stages of
           w.next(p, n_groups);                         // one parity: kStages is even)
           continue;
         }
@@ -406,15 +429,22 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        uint8_t* sb = stage + st * kStageStride;
+        uint8_t* sb = stage + st * Geo::kStride;
         const int32_t page = ph ? pg1 : pg0;
         bool copied = false;
         if (lane == 0) {
           const bool valid = page >= 0 && page < p.idx.n_pages;
-          reinterpret_cast<int*>(sb + kStageMetaOff)[ph] = valid ? page : (page >= p.idx.n_pages ? -2 : -1);
+          reinterpret_cast<int*>(sb + Geo::kMetaOff)[ph] = valid ? page : (page >= p.idx.n_pages ? -2 : -1);
           if (valid) {
-            tc::mbar_arrive_tx(full + st, kPageBytes);
-            tma_load_2d(sb + ph * kPageBytes, &pages, 0, page * 64, full + st);
+            if constexpr (kFp4) {
+              tc::mbar_arrive_tx(full + st, kPackedPageBytes);
+              tc::bulk_g2s(sb + Geo::kPackOff + ph * kPackedPageBytes,
+                           reinterpret_cast<const uint8_t*>(p.idx.data) + (int64_t)page * kPackedPageBytes,
+                           kPackedPageBytes, full + st);
+            } else {
+              tc::mbar_arrive_tx(full + st, kPageBytes);
+              tma_load_2d(sb + ph * kPageBytes, &pages, 0, page * 64, full + st);
+            }
             copied = true;
           } else {
             tc::mbar_arrive(full + st);
@@ -427,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       }
       if (lane == 0 && *abort_flag) {   // drain this warp's copies still in flight
         for (int i = issued > Lay::kStages ? issued - Lay::kStages : 0; i < issued; ++i)
-          if ((i & 1) == parity && (had_copy & (1u << (i % Lay::kStages))))
+          if ((kFp4 || (i & 1) == parity) && (had_copy & (1u << (i % Lay::kStages))))
             tc::mbar_wait_drain(full + i % Lay::kStages, (i / Lay::kStages) & 1);
       }
     }
@@ -446,14 +476,16 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
           prev_g = w.g;
         }
         const int st = i % Lay::kStages, tb = i % Lay::kAcc;
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err))) break;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait((kFp4 ? xfull : full) + st, (i / Lay::kStages) & 1,
+                                                   abort_flag, p.err)))
+          break;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(tempty + tb, ((i / Lay::kAcc) & 1) ^ 1, abort_flag, p.err))) break;
         tc::fence_after_sync();
         const int g_here = w.g;
         w.next(p, n_groups);
         if (lane == 0) {
           const uint32_t d = tmem + tb * N;
-          const uint64_t ad0 = tc::sdesc_sw128(s0 + st * kStageStride, 16, 1024);
+          const uint64_t ad0 = tc::sdesc_sw128(s0 + st * Geo::kStride, 16, 1024);
           const uint64_t bd0 = tc::sdesc_sw128(b0 + (gc & 1) * Lay::kBBytes, 16, 1024);
 #pragma unroll
           for (int k = 0; k < kDI / 32; ++k)   // K = 32 codes = 32 bytes = 2 descriptor units
@@ -470,6 +502,39 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       }
     }
     __syncwarp();
+  } else if (kFp4 && warp >= kExp0) {
+    // ------------------------------------------------------------------ fp4 expanders
+    // Warp kExp0 + e takes the tiles i % 3 == e: once a tile's packed pages have landed,
+    // row r's codes (64 bytes at r * 64 of the packed area) become its 128 e4m3 codes in
+    // the swizzled operand layout, 16 bytes (8 packed bytes) per lane and step.
+    const int e = warp - kExp0;
+    Walk<NQ> w = start;
+    for (int i = 0; i < n_units; ++i) {
+      if (w.g >= n_groups) break;
+      if (i % 3 != e) {
+        w.next(p, n_groups);
+        continue;
+      }
+      const int st = i % Lay::kStages;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err))) break;
+      uint8_t* sb = stage + st * Geo::kStride;
+      const uint8_t* pk = sb + Geo::kPackOff;
+#pragma unroll 4
+      for (int it = 0; it < kTile * 8 / 32; ++it) {
+        const int q = it * 32 + lane, r = q >> 3, c = q & 7;
+        const uint2 v = *reinterpret_cast<const uint2*>(pk + r * 64 + c * 8);
+        uint4 o;
+        o.x = e2m1x4_to_e4m3x4(v.x & 0xFFFFu);
+        o.y = e2m1x4_to_e4m3x4(v.x >> 16);
+        o.z = e2m1x4_to_e4m3x4(v.y & 0xFFFFu);
+        o.w = e2m1x4_to_e4m3x4(v.y >> 16);
+        *reinterpret_cast<uint4*>(sb + tc::sw128_off(r, c)) = o;
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(xfull + st);
+      w.next(p, n_groups);
+    }
   } else if (warp >= kPrep0 && warp < kProd1) {
     // ------------------------------------------------------------------ query preparation
     // Per group: B rows qq*128 + h (hi) and qq*128 + 64 + h (lo), 128 bytes each, K-major
@@ -577,8 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_tc(const __grid_cons
       // the tile's page ids arrive with its codes; the row scale load is issued now and
       // used after the product
       if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
-      const uint8_t* sb = stage + st * kStageStride;
-      const int page = reinterpret_cast<const int*>(sb + kStageMetaOff)[row >> 6];
+      const uint8_t* sb = stage + st * Geo::kStride;
+      const int page = reinterpret_cast<const int*>(sb + Geo::kMetaOff)[row >> 6];
       const float sc = page >= 0 ? __ldg(p.idx.scale + (int64_t)page * 64 + (row & 63)) : 0.f;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty + st);
@@ -649,31 +714,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int NQ>
+template <int NQ, bool kFp4>
 cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
-  using Lay = Layout<NQ>;
+  using Lay = Layout<NQ, kFp4>;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // the pool as a 2-D byte tensor [n_pages * 64 rows][128], one page per box, 128B swizzle
+  // fp8: the pool as a 2-D byte tensor [n_pages * 64 rows][128], one page per box, 128B
+  // swizzle; fp4 pages are plain bulk copies (the map is unused)
   CUtensorMap map;
-  auto enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)kDI, (cuuint64_t)p.idx.n_pages * 64};
-  const cuuint64_t strides[1] = {(cuuint64_t)kDI};
-  const cuuint32_t box[2] = {(cuuint32_t)kDI, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.idx.data, dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  memset(&map, 0, sizeof(map));
+  if (!kFp4) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)kDI, (cuuint64_t)p.idx.n_pages * 64};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDI};
+    const cuuint32_t box[2] = {(cuuint32_t)kDI, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.idx.data, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int64_t n_groups = (p.n_q + NQ - 1) / NQ;
   const int64_t max_units = n_groups * NQ * ((max_vis + kTile - 1) / kTile);
   const int grid = (int)(max_units < sms ? (max_units > 0 ? max_units : 1) : sms);
-  cudaError_t e = cudaFuncSetAttribute(index_scores_tc<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(index_scores_tc<NQ, kFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Lay::bytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(index_scores_tc<NQ>, dim3(grid), dim3(kThreads), Lay::bytes, st, p, map);
+  e = launch_pdl(index_scores_tc<NQ, kFp4>, dim3(grid), dim3(threads_of<kFp4>()), Lay::bytes, st, p, map);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -684,8 +753,12 @@ cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
 // (prefill) are taken two at a time (N = 256) so each key tile feeds two queries.
 cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.idx.n_pages <= 0 || p.idx.n_pages * 64 > INT32_MAX) return cudaErrorInvalidValue;
-  if (p.n_q >= 1024) return launch_tc<2>(p, max_vis, st);
-  return launch_tc<1>(p, max_vis, st);
+  if (p.idx_fp4) {
+    if (p.n_q >= 1024) return launch_tc<2, true>(p, max_vis, st);
+    return launch_tc<1, true>(p, max_vis, st);
+  }
+  if (p.n_q >= 1024) return launch_tc<2, false>(p, max_vis, st);
+  return launch_tc<1, false>(p, max_vis, st);
 }
 
 }  // namespace v4a

@@ -26,6 +26,7 @@ struct CompressParams {
   CacheView attn, idx, swa, state;
   Rope rope;
   int32_t* err;
+  int32_t idx_fp4;             // indexer rows as packed e2m1 + row scale (idx.width in bytes)
   // query RMSNorm rows handled by the warps after the n_tokens insert warps (0: none)
   int64_t n_qrows;             // n_q * H rows of D elements
   const void* q;               // [n_qrows, D] input type
@@ -44,6 +45,7 @@ struct IndexParams {
   const void* q_idx;
   const float* w;
   CacheView idx;
+  int32_t idx_fp4;             // indexer rows as packed e2m1 + row scale (idx.width in bytes)
   float* scores;               // workspace [n_q, row_stride]
   int32_t* topk;               // [n_q, k]
   int32_t* err;
@@ -69,6 +71,8 @@ struct AttnParams {
   int32_t* err;
 };
 
+// The indexer pool as the kernels see it (width in bytes for packed fp4 rows).
+CacheView idx_view(const v4a_layer_cfg* cfg, const v4a_cache* idx);
 int launch_compress_insert(const CompressParams& p, int dtype, cudaStream_t st);
 int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaStream_t st);
 cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st);

@@ -11,7 +11,8 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (BF16_FP8, C4A, C128A, FP32, cache, layer_cfg, v4a_attn_decode,
+from . import (BF16_FP8, C4A, C128A, FP32, IDX_DEFAULT, IDX_FP4, cache, layer_cfg,
+               v4a_attn_decode,
                v4a_attn_decode_q8, v4a_attn_q8_workspace_size,
                v4a_attn_prefill, v4a_attn_workspace_size, v4a_compress_insert,
                v4a_compress_insert_qnorm,
@@ -28,23 +29,26 @@ class PagedPool:
     scale: torch.Tensor | None
     block_table: torch.Tensor
     rows_per_block: int
+    elems_per_byte: int = 1      # 2 for packed fp4 rows
 
     @property
     def c(self):
-        return cache(self.data, self.scale, self.block_table, self.rows_per_block)
+        return cache(self.data, self.scale, self.block_table, self.rows_per_block,
+                     self.elems_per_byte)
 
     def clone(self) -> "PagedPool":
         return PagedPool(self.data.clone(), None if self.scale is None else self.scale.clone(),
-                         self.block_table.clone(), self.rows_per_block)
+                         self.block_table.clone(), self.rows_per_block, self.elems_per_byte)
 
 
-def pool_from_host(p, elem_dtype, device) -> PagedPool:
+def pool_from_host(p, elem_dtype, device, elems_per_byte=1) -> PagedPool:
     if p.data.dtype == np.uint8:
         data = torch.from_numpy(np.ascontiguousarray(p.data)).to(device)
     else:
         data = _t(p.data, elem_dtype, device)
     scale = None if p.scale is None else _t(p.scale, torch.float32, device)
-    return PagedPool(data, scale, _t(p.bt, torch.int32, device), p.rows_per_block)
+    return PagedPool(data, scale, _t(p.bt, torch.int32, device), p.rows_per_block,
+                     elems_per_byte)
 
 
 class Layer:
@@ -63,14 +67,16 @@ class Layer:
         """h: object with spec (kind, fp8, D, d_r, H, H_I, d_I, W, S, win_off, swa, rope_base,
         eps, scale, top_k), bias, gamma, ibias and paged pools attn, idx, swa, state."""
         s = h.spec
+        fp4 = bool(getattr(s, "idx_fp4", False))
         cfg = layer_cfg(C4A if s.kind == "c4a" else C128A, BF16_FP8 if s.fp8 else FP32, s.D,
                         s.d_r, s.H, s.H_I, s.d_I, s.W, s.S, s.win_off, s.swa, s.rope_base,
-                        s.eps, s.scale)
+                        s.eps, s.scale, IDX_FP4 if fp4 else IDX_DEFAULT)
         in_dt = torch.bfloat16 if s.fp8 else torch.float32
         ib = None if h.ibias is None else _t(h.ibias, torch.float32, device)
         return Layer(cfg, _t(h.bias, torch.float32, device), _t(h.gamma, torch.float32, device),
                      ib, pool_from_host(h.attn, torch.float32, device),
-                     None if h.idx is None else pool_from_host(h.idx, torch.float32, device),
+                     None if h.idx is None else pool_from_host(h.idx, torch.float32, device,
+                                                               2 if fp4 else 1),
                      pool_from_host(h.swa, torch.float32, device),
                      pool_from_host(h.state, in_dt, device),
                      s.top_k if s.kind == "c4a" else 0)

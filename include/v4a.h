@@ -67,6 +67,15 @@ typedef struct CUstream_st* v4a_stream_t; /* a cudaStream_t; NULL = legacy defau
 #define V4A_FP32 0                /* fp32 inputs, fp32 caches, fp32 output */
 #define V4A_BF16_FP8 1            /* bf16 inputs, fp8 e4m3 caches + fp32 row scale, bf16 output */
 
+/* indexer-cache formats (v4a_layer_cfg.idx_format) */
+#define V4A_IDX_DEFAULT 0         /* the layer's cache type: fp8 e4m3 (BF16_FP8) or fp32 (FP32) */
+#define V4A_IDX_FP4 1             /* e2m1 codes, two per byte (element 2i in the low nibble), and
+                                     one fp32 scale per row: scale = max|y| / 6 (1 for a zero row),
+                                     code = round-to-nearest-even of y / scale saturated to +-6
+                                     ([notes] 四大核心技术 and [blog] KV 快取記憶體管理: the fp4
+                                     indexer cache; the block of one scale is the whole row).
+                                     BF16_FP8 layers with d_I = 128 only. */
+
 typedef struct v4a_layer_cfg {
   int32_t kind;          /* V4A_C4A or V4A_C128A */
   int32_t dtype;         /* V4A_FP32 or V4A_BF16_FP8 */
@@ -82,6 +91,7 @@ typedef struct v4a_layer_cfg {
   float rope_base;       /* theta_i = rope_base^(-2i/d_r) */
   float rms_eps;         /* RMSNorm epsilon of compressed entries */
   float softmax_scale;   /* logit scale, usually 1/sqrt(D) */
+  int32_t idx_format;    /* V4A_IDX_DEFAULT or V4A_IDX_FP4 (c4a indexer cache) */
 } v4a_layer_cfg;
 
 typedef struct v4a_cache {
@@ -92,7 +102,7 @@ typedef struct v4a_cache {
   int32_t max_blocks;          /* columns of block_table */
   int32_t rows_per_block;      /* 64 (c4a entries), 2 (c128a entries), 256 (token caches) */
   int64_t n_pages;             /* pages in the pool (bounds check of block-table values) */
-  int32_t row_width;           /* elements per row */
+  int32_t row_width;           /* elements per row (an fp4 row holds two per byte) */
   int32_t reserved;            /* must be 0 */
 } v4a_cache;
 

@@ -110,6 +110,36 @@ def check_fp8_rows(gpu_data, gpu_scale, ref_pool, slots):
     return n_close
 
 
+def check_fp4_rows(gpu_data, gpu_scale, ref_pool, slots):
+    """Compare GPU-written packed fp4 rows with the oracle's at the given pool rows: scales
+    within 1e-6 relative; codes equal except the other grid neighbour of y/scale where it
+    lies within 1e-3 of a rounding midpoint (in grid-step units)."""
+    n_close = 0
+    for s in slots:
+        y = ref_pool.raw[s]
+        so = float(ref_pool.scale[s])
+        sg = float(gpu_scale[s])
+        assert abs(sg - so) <= 1e-6 * so, (s, sg, so)
+        cg, co = O.unpack_e2m1(gpu_data[s]), O.unpack_e2m1(ref_pool.data[s])
+        bad = np.nonzero(cg != co)[0]
+        if len(bad) == 0:
+            continue
+        v = y[bad] / so
+        dg, do = O.e2m1_decode(cg[bad]), O.e2m1_decode(co[bad])
+        same_value = dg == do                           # +0 / -0
+        grid = O.e2m1_values()
+        a = np.minimum(np.abs(v), 6.0)
+        hi = np.minimum(np.searchsorted(grid, a, side="left"), 7)
+        lo = np.maximum(hi - 1, 0)
+        sgn = np.where(np.signbit(v), -1.0, 1.0)
+        neighbour = (dg == sgn * grid[lo]) | (dg == sgn * grid[hi])
+        ok = same_value | (neighbour & (O.e2m1_midpoint_distance(v) < 1e-3))
+        assert ok.all(), "row %d: codes %s vs %s at y/scale %s" % (s, cg[bad][~ok], co[bad][~ok],
+                                                                   v[~ok])
+        n_close += int((~same_value).sum())
+    return n_close
+
+
 def check_out(got, ref, fp8):
     d = np.abs(got.astype(np.float64) - ref)
     if fp8:

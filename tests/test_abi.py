@@ -107,6 +107,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert qn(ctypes.byref(cfg), 0, 0, *n13, 1, 1 << 20, 4096, (1 << 20) + 1024, None,
               None) == v4a.ERR_ARG
     assert qn(ctypes.byref(cfg), 0, 0, *n13, 0, None, None, None, None, None) == v4a.OK
+    # fp4 indexer cache: bf16/fp8 c4a layers with d_I = 128 only; unknown formats refused
+    for bad in (_cfg(dtype=v4a.FP32, idx_format=v4a.IDX_FP4), _cfg(idx_format=v4a.IDX_FP4, idx_dim=64),
+                _cfg(idx_format=7)):
+        assert lib.v4a_index_topk(ctypes.byref(bad), 1, 8, 8, 0, 16, 16, ctypes.byref(c), 1, 16,
+                                  None, 0, None, None) == v4a.ERR_UNSUPPORTED
     # the indexer exists only for c4a layers
     assert lib.v4a_index_topk(ctypes.byref(_cfg(kind=v4a.C128A, window=128, stride=128)), 1, 8,
                               8, 0, 16, 16, ctypes.byref(c), 1, 16, None, 0, None,

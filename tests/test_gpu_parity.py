@@ -8,8 +8,8 @@ import torch
 
 import compressed_sparse_long_gb300 as v4a
 import workloads as wl
-from helpers import (DevInputs, T, check_fp8_rows, check_out, check_topk, device_layer,
-                     oracle_insert, oracle_pools)
+from helpers import (DevInputs, T, check_fp4_rows, check_fp8_rows, check_out, check_topk,
+                     device_layer, oracle_insert, oracle_pools)
 from oracle import v4a_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -240,6 +240,49 @@ def test_index_topk_fp8_decode():
     ref, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, 512)
     same = check_topk(topk.cpu().numpy(), ref, scores, 512)
     assert len(same) >= 6
+
+
+def test_compress_insert_fp4_indexer_rows():
+    """fp4 indexer cache: the insert writes each completed indexer entry as packed e2m1
+    codes + amax/6 row scale equal to the oracle's (codes may differ by one grid step only
+    at a rounding tie); attention and window rows are the fp8 rows of the default layer."""
+    spec = wl.LayerSpec("c4a", True, idx_fp4=True)
+    rng = np.random.default_rng(41)
+    ctx, new = [1000, 37, 127, 4096], [300, 1, 129, 257]
+    h = wl.make_layer(rng, spec, ctx, new, prefill_cache=True)
+    h.bias, h.gamma, h.ibias = wl.layer_params(rng, spec)
+    b = wl.make_batch(rng, spec, ctx, new)
+    w = wl.Workload("ragged fp4", [h], b, wl.make_queries(rng, spec, np.arange(4), np.array(ctx),
+                                                         False))
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    assert lay.idx.data.shape[1] == 64 and lay.idx.c.row_width == 128
+    lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    pools = oracle_pools(h)
+    writes = oracle_insert(w, h, pools)
+    slots = sorted({sl for (k, _, _, sl) in writes if k == "idx" and sl >= 0})
+    assert len(slots) > 100
+    g_data, g_scale = _gpu_rows(lay.idx)
+    check_fp4_rows(g_data.astype(np.uint8), g_scale, pools.idx, slots)
+    _compare_written(lay, pools, [wr for wr in writes if wr[0] != "idx"], fp8=True)
+
+
+@pytest.mark.parametrize("B,L", [(8, 8192), (32, 32768)])
+def test_index_topk_fp4_decode(B, L):
+    """Indexer over an fp4 cache (packed pages expanded on chip to exact e4m3 operands):
+    the top-k lists equal the oracle's over the same dequantised keys except near-ties."""
+    w = wl.c4a_decode(seed=43, B=B, L=L, idx_fp4=True)
+    h = w.layers[0]
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    topk = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    q = w.queries
+    sample = np.arange(B) if B <= 8 else np.array([0, 5, 17, 31])
+    pools = oracle_pools(h)
+    ref, scores = O.index_topk(h.spec, pools, q.seq[sample], q.pos[sample], q.q_idx[sample],
+                               q.w[sample], 512)
+    same = check_topk(topk.cpu().numpy()[sample], ref, scores, 512)
+    assert len(same) >= len(sample) - 1
 
 
 @pytest.mark.parametrize("n_q,k", [(16, 512), (5, 64), (3, 2048)])
