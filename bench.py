@@ -39,10 +39,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # ------------------------------------------------------------------ algorithmic work
 def decode_bytes_per_query(n_vis: int, k: int, swa: int, D: int = 512, H: int = 64,
-                           H_I: int = 64, d_I: int = 128) -> dict:
-    """Bytes one decode query must move at least (fp8 rows + fp32 row scale)."""
+                           H_I: int = 64, d_I: int = 128, idx_fp4: bool = False) -> dict:
+    """Bytes one decode query must move at least (fp8 rows + fp32 row scale; the indexer
+    rows packed fp4 + fp32 row scale with idx_fp4)."""
     parts = {
-        "indexer_keys": n_vis * (d_I + 4),
+        "indexer_keys": n_vis * ((d_I // 2 if idx_fp4 else d_I) + 4),
         "selected_rows": k * (D + 4),
         "window_rows": swa * (D + 4),
         "q_and_out": 2 * H * D * 2,
@@ -55,8 +56,9 @@ def decode_bytes_per_query(n_vis: int, k: int, swa: int, D: int = 512, H: int = 
     return parts
 
 
-def index_bytes_per_query(n_vis: int, k: int, H_I: int = 64, d_I: int = 128) -> int:
-    return n_vis * (d_I + 4) + H_I * d_I * 2 + H_I * 4 + k * 4
+def index_bytes_per_query(n_vis: int, k: int, H_I: int = 64, d_I: int = 128,
+                          idx_fp4: bool = False) -> int:
+    return n_vis * ((d_I // 2 if idx_fp4 else d_I) + 4) + H_I * d_I * 2 + H_I * 4 + k * 4
 
 
 def attn_bytes_per_query(k: int, swa: int, H: int = 64, D: int = 512) -> int:
@@ -261,7 +263,9 @@ class DecodeReplica:
 
     def touched_bytes(self):
         n_vis = (self.max_pos - 8) // 4 + 1
-        return len(self.q) * decode_bytes_per_query(n_vis, self.lay.top_k, 128)["total"]
+        fp4 = self.lay.cfg.idx_format == 1
+        return len(self.q) * decode_bytes_per_query(n_vis, self.lay.top_k, 128,
+                                                    idx_fp4=fp4)["total"]
 
 
 def gpu_main(args, rank: int, world: int, local_rank: int):
@@ -387,6 +391,7 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     # per-call timing over the same rotating replicas; the roofline line is the slower of
     # the two large calls (both HBM-bound by arithmetic intensity)
     calls = _per_call_times(reps, args.steps, stream)
+    fp4 = None if args.skip_fp4 else _fp4_indexer(w, reps, args, dev, world, hbm_peak, peak_src)
     n_vis = (L - 8) // 4 + 1
     roof = {}
     for call, kern, nbytes in (
@@ -403,6 +408,8 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     err_bits = 0
     for r in reps:
         err_bits |= int(r.err.item())
+    if fp4 is not None:
+        err_bits |= fp4["device_error_bits"]
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -423,6 +430,7 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         "ms_per_step_one_graph_per_step": ms_one,
         "per_call_ms": calls,
         "side_stream": overlap,
+        "fp4_indexer": fp4,
         "roofline": roof[dominant],
         "roofline_other": roof["attention" if dominant == "index_topk" else "index_topk"],
         "device_error_bits": err_bits,
@@ -461,7 +469,57 @@ def _max_over_ranks(ms, world, dev):
     return float(t.item())
 
 
-def _per_call_times(reps, steps, stream):
+def _fp4_indexer(w8, reps8, args, dev, world, hbm_peak, peak_src):
+    """The same decode step with the indexer cache in fp4 (packed e2m1 + row scale): the
+    step timed like the headline (one graph holds one step of each replica) and the
+    index_topk call alone, with its roofline over the fp4 bytes."""
+    import torch
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+    w = wl.c4a_decode(seed=rank_seed(int(os.environ.get("RANK", "0"))), B=B, L=L, idx_fp4=True)
+    base = Layer.from_host(w.layers[0], dev)
+    n_rep = len(reps8)
+    side = reps8[0].side is not None
+    reps = [DecodeReplica(base, w, dev, clone=False, side=side)] + \
+        [DecodeReplica(base, w, dev, clone=True, side=side) for _ in range(n_rep - 1)]
+    for r in reps:
+        r.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in reps:
+            r.step()
+    stream = torch.cuda.current_stream()
+    k = max(1, args.steps // n_rep)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = _max_over_ranks(e0.elapsed_time(e1), world, dev) / (k * n_rep)
+    ms_idx = _per_call_times(reps, args.steps, stream, only=("index_topk",))["index_topk"]
+    err = 0
+    for r in reps:
+        err |= int(r.err.item())
+    n_vis = (L - 8) // 4 + 1
+    nb = B * index_bytes_per_query(n_vis, 512, idx_fp4=True)
+    gbs = nb / (ms_idx / 1e3) / 1e9
+    del g
+    return {"value": whole_job_rate(B * k * n_rep, world, ms_step * k * n_rep), "unit": UNIT,
+            "ms_per_step": ms_step, "steps": k * n_rep, "device_error_bits": err,
+            "index_topk_ms": ms_idx,
+            "index_roofline": {"kernel": "v4a_index_topk over the fp4 cache", "bound": "hbm",
+                               "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                               "frac": gbs / hbm_peak, "peak_source": peak_src,
+                               "algorithmic_bytes_per_launch": nb},
+            "bytes_per_step": reps[0].touched_bytes()}
+
+
+def _per_call_times(reps, steps, stream, only=None):
     """Device time of each library call: one CUDA graph per (call, replica), replayed
     round-robin over the replicas, timed with events on the launching stream."""
     import torch
@@ -481,6 +539,8 @@ def _per_call_times(reps, steps, stream):
     }
     out = {}
     for name, fn in calls.items():
+        if only is not None and name not in only:
+            continue
         graphs = []
         for r in reps:
             g = torch.cuda.CUDAGraph()
@@ -669,6 +729,7 @@ def main():
     ap.add_argument("--load-s", type=float, default=1.5, dest="load_s")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, dest="cpu_budget_s")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-fp4", action="store_true", dest="skip_fp4")
     ap.add_argument("--serial-step", action="store_true", dest="serial_step",
                     help="time the serial step as the headline (default: the decode insert on a "
                          "side stream beside the indexer; the other variant is reported beside it)")

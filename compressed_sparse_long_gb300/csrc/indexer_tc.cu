@@ -75,8 +75,11 @@ struct StageGeo {
 template <int NQ, bool kFp4>
 struct Layout {
   static constexpr int N = NQ * 2 * kHI;    // hi and lo rows of each query
-  // fp8: even, tiles alternate producer pairs; fp4: the stage holds the packed pages too
-  static constexpr int kStages = kFp4 ? 6 : (NQ == 1 ? 10 : 8);
+  // fp8: even, tiles alternate producer pairs; fp4: the stage holds the packed pages too.
+  // Shallow rings measured faster for the decode grid (a CTA streams only ~14 tiles and a
+  // deep ring floods DRAM with requests that delay its first tiles): fp8 with one query
+  // per group 4 stages (49.6 us per decode step against 51.0 with 10), fp4 6.
+  static constexpr int kStages = kFp4 ? 6 : (NQ == 1 ? 4 : 8);
   static constexpr int kBBytes = N * kDI;   // fp8 B operand of one group
   static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators (512 columns)
   static constexpr int kTmemCols = kAcc * N;
