@@ -313,6 +313,21 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
     tc::tmem_alloc(tmem_slot, Lay::kTmemCols);
     tc::tmem_relinquish();
   }
+  // The query operands are read first by the preparation warps, right after the partition
+  // below: when they are small, every CTA brings its slice of them (and of the positions
+  // and sequence ids the partition reads) into L2 now, one 128-byte line per thread.
+  {
+    const int64_t qb = (int64_t)p.n_q * kHI * kDI * 2, wb = (int64_t)p.n_q * kHI * 4;
+    if (qb + wb <= ((int64_t)4 << 20)) {
+      const int64_t lines_q = (qb + 127) >> 7, lines_w = (wb + 127) >> 7;
+      const int64_t lines = lines_q + lines_w;
+      for (int64_t l = (int64_t)blockIdx.x * kThreads + tid; l < lines; l += (int64_t)gridDim.x * kThreads) {
+        const char* a = l < lines_q ? reinterpret_cast<const char*>(p.q_idx) + (l << 7)
+                                    : reinterpret_cast<const char*>(p.w) + ((l - lines_q) << 7);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      }
+    }
+  }
 
   // ---- this CTA's slice of the units (one block scan when the groups fit the block)
   __shared__ int s_g0, s_off;
