@@ -11,6 +11,8 @@
 // window tokens max(0, p-swa+1) .. p. Split s of a query handles keys
 // [s*keys_per_split, (s+1)*keys_per_split); splits > 1 write (m, l, o) partials that
 // attn_merge combines.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -255,7 +257,14 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
     m_l = p.part_ml[(row0 + (int64_t)lane * H) * 2];
     l_l = p.part_ml[(row0 + (int64_t)lane * H) * 2 + 1];
   }
-  float2 v[4][kPairs];
+  // bf16 partials stay packed (one 32-bit word per pair) until they are used, which halves
+  // the registers and lets more warps keep loads in flight
+  using VT = typename std::conditional<kNorm, uint32_t, float2>::type;
+  VT v[4][kPairs];
+  auto pair_of = [](const VT& x) -> float2 {
+    if constexpr (kNorm) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+    else return x;
+  };
   auto load4 = [&](int s0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -263,10 +272,7 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
       if constexpr (kNorm) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(p.part_o) + ((row0 + (int64_t)s * H) * D >> 1);
 #pragma unroll
-        for (int i = 0; i < kPairs; ++i) {
-          const uint32_t w = s < p.n_split ? src[lane + 32 * i] : 0u;
-          v[u][i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-        }
+        for (int i = 0; i < kPairs; ++i) v[u][i] = s < p.n_split ? src[lane + 32 * i] : 0u;
       } else {
         const float* src = p.part_o + (row0 + (int64_t)s * H) * D;
 #pragma unroll
@@ -309,8 +315,9 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
       if (wg[u] == 0.f) continue;   // a range without keys wrote no partial: never multiply it
 #pragma unroll
       for (int i = 0; i < kPairs; ++i) {
-        a[i] = fmaf(v[u][i].x, wg[u], a[i]);
-        b[i] = fmaf(v[u][i].y, wg[u], b[i]);
+        const float2 f = pair_of(v[u][i]);
+        a[i] = fmaf(f.x, wg[u], a[i]);
+        b[i] = fmaf(f.y, wg[u], b[i]);
       }
     }
   }
