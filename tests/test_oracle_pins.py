@@ -326,6 +326,34 @@ def test_visibility_brute_force(S, W, off):
         assert O.visible_entries(S, W, off, p) == want
 
 
+def test_decode_insert_is_invisible_to_its_own_queries():
+    """R15 (the side stream's condition), by brute force with the oracle: in a decode step
+    the only new token sits at the query's own position, so the entry it completes covers
+    that position and no query of the step can see it; the indexer's scores and top-k are
+    the same computed before or after the insert. In a prefill chunk later queries do see
+    entries completed by earlier tokens of the same call, so there they differ."""
+    for L in (1027, 1031):                        # the token completes an entry at 1031 (4j+7)
+        w = wl.c4a_decode(seed=61, B=3, L=L, top_k=64)
+        h, q = w.layers[0], w.queries
+        before = _fresh_pools(w)
+        t0, s0 = O.index_topk(h.spec, before, q.seq, q.pos, q.q_idx, q.w, 64)
+        after = _fresh_pools(w)
+        writes = _run_compress(w, after)
+        if L == 1031:
+            assert any(k == "idx" for (k, _, _, _) in writes)   # an entry was completed
+        t1, s1 = O.index_topk(h.spec, after, q.seq, q.pos, q.q_idx, q.w, 64)
+        assert np.array_equal(t0, t1)
+        assert all(np.array_equal(a, b) for a, b in zip(s0, s1))
+    w = wl.c4a_prefill(seed=62, cached=256, chunk=64, top_k=64)
+    h, q = w.layers[0], w.queries
+    before = _fresh_pools(w)
+    _, s0 = O.index_topk(h.spec, before, q.seq[-4:], q.pos[-4:], q.q_idx[-4:], q.w[-4:], 64)
+    after = _fresh_pools(w)
+    _run_compress(w, after)
+    _, s1 = O.index_topk(h.spec, after, q.seq[-4:], q.pos[-4:], q.q_idx[-4:], q.w[-4:], 64)
+    assert any(not np.array_equal(a, b) for a, b in zip(s0, s1))
+
+
 def test_entry_counts_at_one_million():
     n4 = O.visible_entries(4, 8, 0, 1 << 20)
     n128 = O.visible_entries(128, 128, 0, 1 << 20)
