@@ -228,16 +228,16 @@ __device__ __forceinline__ float key_value(uint32_t u) {   // inverse of order_k
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// Register-resident variant for rows of up to ITEMS * THREADS entries: entry i = r*THREADS
-// + tid is held by thread tid as u[r] (coalesced loads).
+// Register-resident variant for rows of up to ITEMS * THREADS entries: thread tid holds
+// entries tid*ITEMS .. tid*ITEMS + ITEMS-1 as u[0..ITEMS-1] (16-byte loads).
 // Threshold: 1024 buckets linear in the score between the row's min and max (a monotone
-// map, so every entry of a higher bucket scores strictly higher); the bucket where the
-// count from the top reaches k holds the k-th score, and the exact k-th key is found among
-// that bucket's entries alone (a handful for spread-out scores). When the bucket is large
-// (many equal or clustered scores) or the range is not finite, four 8-bit radix passes find
-// it instead (one atomic per distinct digit per warp, two histograms, two barriers a pass).
-// The compaction ranks entries in index order, (round, warp, lane), from one scan of packed
-// (above, equal) ballot counts.
+// map, so every entry of a higher bucket scores strictly higher); a block-wide scan with one
+// bucket per thread finds the bucket where the count from the top reaches k, which holds
+// the k-th score, and the exact k-th key is found among that bucket's entries alone (a
+// handful for spread-out scores). When the bucket is large (many equal or clustered
+// scores) or the range is not finite, four 8-bit radix passes find it instead (one atomic
+// per distinct digit per warp, two histograms, two barriers a pass). The output places
+// entries in index order from one block scan of each thread's packed (above, equal) counts.
 template <int ITEMS, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_constant__ IndexParams p) {
   pdl_trigger();
