@@ -31,8 +31,13 @@
 //               odd tiles: tcgen05.ld, hi + lo, ReLU, weighted head sum, row scale, store
 //   warps 10-11 query preparation: the hi/lo B operand and w/s of each query group, double
 //               buffered across groups
+// fp4 indexer cache (packed e2m1 rows, one fp32 scale a row): warps 0 and 12 bulk-copy a
+// tile's two 4 KB packed pages into the stage's packed area, and warps 13-15 (added to the
+// block) take turns expanding them into the same swizzled e4m3 operand (every e2m1 value
+// is an e4m3 value, so the product is unchanged); the product waits for the expansion.
 // Work: units = (query group, sequence sub-pass, tile); each CTA takes a contiguous slice
 // of the units of all groups (found with a block scan), so long and short rows balance.
+// At kernel start each CTA prefetches its slice of the query operands into L2.
 // Every wait is bounded (~1 s): on expiry the CTA sets V4A_DEV_TIMEOUT, drains its copies
 // and MMAs, frees its TMEM and returns.
 #include <cstring>
