@@ -509,11 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         const bool even = (lane & 1) == 0;
         for (int b = 0; b < 4; ++b) {
           const int d = b * 128 + row;
+          float ob[2][32];                          // both halves of the block, one wait
+          tc::tmem_ld32(tmem + lane_base + kOCol + b * 64, ob[0]);
+          tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + 32, ob[1]);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            float o[32];
-            tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + half * 32, o);
-            tc::tmem_wait_ld();
+            const float (&o)[32] = ob[half];
 #pragma unroll
             for (int h = 0; h < 32; h += 2) {
               const int hh = half * 32 + h;
