@@ -285,6 +285,25 @@ def test_index_topk_fp4_decode(B, L):
     assert len(same) >= len(sample) - 1
 
 
+def test_index_topk_fp4_prefill_two_queries_per_group():
+    """A prefill chunk of 1024 queries over an fp4 indexer cache runs the fp4 kernel with two
+    queries per group (N = 256 operand rows); sampled rows match the oracle's top-k."""
+    w = wl.c4a_prefill(seed=44, cached=8192, chunk=1024, idx_fp4=True)
+    h = w.layers[0]
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_, dev_err=err)
+    topk = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    pools = oracle_pools(h)
+    oracle_insert(w, h, pools)
+    q = w.queries
+    sample = np.array([0, 1, 511, 512, 1022, 1023])
+    ref, scores = O.index_topk(h.spec, pools, q.seq[sample], q.pos[sample], q.q_idx[sample],
+                               q.w[sample], 512)
+    same = check_topk(topk.cpu().numpy()[sample], ref, scores, 512)
+    assert len(same) >= len(sample) - 1
+
+
 @pytest.mark.parametrize("n_q,k", [(16, 512), (5, 64), (3, 2048)])
 def test_index_topk_prefill_positions(n_q, k):
     """Queries at many positions of one sequence (ragged visibility, rows shorter and
@@ -440,6 +459,27 @@ def test_attention_q8_output(B, L, width):
     assert (np.abs(deq - deq_o) <= step_o * 1.05 + 3e-2).all()
     # fp8 rounding itself (half a step, ~3% of a value) is in both: compare the quantised
     # outputs with the bf16 output's mean tolerance
+    assert np.abs(deq - deq_o).mean() <= 3e-3
+
+
+def test_attention_q8_c128a_dense():
+    """The fp8 output epilogue on a dense c128a layer (every visible entry + window): the
+    quantised rows match the oracle's within one e4m3 step plus the attention tolerance."""
+    w = wl.c128a_decode(seed=24, B=2, L=32768)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    codes, scale = lay.attention_q8(x.q_seq, x.q_pos, x.max_pos, x.q, None, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    codes, scale = codes.cpu().numpy(), scale.cpu().numpy().astype(np.float64)
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, None)
+    codes_o, scale_o = O.quantize(ref)
+    assert np.allclose(scale, scale_o, rtol=3e-2, atol=1e-6)
+    deq = O.e4m3_decode(codes) * scale[..., None]
+    deq_o = O.e4m3_decode(codes_o) * scale_o[..., None]
+    step_o = _e4m3_step(ref / scale_o[..., None]) * scale_o[..., None]
+    assert (np.abs(deq - deq_o) <= step_o * 1.05 + 3e-2).all()
     assert np.abs(deq - deq_o).mean() <= 3e-3
 
 

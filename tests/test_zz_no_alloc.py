@@ -57,6 +57,12 @@ def test_noalloc_matches_workspace_call_twice():
     check_topk(got2, o_top, scores, 512)
 
 
+def test_noalloc_with_the_fp4_cache():
+    w = wl.c4a_decode(seed=34, B=8, L=8192, idx_fp4=True)
+    got, ref = _both(w)
+    assert np.array_equal(got, ref)
+
+
 def test_noalloc_refuses_requests_beyond_the_scratch():
     cap = v4a.v4a_index_topk_noalloc_capacity()
     assert cap == (8 << 20) // 4
