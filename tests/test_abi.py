@@ -140,3 +140,23 @@ def test_workspace_sizes_are_monotone():
     b = v4a.v4a_index_topk_workspace_size(cfg, 8, 8192)
     assert 0 < a < b
     assert v4a.v4a_attn_workspace_size(cfg, 8192, 131072, 512, 1) >= 256
+
+
+def test_attention_split_plan_on_a_152_sm_gpu():
+    """Host planning of decode attention (no device here: the planner assumes 152 SMs). A
+    query's 512 selected rows + 128 window rows are 5 tiles of 128 keys; a plan costs
+    waves x (tiles per range + 1) with one CTA per SM, the smallest split of least cost wins,
+    and a split needs the merge kernel."""
+    c4a = _cfg()
+    assert v4a.v4a_attn_plan(c4a, 32, 32768, 512) == (3, 2)    # 5 ranges = 160 CTAs: 2 waves
+    assert v4a.v4a_attn_plan(c4a, 64, 4096, 512) == (2, 2)     # 3 ranges = 192 CTAs: 2 waves
+    assert v4a.v4a_attn_plan(c4a, 16, 4096, 512) == (5, 2)     # 80 CTAs: one tile each
+    assert v4a.v4a_attn_plan(c4a, 160, 4096, 512) == (1, 1)    # more queries than SMs
+    assert v4a.v4a_attn_plan(c4a, 0, 4096, 512) == (1, 0)      # nothing to launch
+    assert v4a.v4a_attn_plan(c4a, 32, 32768, 512, True) == (1, 1)   # prefill never splits
+    c128a = _cfg(kind=v4a.C128A, window=128, stride=128)
+    # dense: 2^20 / 128 = 8192 compressed rows + 128 window rows = 65 tiles; with one wave
+    # (up to 19 ranges for 8 queries) the cost is ceil(65 / r) + 1, least (5) first at r = 17:
+    # 4 tiles (512 keys) a range, 17 ranges
+    assert v4a.v4a_attn_plan(c128a, 8, 1 << 20, 0) == (17, 2)
+    assert v4a.v4a_attn_plan(c128a, 8, 1 << 20, 0, True) == (1, 1)
