@@ -1,26 +1,34 @@
-// Shared-K=V attention on tcgen05 tensor cores (bf16 queries, fp8 e4m3 keys), with the
-// sliding window and inverse RoPE ([notes] "DeepSeek V4 in vLLM 技术博客详尽笔记", Inverse
-// RoPE 的数学原理 and 共享 Key-Value 向量; [blog] 短滑動窗口).
+// Shared-K=V attention on tcgen05 tensor cores with fp8 e4m3 operands, with the sliding
+// window and inverse RoPE ([notes] "DeepSeek V4 in vLLM 技术博客详尽笔记", Inverse RoPE 的数学原理
+// and 共享 Key-Value 向量; [blog] 短滑動窗口).
 //
 // Work item: one query (prefill) or one key range of one query (decode split). Keys come
 // in tiles of 128 rows gathered from the paged pools (top-k entries or all visible
-// entries, then the window tokens). Per tile:
-//   S^T = K Q~^T      M = 128 keys, N = 64 heads, K = 512 dims   (32 MMAs, TMEM cols 0..63)
-//   softmax over keys per head: column max with redux.sync.max.f32 across the warp and a
-//     4-warp exchange, column sums with a butterfly reduce-scatter; the running max is
-//     raised only when it grows by more than 2^8 (then the O^T accumulator is rescaled)
-//   O^T += V^T P'^T   M = 128 dims x 4 blocks, N = 64 heads, K = 128 keys (32 MMAs,
-//                     TMEM cols 64..319)
-// K = V: the same shared-memory key tile (fp8 codes converted exactly to bf16, 128-byte
-// swizzle) is read K-major by the first product and MN-major by the second. The fp8 row
-// scale is applied to the logits after S^T and folded into P' = p * scale before the
-// second product, so keys stay exact codes. Q~ = RoPE(q, p) * softmax_scale * log2(e) in
-// bf16; logits are in log2 units.
+// entries, then the window tokens). The key tile is the pool's own e4m3 codes, copied
+// row by row into a 128-byte-swizzled buffer (no conversion); per tile:
+//   S^T = K Q~^T      M = 128 keys, N = 128 (64 heads x {hi, lo}), K = 512 dims
+//                     (16 MMAs kind::f8f6f4, TMEM cols 0..127)
+//   softmax over keys per head: logit = (hi + lo) / s_h * row scale; column max with
+//     redux.sync.max.f32 and a 4-warp exchange, column sums with a butterfly
+//     reduce-scatter; the running max is raised only when it grows by more than 2^2
+//     (then the O^T accumulator is rescaled)
+//   O^T += V^T P'^T   M = 128 dims x 4 blocks, N = 64 heads, K = 128 keys, P' = hi + lo
+//                     (32 MMAs, TMEM cols 128..383)
+// K = V: the key tile is read K-major by the first product and MN-major by the second.
+// Two key buffers: tile t+1 is copied while tile t is in use, and S^T of tile t+1 runs
+// during the softmax of tile t (the softmax frees the S^T columns as soon as it has read
+// them).
+// Exact-as-possible e4m3 operands: Q~ = RoPE(q, p) * softmax_scale * log2(e) (logits in
+// log2 units) is scaled per head by s_h = 2^(7 - exponent(max |Q~_h|)) and split into
+// hi = e4m3(Q~ s_h) and lo = e4m3(Q~ s_h - hi), about 8 significant bits like bf16; P' =
+// p * row scale * 2^A (A a per-range power of two that keeps P' below 2^8) is split the
+// same way, and 2^-A is folded into the final 1/l. The row scales stay out of the codes.
 //
 // Warpgroups (setmaxnreg splits the 512 x 128 launch registers as 152 / 128 / 128 / 104):
-// 0 = softmax and epilogue (warp w reads TMEM lanes 32w..32w+31), 1-2 = eight
-// gather/convert warps that also build Q~, 3 = warp 12 allocates TMEM, walks the items
-// converged and issues the MMAs from lane 0 (warps 13-15 idle).
+// 0 = softmax and epilogue (warp w reads TMEM lanes 32w..32w+31), 1-2 = eight copy warps
+// that also build Q~ (warps 4-7 fill key buffer 0 with the even tiles, warps 8-11 buffer 1
+// with the odd tiles), 3 = warp 12 allocates TMEM, walks the items converged and issues
+// the MMAs from lane 0 (warps 13-15 idle).
 // Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
 // Decode split: each key range's CTA writes its partial as o / l in bf16 plus (m, l) in
 // fp32; the merge kernel combines the ranges and applies R^-1.
@@ -32,20 +40,24 @@ namespace v4a {
 namespace {
 
 constexpr int kH = 64, kD = 512, kTile = 128;
-constexpr int kThreads = 512;                 // 4 warpgroups
-constexpr int kKBytes = kTile * kD * 2;        // 128 KB key tile, 8 K-blocks of 16 KB
-constexpr int kQBytes = kH * kD * 2;           // 64 KB Q~, 8 K-blocks of 8 KB
-constexpr int kPBytes = kTile * kH * 2;        // 16 KB P'^T
-constexpr int kOffK = 0, kOffQ = kKBytes, kOffP = kOffQ + kQBytes;
-constexpr int kOffF = kOffP + kPBytes;         // floats: l_fin[2][64] red_max[2][256] red_sum[2][256] sscale[2][128]
-constexpr int kOffBar = kOffF + (128 + 512 + 512 + 256) * 4;
-constexpr int kNBar = 4 + 4 + 13;
+constexpr int kThreads = 512;                  // 4 warpgroups
+constexpr int kKBytes = kTile * kD;            // 64 KB e4m3 key tile, 4 K-blocks of 16 KB
+constexpr int kQBytes = 2 * kH * kD;           // 64 KB Q~ hi (rows 0-63) and lo (64-127), 4 K-blocks
+constexpr int kPBytes = kH * kTile;            // 8 KB per P' term, [64 heads][128 keys]
+constexpr int kOffK = 0, kOffQ = 2 * kKBytes, kOffP = kOffQ + kQBytes;
+// floats: l_fin[2][64] red_max[2][256] red_sum[2][256] sscale[2][128] qinv[3][64] red_sc[2][4]
+constexpr int kOffF = kOffP + 2 * kPBytes;
+constexpr int kNFloats = 128 + 512 + 512 + 256 + 192 + 8;
+constexpr int kOffBar = kOffF + kNFloats * 4;
+constexpr int kNBar = 14;
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBytes % 1024 == 0, "swizzled operands need 1 KB alignment");
+static_assert(kOffBar % 8 == 0 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 0, kOCol = 64;
+constexpr uint32_t kSCol = 0, kOCol = 128;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr float kRescaleThreshold = 2.0f;      // log2 units: p <= 4 between rescales
 
 struct Item {
   int qi, split, seq;
@@ -177,31 +189,75 @@ __device__ __forceinline__ float2 reduce_scatter_sum64(const float (&v)[64]) {
   return make_float2(e[0], e[1]);
 }
 
+// tcgen05.mma kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format
+// code 0), shape M x N; A read MN-major when asked (8-bit operands may be either major).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// 2^a for an integer a in [-126, 127].
+__device__ __forceinline__ float pow2i(int a) { return __uint_as_float((uint32_t)(127 + a) << 23); }
+
+// Binary exponent of a positive normal float.
+__device__ __forceinline__ int exponent_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
+
+// Two values -> e4m3 hi codes (byte 0: a0, byte 1: a1) and the e4m3 codes of the
+// remainders a - hi (round to nearest even, saturating).
+__device__ __forceinline__ void split_e4m3x2(float a0, float a1, uint32_t& hi2, uint32_t& lo2) {
+  const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+  const __nv_fp8x2_storage_t l =
+      __nv_cvt_float2_to_fp8x2(make_float2(a0 - hf.x, a1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+  hi2 = (uint32_t)h;
+  lo2 = (uint32_t)l;
+}
+
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* kbuf = sm + kOffK;
+  uint8_t* kbuf = sm + kOffK;                             // [2][64 KB]
   uint8_t* qbuf = sm + kOffQ;
-  uint8_t* pbuf = sm + kOffP;
-  float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] 1 / l by item parity
+  uint8_t* pbuf = sm + kOffP;                             // hi, then lo
+  float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] 2^-A / l by item parity
   float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
   float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
-  float* sscale = red_sum + 512;                          // [2][128] row scales by tile parity
+  float* sscale = red_sum + 512;                          // [2][128] row scales by key buffer
+  float* qinv = sscale + 256;                             // [3][64] 1 / s_h by item % 3
+  float* red_sc = qinv + 192;                             // [2][4] tile max of the row scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* kfull = bars;
-  uint64_t* kempty = bars + 4;
-  uint64_t* qfull = bars + 8;
-  uint64_t* qempty = bars + 9;
-  uint64_t* sfull = bars + 10;
-  uint64_t* pfull = bars + 11;
-  uint64_t* pvdone = bars + 12;
-  uint64_t* ofull = bars + 13;
-  uint64_t* oempty = bars + 14;
-  uint64_t* redb = bars + 15;
-  uint64_t* done = bars + 16;
-  uint64_t* scfull = bars + 17;
+  uint64_t* kfull = bars;                                 // [2] by key buffer
+  uint64_t* kempty = bars + 2;                            // [2]
+  uint64_t* qfull = bars + 4;
+  uint64_t* qempty = bars + 5;
+  uint64_t* sfull = bars + 6;
+  uint64_t* sempty = bars + 7;
+  uint64_t* pfull = bars + 8;
+  uint64_t* pvdone = bars + 9;
+  uint64_t* ofull = bars + 10;
+  uint64_t* oempty = bars + 11;
+  uint64_t* redb = bars + 12;
+  uint64_t* done = bars + 13;
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
@@ -213,20 +269,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   pdl_trigger();
 
   if (tid == 0) {
-    for (int b = 0; b < 4; ++b) {
-      tc::mbar_init(kfull + b, 8);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(kfull + b, 4);
       tc::mbar_init(kempty + b, 1);
     }
     tc::mbar_init(qfull, 8);
     tc::mbar_init(qempty, 1);
     tc::mbar_init(sfull, 1);
+    tc::mbar_init(sempty, 4);
     tc::mbar_init(pfull, 4);
     tc::mbar_init(pvdone, 1);
     tc::mbar_init(ofull, 1);
     tc::mbar_init(oempty, 4);
     tc::mbar_init(redb, 4);
     tc::mbar_init(done, 1);
-    tc::mbar_init(scfull, 8);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -241,87 +297,83 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 
   if (warp >= 4 && warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 128;");
-    // ------------------------------------------------------------ gather / convert
-    // Eight warps; warp cw owns key rows 16cw .. 16cw+15 of every tile (lanes 0-15 resolve
-    // them and publish their row scales). A lane holds 16 x 16 fp8 codes of a tile in
-    // registers: for block b (128 dims) and j = 0..3, row 16cw + 4j + lane/8, codes
-    // 128b + 16(lane%8) .. +15 (each warp load covers four 128-byte row segments). The
-    // next tile's loads are issued as soon as the current tile is converted, so they are
-    // in flight during the current tile's products and softmax.
-    const int cw = warp - 4;
+    // ------------------------------------------------------------ Q~ build + key copies
+    // Warp cw builds heads 8cw .. 8cw+7 of every item's Q~ (lane l: dims 16l .. 16l+15).
+    // Copy group gb = cw / 4 fills key buffer gb with the tiles of parity gb; warp wg = cw % 4
+    // of the group copies rows 32wg .. 32wg+31 (lane l resolves row 32wg + l, then each
+    // row's 512 bytes go as 32 16-byte copies, lane l taking bytes 16l .. 16l+15).
+    const int cw = warp - 4, gb = cw >> 2, wg = cw & 3;
     int gi = 0, ni = 0;   // global tile / item counters of this CTA
-    bool ok = true;
-    uint4 d[4][4];        // [block][j]
-    float sc_row = 0.f;   // scale of row 16cw + lane (lanes < 16)
-    auto issue = [&](const Item& I, int t) {
-      const int64_t x = I.x0 + (int64_t)t * kTile + cw * 16 + (lane & 15);
-      bool is_swa;
-      const int64_t slot = key_slot(p, I, x, is_swa, lane < 16);
-      const uint8_t* rowp = nullptr;
-      sc_row = 0.f;
-      if (slot >= 0) {
-        const CacheView& cv = is_swa ? p.swa : p.attn;
-        rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
-        sc_row = __ldg(cv.scale + slot);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rowp), 4 * j + (lane >> 3)));
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          d[b][j] = src ? __ldg(reinterpret_cast<const uint4*>(src + b * 128 + (lane & 7) * 16))
-                        : make_uint4(0, 0, 0, 0);
-      }
-    };
-    bool waited = false;
+    bool ok = true, waited = false;
+    const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(p.attn.data);   // any valid address
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = make_item(p, it);
       if (I.n_tiles == 0) continue;
-      if (waited) issue(I, 0);                      // tile 0 of the item in flight
-      // Q~ = RoPE(q, p) * scale * log2(e), bf16, K-major 128B-swizzled [64 heads][512]
+      // ---- Q~ of this item; the buffer is free once the previous item's S^T products are
       if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
       {
         const int tail0 = kD - p.rope.d_r;
-        float c = 1.f, s = 0.f;
-        if (lane < p.rope.d_r / 2) rope_cs(p.rope, I.pos, lane, c, s);
+        float rc[8], rsn[8];                       // RoPE of this lane's 8 dim pairs
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          rc[jj] = 1.f;
+          rsn[jj] = 0.f;
+          const int d = 16 * lane + 2 * jj;
+          if (d >= tail0) rope_cs(p.rope, I.pos, (d - tail0) >> 1, rc[jj], rsn[jj]);
+        }
         const float qs = p.scale * kLog2e;
         const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                                        (int64_t)I.qi * kH * kD);
-        const int ct = cw * 32 + lane;              // 0..255
-#pragma unroll 1
-        for (int base = 0; base < kH * (kD / 8); base += 256 * 8) {
-          uint4 u[8];
+                                                        ((int64_t)I.qi * kH + 8 * cw) * kD) + 2 * lane;
+        uint4 u[16];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = __ldg(q + base + k * 256 + ct);
+        for (int i = 0; i < 8; ++i) {
+          u[2 * i] = __ldg(q + i * (kD / 8));
+          u[2 * i + 1] = __ldg(q + i * (kD / 8) + 1);
+        }
+        float* qinv_item = qinv + (ni % 3) * 64;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int item = base + k * 256 + ct;
-            const int h = item / (kD / 8), ch = item % (kD / 8);   // 8 dims per chunk
-            const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u[k]);
-            float f[8];
+        for (int i = 0; i < 8; ++i) {
+          const int h = 8 * cw + i;
+          float f[16];
+          {
+            const __nv_bfloat162* e0 = reinterpret_cast<const __nv_bfloat162*>(&u[2 * i]);
+            const __nv_bfloat162* e1 = reinterpret_cast<const __nv_bfloat162*>(&u[2 * i + 1]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-            const int d0 = ch * 8;
-            const bool tail = d0 >= tail0;
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-              const int pi = tail ? (d0 + j - tail0) >> 1 : 0;
-              const float cc = __shfl_sync(0xffffffffu, c, pi);
-              const float ss = __shfl_sync(0xffffffffu, s, pi);
-              if (tail) {
-                const float a0 = f[j], a1 = f[j + 1];
-                f[j] = a0 * cc - a1 * ss;
-                f[j + 1] = a0 * ss + a1 * cc;
-              }
+            for (int j = 0; j < 4; ++j) {
+              const float2 a = __bfloat1622float2(e0[j]);
+              const float2 b = __bfloat1622float2(e1[j]);
+              f[2 * j] = a.x;
+              f[2 * j + 1] = a.y;
+              f[8 + 2 * j] = b.x;
+              f[8 + 2 * j + 1] = b.y;
             }
-            uint4 o;
-            o.x = pack_bf16(f[0] * qs, f[1] * qs);
-            o.y = pack_bf16(f[2] * qs, f[3] * qs);
-            o.z = pack_bf16(f[4] * qs, f[5] * qs);
-            o.w = pack_bf16(f[6] * qs, f[7] * qs);
-            *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * 8192 + tc::sw128_off(h, ch & 7)) = o;
           }
+          float amax = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float a0 = f[2 * jj], a1 = f[2 * jj + 1];
+            f[2 * jj] = (a0 * rc[jj] - a1 * rsn[jj]) * qs;
+            f[2 * jj + 1] = (a0 * rsn[jj] + a1 * rc[jj]) * qs;
+            amax = fmaxf(amax, fmaxf(fabsf(f[2 * jj]), fabsf(f[2 * jj + 1])));
+          }
+          amax = redux_max(amax);
+          // s = 2^(7 - ex) with amax = f * 2^ex, f in [1, 2): max |Q~ s| < 256 <= 448
+          int ex = exponent_of(amax);
+          if (!(amax > 0.f) || ex < -100 || ex > 100) ex = 7;   // zero, tiny or huge row: s = 1
+          const float s = pow2i(7 - ex);
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t h0, l0, h1, l1;
+            split_e4m3x2(f[4 * k] * s, f[4 * k + 1] * s, h0, l0);
+            split_e4m3x2(f[4 * k + 2] * s, f[4 * k + 3] * s, h1, l1);
+            hw[k] = h0 | (h1 << 16);
+            lw[k] = l0 | (l1 << 16);
+          }
+          uint8_t* dst = qbuf + (lane >> 3) * 16384;
+          *reinterpret_cast<uint4*>(dst + tc::sw128_off(h, lane & 7)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(dst + tc::sw128_off(kH + h, lane & 7)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          if (lane == 0) qinv_item[h] = pow2i(ex - 7);
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -330,35 +382,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       if (!waited) {                                // first item: Q~ was built meanwhile
         pdl_wait();
         waited = true;
-        issue(I, 0);
       }
-      for (int t = 0; t < I.n_tiles; ++t, ++gi) {
-        for (int b = 0; b < 4; ++b) {
-          if (!tc::mbar_wait(kempty + b, (gi & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
-          if (b == 0) {
-            // row scales for the softmax warps; the previous tile's product is done, so the
-            // softmax warps have consumed the previous hand-off
-            if (lane < 16) sscale[(gi & 1) * kTile + cw * 16 + lane] = sc_row;
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(scfull);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 lo, hi;
-            e4m3x16_to_bf16x16(d[b][j], lo, hi);
-            const int r = cw * 16 + 4 * j + (lane >> 3);
-            const int c0 = 2 * (lane & 7);               // bf16 chunk within the 128-dim block
-            const int kb = 2 * b + (c0 >> 3);
-            *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, c0 & 7)) = lo;
-            *reinterpret_cast<uint4*>(kbuf + kb * 16384 + tc::sw128_off(r, (c0 + 1) & 7)) = hi;
-          }
-          tc::fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(kfull + b);
+      // every warp's Q~ part and 1 / s_h are complete (ordered before this group's kfull)
+      if (!tc::mbar_wait(qfull, ni & 1, abort_flag, p.err)) { ok = false; break; }
+      for (int t = 0; t < I.n_tiles; ++t) {
+        const int g = gi + t;
+        if ((g & 1) != gb) continue;
+        // resolve the row first (top-k id, block table, scale), then wait for the buffer
+        const int64_t x = I.x0 + (int64_t)t * kTile + wg * 32 + lane;
+        bool is_swa;
+        const int64_t slot = key_slot(p, I, x, is_swa, true);
+        const uint8_t* rowp = nullptr;
+        float sc = 0.f;
+        if (slot >= 0) {
+          const CacheView& cv = is_swa ? p.swa : p.attn;
+          rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
+          sc = __ldg(cv.scale + slot);
         }
-        if (!ok) break;
-        if (t + 1 < I.n_tiles) issue(I, t + 1);     // next tile in flight during this one
+        if (g >= 2 && !tc::mbar_wait(kempty + gb, ((g >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        uint8_t* kb = kbuf + gb * kKBytes + (lane >> 3) * 16384;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rowp), i));
+          cp_async16(tc::smem_u32(kb + tc::sw128_off(wg * 32 + i, lane & 7)), src ? src + 16 * lane : zsrc,
+                     src ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        tc::fence_proxy_async();                    // the copied codes, for the tensor core
+        sscale[gb * kTile + wg * 32 + lane] = sc;   // 0 for a masked key
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(kfull + gb);
       }
+      gi += I.n_tiles;
       ++ni;
     }
   } else if (warp < 4) {
@@ -371,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     const int quad = warp;
     const int row = quad * 32 + lane;             // TMEM lane: key (S^T) or dim (O^T)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    // this thread's byte of every P' row: key `row` = byte row % 16 of 16-byte chunk row / 16
+    uint32_t xo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xo[k] = ((uint32_t)((row >> 4) ^ k) << 4) + (uint32_t)(row & 15);
     int gi = 0, ni = 0, ru = 0;
     bool ok = true;
     auto group_sync = [&]() -> bool {             // all four softmax warps
@@ -392,43 +453,68 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         }
         continue;
       }
+      const float* qv = qinv + (ni % 3) * 64;
       float l_reg = 0.f;                          // owner threads (row < 64)
       float mc0 = -INFINITY, mc1 = -INFINITY;     // running max of heads lane, lane + 32
+      int A = 0;                                  // P' = p * row scale * 2^A
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
         if (!tc::mbar_wait(sfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
         tc::fence_after_sync();
         float s[64];
-        {
-          float a[32];
-          tc::tmem_ld32(tmem + lane_base + kSCol, a);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) s[h] = a[h];
-          tc::tmem_ld32(tmem + lane_base + kSCol + 32, a);
-#pragma unroll
-          for (int h = 0; h < 32; ++h) s[32 + h] = a[h];
+        for (int half = 0; half < 2; ++half) {
+          float a[32], b[32];
+          tc::tmem_ld32(tmem + lane_base + kSCol + half * 32, a);        // hi
+          tc::tmem_ld32(tmem + lane_base + kSCol + kH + half * 32, b);   // lo
           tc::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s[half * 32 + h] = a[h] + b[h];
         }
-        if (!tc::mbar_wait(scfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
+        // S^T is in registers: the next tile's product may overwrite it
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(sempty);
+        // row scales of this tile (and the copy of its keys) are published with the buffer
+        if (!tc::mbar_wait(kfull + (gi & 1), (gi >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
         const float sc = sscale[(gi & 1) * kTile + row];   // 0 for a masked key
 #pragma unroll
-        for (int h = 0; h < 64; ++h) s[h] = sc > 0.f ? s[h] * sc : -INFINITY;
-        // ---- per-head max over the tile's 128 keys
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 w = *reinterpret_cast<const float4*>(qv + 4 * h4);
+          s[4 * h4 + 0] = sc > 0.f ? s[4 * h4 + 0] * (w.x * sc) : -INFINITY;
+          s[4 * h4 + 1] = sc > 0.f ? s[4 * h4 + 1] * (w.y * sc) : -INFINITY;
+          s[4 * h4 + 2] = sc > 0.f ? s[4 * h4 + 2] * (w.z * sc) : -INFINITY;
+          s[4 * h4 + 3] = sc > 0.f ? s[4 * h4 + 3] * (w.w * sc) : -INFINITY;
+        }
+        // ---- per-head max over the tile's 128 keys, and the tile's largest row scale
         float* rb = red_max + (ru & 1) * 256;
 #pragma unroll
         for (int h = 0; h < 64; ++h) {
           const float mh = redux_max(s[h]);
           if (lane == (h & 31)) rb[h * 4 + quad] = mh;
         }
+        {
+          const float scw = redux_max(sc);
+          if (lane == 0) red_sc[(ru & 1) * 4 + quad] = scw;
+        }
+        const float* rsc = red_sc + (ru & 1) * 4;
         if (!group_sync()) { ok = false; break; }
         // new running max of heads lane and lane + 32 (raised only past the threshold) and
-        // the correction factors exp2(old - new) of the accumulated O^T and denominators
+        // the correction factors exp2(old - new) of the accumulated O^T and denominators;
+        // P' keeps the tile's largest row scale times 2^A below 64, so P' < 4 * 64 = 256
         float mn0, mn1, cr0 = 1.f, cr1 = 1.f;
         bool any_rescale = false;
+        int a_new = A;
         {
           const float4 v0 = *reinterpret_cast<const float4*>(rb + lane * 4);
           const float4 v1 = *reinterpret_cast<const float4*>(rb + (lane + 32) * 4);
           const float mt0 = fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w));
           const float mt1 = fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w));
+          const float scm = fmaxf(fmaxf(rsc[0], rsc[1]), fmaxf(rsc[2], rsc[3]));
+          if (scm > 0.f) {
+            // 2^A = 2^(4 - ex): the largest row scale times 2^A lands in [16, 32)
+            const int ex = max(-100, min(100, exponent_of(scm)));
+            if (t == 0 || scm * pow2i(A) >= 64.f) a_new = 4 - ex;
+          }
           if (t == 0) {                          // nothing accumulated yet
             mn0 = mt0;
             mn1 = mt1;
@@ -437,7 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
             mn1 = mt1 > mc1 + kRescaleThreshold ? mt1 : mc1;
             if (mn0 != mc0) cr0 = fast_exp2(mc0 - mn0);   // 0 when the old max is -inf
             if (mn1 != mc1) cr1 = fast_exp2(mc1 - mn1);
-            any_rescale = __any_sync(0xffffffffu, mn0 != mc0 || mn1 != mc1);
+            const bool grew = __any_sync(0xffffffffu, mn0 != mc0 || mn1 != mc1);
+            any_rescale = grew || a_new != A;
           }
         }
 #pragma unroll
@@ -445,9 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           const float mn = __shfl_sync(0xffffffffu, h < 32 ? mn0 : mn1, h & 31);
           s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
         }
-        // ---- the P' buffer and O^T must be free of the previous tile's product
+        // ---- the P' buffers and O^T must be free of the previous tile's product
         if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         if (any_rescale) {
+          const float fa = pow2i(max(-126, a_new - A));   // a_new < A when it changed
+          const float f0 = cr0 * fa, f1 = cr1 * fa;
           tc::fence_after_sync();
 #pragma unroll 1
           for (int b = 0; b < 4; ++b) {
@@ -458,21 +547,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
               tc::tmem_ld32(addr, o);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; ++h) o[h] *= __shfl_sync(0xffffffffu, half ? cr1 : cr0, h);
+              for (int h = 0; h < 32; ++h) o[h] *= __shfl_sync(0xffffffffu, half ? f1 : f0, h);
               tmem_st32(addr, o);
             }
           }
           tmem_wait_st();
         }
-        // ---- P'^T row of this key: p * row scale, bf16, MN-major swizzled [128 keys][64 heads]
+        A = a_new;
+        // ---- P'^T = p * row scale * 2^A as e4m3 hi + lo, K-major [64 heads][128 keys]:
+        // this thread writes byte `row` of every head's row in both terms
+        {
+          const float f = sc * pow2i(A);
+          uint8_t* ph = pbuf;
+          uint8_t* pl = pbuf + kPBytes;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16(s[8 * c + 0] * sc, s[8 * c + 1] * sc);
-          v.y = pack_bf16(s[8 * c + 2] * sc, s[8 * c + 3] * sc);
-          v.z = pack_bf16(s[8 * c + 4] * sc, s[8 * c + 5] * sc);
-          v.w = pack_bf16(s[8 * c + 6] * sc, s[8 * c + 7] * sc);
-          *reinterpret_cast<uint4*>(pbuf + tc::sw128_off(row, c)) = v;
+          for (int h = 0; h < 64; h += 2) {
+            uint32_t hi2, lo2;
+            split_e4m3x2(s[h] * f, s[h + 1] * f, hi2, lo2);
+            const uint32_t o0 = (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u + xo[h & 7];
+            const uint32_t o1 = (uint32_t)((h + 1) >> 3) * 1024u + (uint32_t)((h + 1) & 7) * 128u + xo[(h + 1) & 7];
+            ph[o0] = (uint8_t)(hi2 & 0xFFu);
+            ph[o1] = (uint8_t)(hi2 >> 8);
+            pl[o0] = (uint8_t)(lo2 & 0xFFu);
+            pl[o1] = (uint8_t)(lo2 >> 8);
+          }
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -493,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         }
       }
       if (!ok) break;
-      // ---- publish the denominators, then read O^T (lanes: dims 128b + row; cols: heads)
-      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg > 0.f ? 1.f / l_reg : 0.f;   // 1 / l
+      // ---- publish 2^-A / l, then read O^T (lanes: dims 128b + row; cols: heads)
+      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg > 0.f ? pow2i(-A) / l_reg : 0.f;
       const float m_final = quad == 0 ? mc0 : mc1;   // used by the owners (row < 64)
       if (!group_sync()) { ok = false; break; }
       const float* linv = l_fin + (ni & 1) * 64;
@@ -562,62 +660,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
     // ------------------------------------------------------------ MMA issuer (warp 12)
-    // The whole warp walks the items and waits (a converged warp); lane 0 issues.
+    // The whole warp walks the items and waits (a converged warp); lane 0 issues. Order per
+    // item: S(0); then for each tile t: S(t+1) as soon as the softmax has read S(t) and
+    // tile t+1 is copied, then O += V P' of tile t once P'(t) is written.
     if (warp == 12) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16(kTile, kH);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16(128, kH, true, true);
+      constexpr uint32_t idesc_qk = idesc_e4m3(kTile, 2 * kH);
+      constexpr uint32_t idesc_pv = idesc_e4m3(128, kH, true);
       const uint32_t k0 = tc::smem_u32(kbuf), q0 = tc::smem_u32(qbuf), p0 = tc::smem_u32(pbuf);
-      const uint64_t dk_k = tc::sdesc_sw128(k0, 16, 1024);        // key tile, K-major
-      const uint64_t dq_k = tc::sdesc_sw128(q0, 16, 1024);        // Q~, K-major
-      const uint64_t dk_mn = tc::sdesc_sw128(k0, 16384, 1024);    // key tile as V^T, MN-major
-      const uint64_t dp_mn = tc::sdesc_sw128(p0, 8192, 1024);     // P'^T, MN-major
+      const uint64_t dq = tc::sdesc_sw128(q0, 16, 1024);                   // Q~ hi/lo, K-major
+      const uint64_t dph = tc::sdesc_sw128(p0, 16, 1024);                  // P' hi, K-major
+      const uint64_t dpl = tc::sdesc_sw128(p0 + kPBytes, 16, 1024);        // P' lo, K-major
       int gi = 0, ni = 0;
       bool ok = true;
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, abort_flag, p.err));
+      };
+      // S^T(g) = K Q~^T: 4 K-blocks x 4 steps of 32 dims
+      auto issue_s = [&](int g, bool last) {
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const uint64_t dk = tc::sdesc_sw128(k0 + (uint32_t)(g & 1) * kKBytes, 16, 1024);
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              // descriptor start address field counts 16-byte units
+              const uint64_t off = (uint64_t)((kb * 16384 + s4 * 32) >> 4);
+              mma_e4m3(tmem + kSCol, dk + off, dq + off, idesc_qk, (kb | s4) ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(sfull);
+          if (last) tc::mma_commit(qempty);
+        }
+        __syncwarp();
+      };
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const Item I = make_item(p, it);
         if (I.n_tiles == 0) continue;
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(qfull, ni & 1, abort_flag, p.err))) break;
+        if (!wait_all(qfull, ni & 1)) break;
+        // S(first tile): the copy of its keys, and the softmax done reading the S^T columns
+        if (!wait_all(kfull + (gi & 1), (gi >> 1) & 1)) break;
+        if (gi > 0 && !wait_all(sempty, (gi - 1) & 1)) break;
+        issue_s(gi, I.n_tiles == 1);
         for (int t = 0; t < I.n_tiles; ++t, ++gi) {
-          // S^T = K Q~^T over the 8 K-blocks, block pair b as soon as it is converted
-          for (int b = 0; b < 4; ++b) {
-            if (!__all_sync(0xffffffffu, tc::mbar_wait(kfull + b, gi & 1, abort_flag, p.err))) { ok = false; break; }
-            tc::fence_after_sync();
-            if (lane == 0) {
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                const int kb = 2 * b + kk;
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                  // descriptor start address field counts 16-byte units
-                  const uint64_t ad = dk_k + (uint64_t)((kb * 16384 + s4 * 32) >> 4);
-                  const uint64_t bd = dq_k + (uint64_t)((kb * 8192 + s4 * 32) >> 4);
-                  tc::mma_bf16(tmem + kSCol, ad, bd, idesc_qk, (kb | s4) ? 1u : 0u);
-                }
-              }
-            }
-            __syncwarp();
+          if (t + 1 < I.n_tiles) {
+            const int g1 = gi + 1;
+            if (!wait_all(kfull + (g1 & 1), (g1 >> 1) & 1)) { ok = false; break; }
+            if (!wait_all(sempty, gi & 1)) { ok = false; break; }
+            issue_s(g1, t + 2 == I.n_tiles);
           }
-          if (!ok) break;
-          if (lane == 0) {
-            tc::mma_commit(sfull);
-            if (t == I.n_tiles - 1) tc::mma_commit(qempty);
-          }
-          __syncwarp();
-          if (!__all_sync(0xffffffffu, tc::mbar_wait(pfull, gi & 1, abort_flag, p.err))) { ok = false; break; }
-          if (t == 0 && ni > 0 &&
-              !__all_sync(0xffffffffu, tc::mbar_wait(oempty, (ni - 1) & 1, abort_flag, p.err))) { ok = false; break; }
+          if (!wait_all(pfull, gi & 1)) { ok = false; break; }
+          if (t == 0 && ni > 0 && !wait_all(oempty, (ni - 1) & 1)) { ok = false; break; }
           tc::fence_after_sync();
           if (lane == 0) {
-            // O^T[dims of block b] += V^T P'^T; V^T is the key tile read MN-major
+            // O^T[dims of block b] += V^T (P'_hi + P'_lo)^T; V^T is the key tile read MN-major
+            const uint64_t dv = tc::sdesc_sw128(k0 + (uint32_t)(gi & 1) * kKBytes, 16384, 1024);
             for (int b = 0; b < 4; ++b) {
 #pragma unroll
-              for (int s8 = 0; s8 < 8; ++s8) {
-                const uint64_t ad = dk_mn + (uint64_t)(((2 * b) * 16384 + s8 * 2048) >> 4);
-                const uint64_t bd = dp_mn + (uint64_t)((s8 * 2048) >> 4);
-                tc::mma_bf16(tmem + kOCol + b * 64, ad, bd, idesc_pv, (t > 0 || s8 > 0) ? 1u : 0u);
+              for (int s4 = 0; s4 < 4; ++s4) {
+                const uint64_t ad = dv + (uint64_t)((b * 16384 + s4 * 4096) >> 4);
+                const uint64_t boff = (uint64_t)((s4 * 32) >> 4);
+                mma_e4m3(tmem + kOCol + b * 64, ad, dph + boff, idesc_pv, (t > 0 || s4 > 0) ? 1u : 0u);
+                mma_e4m3(tmem + kOCol + b * 64, ad, dpl + boff, idesc_pv, 1u);
               }
-              tc::mma_commit(kempty + b);
             }
+            tc::mma_commit(kempty + (gi & 1));
             tc::mma_commit(pvdone);
             if (t == I.n_tiles - 1) tc::mma_commit(ofull);
           }
