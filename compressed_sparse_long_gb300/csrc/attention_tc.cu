@@ -5,24 +5,27 @@
 // Work item: one query (prefill) or one key range of one query (decode split). Keys come
 // in tiles of 128 rows gathered from the paged pools (top-k entries or all visible
 // entries, then the window tokens). The key tile is the pool's own e4m3 codes, copied
-// row by row into a 128-byte-swizzled buffer (no conversion); per tile:
+// row by row (16-byte cp.async) into a 128-byte-swizzled buffer, no conversion; per tile:
 //   S^T = K Q~^T      M = 128 keys, N = 128 (64 heads x {hi, lo}), K = 512 dims
 //                     (16 MMAs kind::f8f6f4, TMEM cols 0..127)
-//   softmax over keys per head: logit = (hi + lo) / s_h * row scale; column max with
-//     redux.sync.max.f32 and a 4-warp exchange, column sums with a butterfly
-//     reduce-scatter; the running max is raised only when it grows by more than 2^2
-//     (then the O^T accumulator is rescaled)
+//   softmax over keys per head: logit = (hi + lo) / s * row scale; column max with
+//     redux.sync.max.f32 and a 4-warp exchange; the running max is raised only when it
+//     grows by more than 2^2 (then the O^T accumulator is rescaled); the per-row partial
+//     denominators accumulate in TMEM (cols 384..447) and are summed over the keys once per
+//     work item
 //   O^T += V^T P'^T   M = 128 dims x 4 blocks, N = 64 heads, K = 128 keys, P' = hi + lo
 //                     (32 MMAs, TMEM cols 128..383)
-// K = V: the key tile is read K-major by the first product and MN-major by the second.
+// K = V: the key tile is read K-major by the first product and MN-major by the second;
+// P'^T is MN-major with a 64-byte swizzle (a thread writes its key's 64-byte row).
 // Two key buffers: tile t+1 is copied while tile t is in use, and S^T of tile t+1 runs
 // during the softmax of tile t (the softmax frees the S^T columns as soon as it has read
 // them).
-// Exact-as-possible e4m3 operands: Q~ = RoPE(q, p) * softmax_scale * log2(e) (logits in
-// log2 units) is scaled per head by s_h = 2^(7 - exponent(max |Q~_h|)) and split into
-// hi = e4m3(Q~ s_h) and lo = e4m3(Q~ s_h - hi), about 8 significant bits like bf16; P' =
-// p * row scale * 2^A (A a per-range power of two that keeps P' below 2^8) is split the
-// same way, and 2^-A is folded into the final 1/l. The row scales stay out of the codes.
+// e4m3 operands close to bf16 precision: Q~ = RoPE(q, p) * softmax_scale * log2(e) (logits
+// in log2 units) is scaled by one power of two s per query (from sqrt(2) max |q|, which
+// bounds |RoPE(q)|) and split into hi = e4m3(Q~ s) and lo = e4m3(Q~ s - hi), through f16,
+// about 8 significant bits; P' = p * row scale * 2^A (A a per-range power of two that keeps
+// P' below 2^8) is split the same way, and 2^-A is folded into the final 1/l. The row
+// scales stay out of the codes.
 //
 // Warpgroups (setmaxnreg splits the 512 x 128 launch registers as 152 / 128 / 128 / 104):
 // 0 = softmax and epilogue (warp w reads TMEM lanes 32w..32w+31), 1-2 = eight copy warps
@@ -43,19 +46,21 @@ constexpr int kH = 64, kD = 512, kTile = 128;
 constexpr int kThreads = 512;                  // 4 warpgroups
 constexpr int kKBytes = kTile * kD;            // 64 KB e4m3 key tile, 4 K-blocks of 16 KB
 constexpr int kQBytes = 2 * kH * kD;           // 64 KB Q~ hi (rows 0-63) and lo (64-127), 4 K-blocks
-constexpr int kPBytes = kH * kTile;            // 8 KB per P' term, [64 heads][128 keys]
+constexpr int kPBytes = kH * kTile;            // 8 KB per P' term, [128 keys][64 heads]
 constexpr int kOffK = 0, kOffQ = 2 * kKBytes, kOffP = kOffQ + kQBytes;
-// floats: l_fin[2][64] red_max[2][256] red_sum[2][256] sscale[2][128] qinv[3][64] red_sc[2][4]
+// floats: l_fin[2][64] red_max[2][256] red_sum[256] sscale[2][128] mwarp[4][128] qamax[8]
+// qinv[3] red_sc[2][4]
 constexpr int kOffF = kOffP + 2 * kPBytes;
-constexpr int kNFloats = 128 + 512 + 512 + 256 + 192 + 8;
+constexpr int kNFloats = 128 + 512 + 256 + 256 + 512 + 8 + 4 + 8;
 constexpr int kOffBar = kOffF + kNFloats * 4;
-constexpr int kNBar = 14;
+constexpr int kNBar = 15;
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBytes % 1024 == 0, "swizzled operands need 1 KB alignment");
 static_assert(kOffBar % 8 == 0 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 0, kOCol = 128;
+// S^T (hi, lo), O^T (4 blocks of 64 heads), per-row partial denominators (64 heads)
+constexpr uint32_t kSCol = 0, kOCol = 128, kLCol = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 2.0f;      // log2 units: p <= 4 between rescales
 
@@ -190,10 +195,12 @@ __device__ __forceinline__ float2 reduce_scatter_sum64(const float (&v)[64]) {
 }
 
 // tcgen05.mma kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format
-// code 0), shape M x N; A read MN-major when asked (8-bit operands may be either major).
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// code 0), shape M x N; A and B read MN-major when asked (8-bit operands may be either
+// major).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false,
+                                                  bool b_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -219,16 +226,33 @@ __device__ __forceinline__ float pow2i(int a) { return __uint_as_float((uint32_t
 // Binary exponent of a positive normal float.
 __device__ __forceinline__ int exponent_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
 
-// Two values -> e4m3 hi codes (byte 0: a0, byte 1: a1) and the e4m3 codes of the
-// remainders a - hi (round to nearest even, saturating).
+// Two values -> e4m3 codes hi (byte 0: a0, byte 1: a1) and the e4m3 codes of the
+// remainders x - hi, where x is the pair rounded to f16 (11 significant bits; x - hi is
+// exact in f16). hi + lo holds about 8 significant bits of each value.
 __device__ __forceinline__ void split_e4m3x2(float a0, float a1, uint32_t& hi2, uint32_t& lo2) {
-  const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
-  const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
-  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+  const __half2 x = __floats2half2_rn(a0, a1);
+  const __nv_fp8x2_storage_t h =
+      __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&x), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+  const __half2 r = __hsub2(x, *reinterpret_cast<const __half2*>(&hr));
   const __nv_fp8x2_storage_t l =
-      __nv_cvt_float2_to_fp8x2(make_float2(a0 - hf.x, a1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+      __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3);
   hi2 = (uint32_t)h;
   lo2 = (uint32_t)l;
+}
+
+// Shared-memory matrix descriptor, 64-byte swizzle (atoms of 8 rows x 64 bytes, 16-byte
+// chunk c of row r stored at chunk c ^ ((r / 2) % 4)). Used for an MN-major operand whose
+// M/N extent is one atom wide: rows are K indices, 8-row groups SBO bytes apart (LBO, the
+// stride between atoms along M/N, is not needed and is given the same value).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
 }
 
 template <bool kSplit>
@@ -241,10 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   uint8_t* pbuf = sm + kOffP;                             // hi, then lo
   float* l_fin = reinterpret_cast<float*>(sm + kOffF);   // [2][64] 2^-A / l by item parity
   float* red_max = l_fin + 128;                           // [2][64 heads][4 warps]
-  float* red_sum = red_max + 512;                         // [2][64 heads][4 warps]
-  float* sscale = red_sum + 512;                          // [2][128] row scales by key buffer
-  float* qinv = sscale + 256;                             // [3][64] 1 / s_h by item % 3
-  float* red_sc = qinv + 192;                             // [2][4] tile max of the row scales
+  float* red_sum = red_max + 512;                         // [64 heads][4 warps]
+  float* sscale = red_sum + 256;                          // [2][128] row scales by key buffer
+  float* mwarp = sscale + 256;                            // [4 warps][128] per-warp head broadcast
+  float* qamax = mwarp + 512;                             // [8] raw |q| max of each build warp
+  float* qinv = qamax + 8;                                // [3] 1 / s by item % 3 (+1 pad)
+  float* red_sc = qinv + 4;                               // [2][4] tile max of the row scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* kfull = bars;                                 // [2] by key buffer
   uint64_t* kempty = bars + 2;                            // [2]
@@ -258,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   uint64_t* oempty = bars + 11;
   uint64_t* redb = bars + 12;
   uint64_t* done = bars + 13;
+  uint64_t* qmx = bars + 14;
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
@@ -283,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     tc::mbar_init(oempty, 4);
     tc::mbar_init(redb, 4);
     tc::mbar_init(done, 1);
+    tc::mbar_init(qmx, 8);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -312,16 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       // ---- Q~ of this item; the buffer is free once the previous item's S^T products are
       if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
       {
-        const int tail0 = kD - p.rope.d_r;
-        float rc[8], rsn[8];                       // RoPE of this lane's 8 dim pairs
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          rc[jj] = 1.f;
-          rsn[jj] = 0.f;
-          const int d = 16 * lane + 2 * jj;
-          if (d >= tail0) rope_cs(p.rope, I.pos, (d - tail0) >> 1, rc[jj], rsn[jj]);
-        }
-        const float qs = p.scale * kLog2e;
         const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
                                                         ((int64_t)I.qi * kH + 8 * cw) * kD) + 2 * lane;
         uint4 u[16];
@@ -330,7 +348,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           u[2 * i] = __ldg(q + i * (kD / 8));
           u[2 * i + 1] = __ldg(q + i * (kD / 8) + 1);
         }
-        float* qinv_item = qinv + (ni % 3) * 64;
+        // RoPE of this lane's 8 dim pairs: lane i computes pair i, the tail lanes collect theirs
+        const int tail0 = kD - p.rope.d_r;
+        float c_l = 1.f, s_l = 0.f;
+        if (lane < p.rope.d_r / 2) rope_cs(p.rope, I.pos, lane, c_l, s_l);
+        float rc[8], rsn[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int d = 16 * lane + 2 * jj;
+          const int pi = d >= tail0 ? ((d - tail0) >> 1) : 0;
+          rc[jj] = __shfl_sync(0xffffffffu, c_l, pi & 31);
+          rsn[jj] = __shfl_sync(0xffffffffu, s_l, pi & 31);
+          if (d < tail0) {
+            rc[jj] = 1.f;
+            rsn[jj] = 0.f;
+          }
+        }
+        // one power of two s per query: |RoPE(q)| <= sqrt(2) max |q|, so
+        // s = 2^(7 - exponent(sqrt(2) |scale| max |q|)) keeps every |Q~ s| below 256 <= 448
+        {
+          __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&u[k]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(e[j]));
+          }
+          const float2 mf = __bfloat1622float2(m2);
+          const float am = redux_max(fmaxf(mf.x, mf.y));
+          if (lane == 0) qamax[cw] = am;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(qmx);
+        }
+        if (!tc::mbar_wait(qmx, ni & 1, abort_flag, p.err)) { ok = false; break; }
+        const float4 qa = *reinterpret_cast<const float4*>(qamax);
+        const float4 qb = *reinterpret_cast<const float4*>(qamax + 4);
+        const float qs = p.scale * kLog2e;
+        const float bound = fmaxf(fmaxf(fmaxf(qa.x, qa.y), fmaxf(qa.z, qa.w)),
+                                  fmaxf(fmaxf(qb.x, qb.y), fmaxf(qb.z, qb.w))) * fabsf(qs) * 1.4142137f;
+        int ex = exponent_of(bound);
+        if (!(bound > 0.f) || ex < -100 || ex > 100) ex = 7;   // zero, tiny or huge query: s = 1
+        const float kq = qs * pow2i(7 - ex);
+        if (cw == 0 && lane == 0) qinv[ni % 3] = pow2i(ex - 7);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int h = 8 * cw + i;
@@ -348,32 +407,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
               f[8 + 2 * j + 1] = b.y;
             }
           }
-          float amax = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const float a0 = f[2 * jj], a1 = f[2 * jj + 1];
-            f[2 * jj] = (a0 * rc[jj] - a1 * rsn[jj]) * qs;
-            f[2 * jj + 1] = (a0 * rsn[jj] + a1 * rc[jj]) * qs;
-            amax = fmaxf(amax, fmaxf(fabsf(f[2 * jj]), fabsf(f[2 * jj + 1])));
-          }
-          amax = redux_max(amax);
-          // s = 2^(7 - ex) with amax = f * 2^ex, f in [1, 2): max |Q~ s| < 256 <= 448
-          int ex = exponent_of(amax);
-          if (!(amax > 0.f) || ex < -100 || ex > 100) ex = 7;   // zero, tiny or huge row: s = 1
-          const float s = pow2i(7 - ex);
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint32_t h0, l0, h1, l1;
-            split_e4m3x2(f[4 * k] * s, f[4 * k + 1] * s, h0, l0);
-            split_e4m3x2(f[4 * k + 2] * s, f[4 * k + 3] * s, h1, l1);
+            float x[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int jj = 2 * k + j;
+              const float a0 = f[2 * jj], a1 = f[2 * jj + 1];
+              x[2 * j] = (a0 * rc[jj] - a1 * rsn[jj]) * kq;
+              x[2 * j + 1] = (a0 * rsn[jj] + a1 * rc[jj]) * kq;
+            }
+            split_e4m3x2(x[0], x[1], h0, l0);
+            split_e4m3x2(x[2], x[3], h1, l1);
             hw[k] = h0 | (h1 << 16);
             lw[k] = l0 | (l1 << 16);
           }
           uint8_t* dst = qbuf + (lane >> 3) * 16384;
           *reinterpret_cast<uint4*>(dst + tc::sw128_off(h, lane & 7)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(dst + tc::sw128_off(kH + h, lane & 7)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          if (lane == 0) qinv_item[h] = pow2i(ex - 7);
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -383,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         pdl_wait();
         waited = true;
       }
-      // every warp's Q~ part and 1 / s_h are complete (ordered before this group's kfull)
+      // every warp's Q~ part and 1 / s are complete (ordered before this group's kfull)
       if (!tc::mbar_wait(qfull, ni & 1, abort_flag, p.err)) { ok = false; break; }
       for (int t = 0; t < I.n_tiles; ++t) {
         const int g = gi + t;
@@ -422,16 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     pdl_wait();
     // ------------------------------------------------------------ softmax + epilogue
-    // Every lane keeps the running max of heads `lane` and `lane + 32` in registers (all
-    // four warps hold the same copy); the owner of head h (thread row h) keeps its
-    // denominator in a register and publishes it in l_fin[item parity][64] for the epilogue.
+    // Thread `row` holds key `row` of the tile for all 64 heads. Every lane keeps the
+    // running max of heads `lane` and `lane + 32` in registers (all four warps hold the same
+    // copy) and publishes it in its warp's mwarp slice for the per-element exponentials.
+    // The per-row partial denominators (sum over this thread's keys of p, per head) stay in
+    // TMEM columns kLCol.. and are reduced over the keys once per item.
     const int quad = warp;
     const int row = quad * 32 + lane;             // TMEM lane: key (S^T) or dim (O^T)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    // this thread's byte of every P' row: key `row` = byte row % 16 of 16-byte chunk row / 16
-    uint32_t xo[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) xo[k] = ((uint32_t)((row >> 4) ^ k) << 4) + (uint32_t)(row & 15);
+    float* mb = mwarp + quad * 128;               // [0,64): max; [64,128): rescale factors
+    // this thread's P' row (key `row`, 64 bytes): 16-byte chunk c at c ^ ((row / 2) % 4)
+    const uint32_t prow = (uint32_t)row * 64u, pswz = (uint32_t)((row >> 1) & 3);
     int gi = 0, ni = 0, ru = 0;
     bool ok = true;
     auto group_sync = [&]() -> bool {             // all four softmax warps
@@ -453,8 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         }
         continue;
       }
-      const float* qv = qinv + (ni % 3) * 64;
-      float l_reg = 0.f;                          // owner threads (row < 64)
       float mc0 = -INFINITY, mc1 = -INFINITY;     // running max of heads lane, lane + 32
       int A = 0;                                  // P' = p * row scale * 2^A
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
@@ -477,13 +529,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         // row scales of this tile (and the copy of its keys) are published with the buffer
         if (!tc::mbar_wait(kfull + (gi & 1), (gi >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
         const float sc = sscale[(gi & 1) * kTile + row];   // 0 for a masked key
+        {
+          // 1 / s of this item's Q~ (written before the builders' qfull, which the copy
+          // warps waited for before publishing this buffer)
+          const float fq = sc * qinv[ni % 3];
 #pragma unroll
-        for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 w = *reinterpret_cast<const float4*>(qv + 4 * h4);
-          s[4 * h4 + 0] = sc > 0.f ? s[4 * h4 + 0] * (w.x * sc) : -INFINITY;
-          s[4 * h4 + 1] = sc > 0.f ? s[4 * h4 + 1] * (w.y * sc) : -INFINITY;
-          s[4 * h4 + 2] = sc > 0.f ? s[4 * h4 + 2] * (w.z * sc) : -INFINITY;
-          s[4 * h4 + 3] = sc > 0.f ? s[4 * h4 + 3] * (w.w * sc) : -INFINITY;
+          for (int h = 0; h < 64; ++h) s[h] *= fq;
+          if (!(sc > 0.f)) {
+#pragma unroll
+            for (int h = 0; h < 64; ++h) s[h] = -INFINITY;
+          }
         }
         // ---- per-head max over the tile's 128 keys, and the tile's largest row scale
         float* rb = red_max + (ru & 1) * 256;
@@ -527,10 +582,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
             any_rescale = grew || a_new != A;
           }
         }
+        // broadcast the maxima (a head with no finite logit yet subtracts 0: its p are 0) and
+        // the correction factors through this warp's slice
+        mb[lane] = mn0 == -INFINITY ? 0.f : mn0;
+        mb[32 + lane] = mn1 == -INFINITY ? 0.f : mn1;
+        mb[64 + lane] = cr0;
+        mb[96 + lane] = cr1;
+        __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 64; ++h) {
-          const float mn = __shfl_sync(0xffffffffu, h < 32 ? mn0 : mn1, h & 31);
-          s[h] = (mn == -INFINITY || s[h] == -INFINITY) ? 0.f : fast_exp2(s[h] - mn);
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 m = *reinterpret_cast<const float4*>(mb + 4 * h4);
+          s[4 * h4 + 0] = fast_exp2(s[4 * h4 + 0] - m.x);   // exp2(-inf) = 0 for masked keys
+          s[4 * h4 + 1] = fast_exp2(s[4 * h4 + 1] - m.y);
+          s[4 * h4 + 2] = fast_exp2(s[4 * h4 + 2] - m.z);
+          s[4 * h4 + 3] = fast_exp2(s[4 * h4 + 3] - m.w);
+        }
+        // ---- per-row partial denominators: l_row = l_row * cr + p (TMEM, 64 columns)
+        {
+          const uint32_t la = tmem + lane_base + kLCol;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float l[32];
+            if (t > 0) {
+              tc::tmem_ld32(la + half * 32, l);
+              tc::tmem_wait_ld();
+              if (any_rescale) {
+#pragma unroll
+                for (int h4 = 0; h4 < 8; ++h4) {
+                  const float4 c = *reinterpret_cast<const float4*>(mb + 64 + half * 32 + 4 * h4);
+                  l[4 * h4 + 0] = fmaf(l[4 * h4 + 0], c.x, s[half * 32 + 4 * h4 + 0]);
+                  l[4 * h4 + 1] = fmaf(l[4 * h4 + 1], c.y, s[half * 32 + 4 * h4 + 1]);
+                  l[4 * h4 + 2] = fmaf(l[4 * h4 + 2], c.z, s[half * 32 + 4 * h4 + 2]);
+                  l[4 * h4 + 3] = fmaf(l[4 * h4 + 3], c.w, s[half * 32 + 4 * h4 + 3]);
+                }
+              } else {
+#pragma unroll
+                for (int h = 0; h < 32; ++h) l[h] += s[half * 32 + h];
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 32; ++h) l[h] = s[half * 32 + h];
+            }
+            tmem_st32(la + half * 32, l);
+          }
+          tmem_wait_st();
         }
         // ---- the P' buffers and O^T must be free of the previous tile's product
         if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
@@ -554,57 +649,65 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           tmem_wait_st();
         }
         A = a_new;
-        // ---- P'^T = p * row scale * 2^A as e4m3 hi + lo, K-major [64 heads][128 keys]:
-        // this thread writes byte `row` of every head's row in both terms
+        // ---- P'^T = p * row scale * 2^A as e4m3 hi + lo, MN-major [128 keys][64 heads],
+        // 64-byte swizzle: this thread writes its key's row, four 16-byte chunks per term
         {
-          const float f = sc * pow2i(A);
-          uint8_t* ph = pbuf;
-          uint8_t* pl = pbuf + kPBytes;
+          const float fp = sc * pow2i(A);
 #pragma unroll
-          for (int h = 0; h < 64; h += 2) {
-            uint32_t hi2, lo2;
-            split_e4m3x2(s[h] * f, s[h + 1] * f, hi2, lo2);
-            const uint32_t o0 = (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u + xo[h & 7];
-            const uint32_t o1 = (uint32_t)((h + 1) >> 3) * 1024u + (uint32_t)((h + 1) & 7) * 128u + xo[(h + 1) & 7];
-            ph[o0] = (uint8_t)(hi2 & 0xFFu);
-            ph[o1] = (uint8_t)(hi2 >> 8);
-            pl[o0] = (uint8_t)(lo2 & 0xFFu);
-            pl[o1] = (uint8_t)(lo2 >> 8);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t h0, l0, h1, l1;
+              const int h = 16 * c + 4 * k;
+              split_e4m3x2(s[h] * fp, s[h + 1] * fp, h0, l0);
+              split_e4m3x2(s[h + 2] * fp, s[h + 3] * fp, h1, l1);
+              hw[k] = h0 | (h1 << 16);
+              lw[k] = l0 | (l1 << 16);
+            }
+            const uint32_t off = prow + (((uint32_t)c ^ pswz) << 4);
+            *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(pbuf + kPBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(pfull);
-        // ---- per-head sums of p over the tile's keys -> the owners' denominators (these
-        // overlap the P'V product, which only needs P')
-        float* rs = red_sum + (ru & 1) * 256;
-        const float2 part = reduce_scatter_sum64(s);
-        rs[(2 * lane) * 4 + quad] = part.x;
-        rs[(2 * lane + 1) * 4 + quad] = part.y;
-        if (!group_sync()) { ok = false; break; }
         mc0 = mn0;
         mc1 = mn1;
-        if (row < 64) {
-          const float4 v = *reinterpret_cast<const float4*>(rs + row * 4);
-          l_reg = l_reg * (quad == 0 ? cr0 : cr1) + ((v.x + v.y) + (v.z + v.w));
-        }
       }
       if (!ok) break;
-      // ---- publish 2^-A / l, then read O^T (lanes: dims 128b + row; cols: heads)
-      if (row < 64) l_fin[(ni & 1) * 64 + row] = l_reg > 0.f ? pow2i(-A) / l_reg : 0.f;
+      // ---- denominators: sum the per-row partials over the 128 rows (keys), owner thread h
+      // (row < 64) gets head h's l and publishes 2^-A / l
+      float l_own = 0.f;
+      {
+        float lv[64];
+        tc::tmem_ld32(tmem + lane_base + kLCol, *reinterpret_cast<float(*)[32]>(&lv[0]));
+        tc::tmem_ld32(tmem + lane_base + kLCol + 32, *reinterpret_cast<float(*)[32]>(&lv[32]));
+        tc::tmem_wait_ld();
+        const float2 part = reduce_scatter_sum64(lv);
+        red_sum[(2 * lane) * 4 + quad] = part.x;
+        red_sum[(2 * lane + 1) * 4 + quad] = part.y;
+        if (!group_sync()) { ok = false; break; }
+        if (row < 64) {
+          const float4 v = *reinterpret_cast<const float4*>(red_sum + row * 4);
+          l_own = (v.x + v.y) + (v.z + v.w);
+          l_fin[(ni & 1) * 64 + row] = l_own > 0.f ? pow2i(-A) / l_own : 0.f;
+        }
+      }
       const float m_final = quad == 0 ? mc0 : mc1;   // used by the owners (row < 64)
       if (!group_sync()) { ok = false; break; }
       const float* linv = l_fin + (ni & 1) * 64;
       if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }
       tc::fence_after_sync();
+      const bool even = (lane & 1) == 0;
       if (kSplit) {
         // partial o / l in bf16 (the range's max and denominator go out in fp32): lanes 2i
         // and 2i+1 hold dims d, d+1; for heads (h, h+1) the even lane stores head h's pair
         // and the odd lane head h+1's, one 32-bit store each
         const int64_t base = ((int64_t)I.qi * p.n_split + I.split) * kH;
         uint32_t* part = reinterpret_cast<uint32_t*>(p.part_o);
-        const bool even = (lane & 1) == 0;
         for (int b = 0; b < 4; ++b) {
           const int d = b * 128 + row;
           float ob[2][32];                          // both halves of the block, one wait
@@ -617,7 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 #pragma unroll
             for (int h = 0; h < 32; h += 2) {
               const int hh = half * 32 + h;
-              const float a = o[h] * linv[hh], bb = o[h + 1] * linv[hh + 1];
+              const float2 li = *reinterpret_cast<const float2*>(linv + hh);
+              const float a = o[h] * li.x, bb = o[h + 1] * li.y;
               const float recv = __shfl_xor_sync(0xffffffffu, even ? bb : a, 1);
               const uint32_t w = even ? pack_bf16(a, recv) : pack_bf16(recv, bb);
               const int head = even ? hh : hh + 1, d0 = even ? d : d - 1;
@@ -627,27 +731,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         }
         if (row < 64) {
           p.part_ml[(base + row) * 2] = m_final;
-          p.part_ml[(base + row) * 2 + 1] = l_reg;
+          p.part_ml[(base + row) * 2 + 1] = l_own;
         }
       } else {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)I.qi * kH * kD;
+        // out = R^-1 (o / l) in bf16: the same pairing, the even lane rotating head h's pair
+        // (d, d+1) and the odd lane head h+1's
+        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                    (int64_t)I.qi * kH * kD);
         const int tail0 = kD - p.rope.d_r;
         for (int b = 0; b < 4; ++b) {
-          const int d = b * 128 + row;
+          const int d = b * 128 + row, d0 = even ? d : d - 1;
           float c = 1.f, sn = 0.f;
-          const bool tail = d >= tail0;
-          if (tail) rope_cs(p.rope, I.pos, (d - tail0) >> 1, c, sn);
+          if (d0 >= tail0) rope_cs(p.rope, I.pos, (d0 - tail0) >> 1, c, sn);
+          float ob[2][32];
+          tc::tmem_ld32(tmem + lane_base + kOCol + b * 64, ob[0]);
+          tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + 32, ob[1]);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            float o[32];
-            tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + half * 32, o);
-            tc::tmem_wait_ld();
+            const float (&o)[32] = ob[half];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              float v = o[h] * linv[half * 32 + h];
-              const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-              if (tail) v = (d & 1) ? (-partner * sn + v * c) : (v * c + partner * sn);
-              out[(int64_t)(half * 32 + h) * kD + d] = __float2bfloat16_rn(v);
+            for (int h = 0; h < 32; h += 2) {
+              const int hh = half * 32 + h;
+              const float2 li = *reinterpret_cast<const float2*>(linv + hh);
+              const float a = o[h] * li.x, bb = o[h + 1] * li.y;
+              const float recv = __shfl_xor_sync(0xffffffffu, even ? bb : a, 1);
+              const float x0 = even ? a : recv, x1 = even ? recv : bb;   // dims d0, d0 + 1
+              const int head = even ? hh : hh + 1;
+              out[((int64_t)head * kD + d0) >> 1] = pack_bf16(x0 * c + x1 * sn, x1 * c - x0 * sn);
             }
           }
         }
@@ -665,11 +776,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     // tile t+1 is copied, then O += V P' of tile t once P'(t) is written.
     if (warp == 12) {
       constexpr uint32_t idesc_qk = idesc_e4m3(kTile, 2 * kH);
-      constexpr uint32_t idesc_pv = idesc_e4m3(128, kH, true);
+      constexpr uint32_t idesc_pv = idesc_e4m3(128, kH, true, true);
       const uint32_t k0 = tc::smem_u32(kbuf), q0 = tc::smem_u32(qbuf), p0 = tc::smem_u32(pbuf);
       const uint64_t dq = tc::sdesc_sw128(q0, 16, 1024);                   // Q~ hi/lo, K-major
-      const uint64_t dph = tc::sdesc_sw128(p0, 16, 1024);                  // P' hi, K-major
-      const uint64_t dpl = tc::sdesc_sw128(p0 + kPBytes, 16, 1024);        // P' lo, K-major
+      const uint64_t dph = sdesc_sw64(p0, 512);                            // P' hi, MN-major
+      const uint64_t dpl = sdesc_sw64(p0 + kPBytes, 512);                  // P' lo, MN-major
       int gi = 0, ni = 0;
       bool ok = true;
       auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -719,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 #pragma unroll
               for (int s4 = 0; s4 < 4; ++s4) {
                 const uint64_t ad = dv + (uint64_t)((b * 16384 + s4 * 4096) >> 4);
-                const uint64_t boff = (uint64_t)((s4 * 32) >> 4);
+                const uint64_t boff = (uint64_t)((s4 * 32 * 64) >> 4);   // 32 keys of 64 bytes
                 mma_e4m3(tmem + kOCol + b * 64, ad, dph + boff, idesc_pv, (t > 0 || s4 > 0) ? 1u : 0u);
                 mma_e4m3(tmem + kOCol + b * 64, ad, dpl + boff, idesc_pv, 1u);
               }
