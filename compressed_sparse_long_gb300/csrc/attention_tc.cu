@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       }
       float mc0 = -INFINITY, mc1 = -INFINITY;     // running max of heads lane, lane + 32
       int A = 0;                                  // P' = p * row scale * 2^A
+      bool a_set = false;                         // A chosen (a tile with an unmasked key seen)
       for (int t = 0; t < I.n_tiles; ++t, ++gi) {
         if (!tc::mbar_wait(sfull, gi & 1, abort_flag, p.err)) { ok = false; break; }
         tc::fence_after_sync();
@@ -566,9 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
           const float mt1 = fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w));
           const float scm = fmaxf(fmaxf(rsc[0], rsc[1]), fmaxf(rsc[2], rsc[3]));
           if (scm > 0.f) {
-            // 2^A = 2^(4 - ex): the largest row scale times 2^A lands in [16, 32)
+            // 2^A = 2^(4 - ex): the largest row scale times 2^A lands in [16, 32); chosen at
+            // the range's first tile with an unmasked key (O^T is still zero when earlier
+            // tiles were all masked) and lowered when a tile's scales outgrow it
             const int ex = max(-100, min(100, exponent_of(scm)));
-            if (t == 0 || scm * pow2i(A) >= 64.f) a_new = 4 - ex;
+            if (!a_set || scm * pow2i(A) >= 64.f) a_new = 4 - ex;
+            a_set = true;
           }
           if (t == 0) {                          // nothing accumulated yet
             mn0 = mt0;
@@ -630,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         // ---- the P' buffers and O^T must be free of the previous tile's product
         if (gi > 0 && !tc::mbar_wait(pvdone, (gi - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         if (any_rescale) {
-          const float fa = pow2i(max(-126, a_new - A));   // a_new < A when it changed
+          const float fa = pow2i(max(-126, min(127, a_new - A)));
           const float f0 = cr0 * fa, f1 = cr1 * fa;
           tc::fence_after_sync();
 #pragma unroll 1

@@ -416,6 +416,39 @@ def test_attention_split_merge_modes(B, L, plan):
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
 
+def _lists_with_masked_blocks(rng, pos, spec):
+    """Top-512 lists whose key blocks 0-127 and 256-383 are all -1 (masked) and whose blocks
+    128-255 and 384-511 hold distinct visible entries: with 128-key tiles, a key range may
+    then begin with a tile that has no key."""
+    out = np.full((len(pos), 512), -1, np.int32)
+    for i, p in enumerate(pos):
+        n = O.visible_entries(spec.S, spec.W, spec.win_off, int(p))
+        e = rng.choice(n, 256, replace=False)
+        out[i, 128:256] = np.sort(e[:128])
+        out[i, 384:512] = np.sort(e[128:])
+    return out
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_key_range_starting_with_a_masked_tile(prefill):
+    """Decode (3 key ranges of 256/256/128 keys) and prefill (one range of 5 tiles) where
+    tiles 0 and 2 hold only masked list entries: the per-range scaling of P' must be set by
+    the first tile that has a key, not by the range's first tile."""
+    w = wl.c4a_decode(seed=23, B=32, L=4096)
+    h = w.layers[0]
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lists = _lists_with_masked_blocks(np.random.default_rng(8), q.pos, h.spec)
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    if not prefill:
+        assert v4a.v4a_attn_plan(lay.cfg, 32, x.max_pos, 512) == (3, 2)
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32),
+                        prefill=prefill, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
+    check_out(out.float().cpu().numpy(), ref, fp8=True)
+
+
 def _e4m3_step(v):
     """Grid step of the e4m3 value nearest |v| (the spacing a rounding error is bounded by)."""
     g = O.e4m3_values()
