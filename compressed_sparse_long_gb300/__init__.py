@@ -16,6 +16,8 @@ import torch
 __all__ = [
     "V4AError", "LayerCfg", "Cache", "library", "layer_cfg", "cache",
     "v4a_compress_insert", "v4a_compress_insert_qnorm", "v4a_index_topk", "v4a_index_topk_workspace_size",
+    "v4a_index_scores", "v4a_index_scores_row_stride", "v4a_index_topk_noalloc",
+    "v4a_index_topk_noalloc_capacity",
     "v4a_attn_decode", "v4a_attn_prefill", "v4a_attn_workspace_size", "v4a_slot_mapping",
     "v4a_attn_decode_q8", "v4a_attn_q8_workspace_size", "v4a_attn_plan",
     "v4a_get_error", "v4a_version",
@@ -27,10 +29,11 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libv4a.so")
 C4A, C128A = 0, 1
 FP32, BF16_FP8 = 0, 1
 IDX_DEFAULT, IDX_FP4 = 0, 1
-OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4
+OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE, ERR_TOO_LARGE = 0, -1, -2, -3, -4, -5
 DEV_MISSING_PAGE, DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_BAD_POS = 1, 2, 4, 8
 _NAMES = {ERR_ARG: "V4A_ERR_ARG", ERR_UNSUPPORTED: "V4A_ERR_UNSUPPORTED",
-          ERR_CUDA: "V4A_ERR_CUDA", ERR_DEVICE: "V4A_ERR_DEVICE"}
+          ERR_CUDA: "V4A_ERR_CUDA", ERR_DEVICE: "V4A_ERR_DEVICE",
+          ERR_TOO_LARGE: "V4A_ERR_TOO_LARGE"}
 
 
 class V4AError(RuntimeError):
@@ -83,6 +86,9 @@ _SIGS = {
     "v4a_attn_q8_workspace_size": (_SZ, [_CFG, _I32, _I64, _I32]),
     "v4a_attn_decode_q8": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _I32, _CACHE, _CACHE,
                                           _P, _P, _P, _SZ, _P, _P]),
+    "v4a_index_scores_row_stride": (_I64, [_CFG, _I64]),
+    "v4a_index_scores": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _P, _SZ, _P,
+                                        _P]),
     "v4a_index_topk_noalloc_capacity": (_SZ, []),
     "v4a_index_topk_noalloc": (ctypes.c_int, [_CFG, _I32, _P, _P, _I64, _P, _P, _CACHE, _I32,
                                               _P, _P, _P]),
@@ -186,6 +192,19 @@ def v4a_index_topk(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, k, topk_out, 
         ctypes.byref(cfg), n_q, _ptr(q_seq), _ptr(q_pos), max_pos, _ptr(q_idx), _ptr(w),
         ctypes.byref(idx), k, _ptr(topk_out), _ptr(workspace), ws_bytes, _ptr(dev_err),
         _stream(stream)))
+
+
+def v4a_index_scores_row_stride(cfg, max_pos) -> int:
+    return library().v4a_index_scores_row_stride(ctypes.byref(cfg), max_pos)
+
+
+def v4a_index_scores(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, scores, dev_err=None,
+                     stream=None):
+    """Indexer score rows alone: scores [n_q, v4a_index_scores_row_stride(cfg, max_pos)] fp32."""
+    nb = 0 if scores is None else scores.numel() * scores.element_size()
+    _check("v4a_index_scores", library().v4a_index_scores(
+        ctypes.byref(cfg), n_q, _ptr(q_seq), _ptr(q_pos), max_pos, _ptr(q_idx), _ptr(w),
+        ctypes.byref(idx), _ptr(scores), nb, _ptr(dev_err), _stream(stream)))
 
 
 def v4a_index_topk_noalloc_capacity() -> int:

@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 13;
+constexpr int32_t kVersion = 14;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -33,8 +33,10 @@ Rope make_rope(const v4a_layer_cfg* c) {
   return r;
 }
 
+}  // namespace
+
 // Layer-level checks shared by every call.
-int check_cfg(const v4a_layer_cfg* c) {
+int v4a::check_cfg(const v4a_layer_cfg* c) {
   if (!c) return V4A_ERR_ARG;
   if (c->kind != V4A_C4A && c->kind != V4A_C128A) return V4A_ERR_UNSUPPORTED;
   if (c->dtype != V4A_FP32 && c->dtype != V4A_BF16_FP8) return V4A_ERR_UNSUPPORTED;
@@ -54,18 +56,8 @@ int check_cfg(const v4a_layer_cfg* c) {
   return V4A_OK;
 }
 
-}  // namespace
-
-// The indexer pool as the kernels see it: width in bytes for packed fp4 rows.
-CacheView v4a::idx_view(const v4a_layer_cfg* cfg, const v4a_cache* idx) {
-  CacheView v = view_of(idx);
-  if (cfg->idx_format == V4A_IDX_FP4) v.width = idx->row_width / 2;
-  return v;
-}
-
-namespace {
-
-int check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8) {
+// Checks of a cache descriptor: geometry, alignment, scales of fp8 pools.
+int v4a::check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8) {
   if (!c || !c->data || !c->block_table) return V4A_ERR_ARG;
   if (c->rows_per_block != rows_per_block || c->row_width != width) return V4A_ERR_ARG;
   if (c->max_blocks <= 0 || c->n_pages < 0 || c->reserved != 0) return V4A_ERR_ARG;
@@ -74,9 +66,54 @@ int check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8) {
   return V4A_OK;
 }
 
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// The indexer pool as the kernels see it: width in bytes for packed fp4 rows.
+CacheView v4a::idx_view(const v4a_layer_cfg* cfg, const v4a_cache* idx) {
+  CacheView v = view_of(idx);
+  if (cfg->idx_format == V4A_IDX_FP4) v.width = idx->row_width / 2;
+  return v;
+}
 
-int cuda_status(int rc) { return rc; }
+// Host-side validation and parameters of the indexer calls (v4a_index_topk,
+// v4a_index_topk_noalloc, v4a_index_scores): every one of them returns the same code for
+// the same arguments. with_topk: k and topk_out are part of the call. p->scores is left for
+// the caller to set.
+int v4a::prepare_index(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                       const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
+                       const v4a_cache* idx, int32_t k, int32_t* topk_out, bool with_topk,
+                       int32_t* dev_err, IndexParams* p, int64_t* max_vis) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (cfg->kind != V4A_C4A) return V4A_ERR_UNSUPPORTED;
+  if (n_q < 0 || (with_topk && k <= 0) || max_pos < 0) return V4A_ERR_ARG;
+  if (n_q == 0) return V4A_OK;
+  if (!q_seq || !q_pos || !q_idx || !w || (with_topk && !topk_out)) return V4A_ERR_ARG;
+  const bool fp8 = cfg->dtype == V4A_BF16_FP8;
+  if ((rc = check_cache(idx, kBlock / cfg->stride, cfg->idx_dim, fp8))) return rc;
+  if (!aligned(q_idx, 16) || !aligned(w, 16)) return V4A_ERR_ARG;
+  *max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
+  *p = IndexParams{};
+  p->n_q = n_q;
+  p->H_I = cfg->idx_heads;
+  p->d_I = cfg->idx_dim;
+  p->W = cfg->window;
+  p->S = cfg->stride;
+  p->win_off = cfg->win_off;
+  p->k = with_topk ? k : 0;
+  p->row_stride = score_row_stride(*max_vis);
+  p->q_seq = q_seq;
+  p->q_pos = q_pos;
+  p->q_idx = q_idx;
+  p->w = w;
+  p->idx = idx_view(cfg, idx);
+  p->idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
+  p->topk = with_topk ? topk_out : nullptr;
+  p->err = dev_err;
+  return V4A_OK;
+}
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
@@ -198,41 +235,39 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                    const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
                    const v4a_cache* idx, int32_t k, int32_t* topk_out, void* workspace,
                    size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream) {
-  int rc = check_cfg(cfg);
-  if (rc) return rc;
-  if (cfg->kind != V4A_C4A) return V4A_ERR_UNSUPPORTED;
-  if (n_q < 0 || k <= 0 || max_pos < 0) return V4A_ERR_ARG;
-  if (n_q == 0) return V4A_OK;
-  if (!q_seq || !q_pos || !q_idx || !w || !topk_out) return V4A_ERR_ARG;
-  const bool fp8 = cfg->dtype == V4A_BF16_FP8;
-  if ((rc = check_cache(idx, kBlock / cfg->stride, cfg->idx_dim, fp8))) return rc;
-  if (!aligned(q_idx, 16) || !aligned(w, 16)) return V4A_ERR_ARG;
-  const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
+  IndexParams p{};
+  int64_t max_vis = 0;
+  int rc = prepare_index(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, k, topk_out, true,
+                         dev_err, &p, &max_vis);
+  if (rc || n_q == 0) return rc;
   if (max_vis > 0) {
     if (!workspace || !aligned(workspace, 256)) return V4A_ERR_ARG;
     if (workspace_bytes < v4a_index_topk_workspace_size(cfg, n_q, max_pos)) return V4A_ERR_ARG;
   }
-  IndexParams p{};
-  p.n_q = n_q;
-  p.H_I = cfg->idx_heads;
-  p.d_I = cfg->idx_dim;
-  p.W = cfg->window;
-  p.S = cfg->stride;
-  p.win_off = cfg->win_off;
-  p.k = k;
-  p.row_stride = score_row_stride(max_vis);
-  p.q_seq = q_seq;
-  p.q_pos = q_pos;
-  p.q_idx = q_idx;
-  p.w = w;
-  p.idx = idx_view(cfg, idx);
-  p.idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
   p.scores = reinterpret_cast<float*>(workspace);
-  p.topk = topk_out;
-  p.err = dev_err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = launch_index_scores(p, cfg->dtype, max_vis, st))) return rc;
   return launch_topk(p, max_vis, st);
+}
+
+int64_t v4a_index_scores_row_stride(const v4a_layer_cfg* cfg, int64_t max_pos) {
+  if (check_cfg(cfg) || max_pos < 0) return 0;
+  return score_row_stride(visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off));
+}
+
+int v4a_index_scores(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                     const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
+                     const v4a_cache* idx, float* scores, size_t scores_bytes, int32_t* dev_err,
+                     v4a_stream_t stream) {
+  IndexParams p{};
+  int64_t max_vis = 0;
+  int rc = prepare_index(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, 0, nullptr, false,
+                         dev_err, &p, &max_vis);
+  if (rc || n_q == 0 || max_vis == 0) return rc;
+  if (!scores || !aligned(scores, 16)) return V4A_ERR_ARG;
+  if (scores_bytes < (size_t)n_q * (size_t)p.row_stride * sizeof(float)) return V4A_ERR_ARG;
+  p.scores = scores;
+  return launch_index_scores(p, cfg->dtype, max_vis, reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace {

@@ -12,8 +12,10 @@
 // loads the library holds it until the process exits. A call needs n_q * visible(max_pos)
 // fp32 scores; a larger request is refused with V4A_ERR_TOO_LARGE before anything is
 // enqueued. The first call on each device looks up the array's device address
-// (cudaGetSymbolAddress, with that device current) and keeps it; make that first call
-// before any stream capture. All calls share the one array and it keeps the last call's
+// (cudaGetSymbolAddress, with that device current) and keeps it for the life of the
+// process; make that first call before any stream capture. A device reset
+// (cudaDeviceReset) unloads the library's device image, so the kept address is no longer
+// valid: do not call this entry point on a device after resetting it. All calls share the one array and it keeps the last call's
 // contents: every score the selection reads is written earlier in the same call, so nothing
 // has to be cleared, but two calls whose kernels overlap on the GPU (different streams
 // without ordering between them) race on the array and give wrong lists.
@@ -59,51 +61,17 @@ extern "C" int v4a_index_topk_noalloc(const v4a_layer_cfg* cfg, int32_t n_q, con
                                       const int64_t* q_pos, int64_t max_pos, const void* q_idx,
                                       const float* w, const v4a_cache* idx, int32_t k,
                                       int32_t* topk_out, int32_t* dev_err, v4a_stream_t stream) {
-  if (!cfg) return V4A_ERR_ARG;
-  if (cfg->kind != V4A_C4A) return V4A_ERR_UNSUPPORTED;
-  if (cfg->dtype != V4A_FP32 && cfg->dtype != V4A_BF16_FP8) return V4A_ERR_UNSUPPORTED;
-  if (cfg->window <= 0 || cfg->stride <= 0 || kBlock % cfg->stride != 0) return V4A_ERR_UNSUPPORTED;
-  if (cfg->win_off > 0 || cfg->win_off <= -cfg->window) return V4A_ERR_ARG;
-  if (cfg->idx_format != V4A_IDX_DEFAULT && cfg->idx_format != V4A_IDX_FP4) return V4A_ERR_UNSUPPORTED;
-  if (cfg->idx_format == V4A_IDX_FP4 && (cfg->dtype != V4A_BF16_FP8 || cfg->idx_dim != 128))
-    return V4A_ERR_UNSUPPORTED;
-  if (n_q < 0 || k <= 0 || max_pos < 0) return V4A_ERR_ARG;
-  if (n_q == 0) return V4A_OK;
-  if (!q_seq || !q_pos || !q_idx || !w || !topk_out) return V4A_ERR_ARG;
-  if (reinterpret_cast<uintptr_t>(q_idx) % 16 != 0 || reinterpret_cast<uintptr_t>(w) % 16 != 0)
-    return V4A_ERR_ARG;
-  const bool fp8 = cfg->dtype == V4A_BF16_FP8;
-  if (!idx || !idx->data || !idx->block_table || idx->rows_per_block != kBlock / cfg->stride ||
-      idx->row_width != cfg->idx_dim || idx->max_blocks <= 0 || idx->n_pages < 0 ||
-      idx->reserved != 0 || reinterpret_cast<uintptr_t>(idx->data) % 16 != 0 ||
-      (fp8 && (!idx->scale || reinterpret_cast<uintptr_t>(idx->scale) % 16 != 0)))
-    return V4A_ERR_ARG;
-  const int64_t max_vis = visible_entries(max_pos, cfg->stride, cfg->window, cfg->win_off);
-  if ((uint64_t)n_q * (uint64_t)score_row_stride(max_vis) > kNoallocScoreFloats)
-    return V4A_ERR_TOO_LARGE;
+  // the same host checks, in the same order, as v4a_index_topk
+  IndexParams p{};
+  int64_t max_vis = 0;
+  int rc = prepare_index(cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, idx, k, topk_out, true,
+                         dev_err, &p, &max_vis);
+  if (rc || n_q == 0) return rc;
+  if ((uint64_t)n_q * (uint64_t)p.row_stride > kNoallocScoreFloats) return V4A_ERR_TOO_LARGE;
 
   float* scratch = nullptr;
-  int rc = noalloc_scratch(&scratch);
-  if (rc) return rc;
-
-  IndexParams p{};
-  p.n_q = n_q;
-  p.H_I = cfg->idx_heads;
-  p.d_I = cfg->idx_dim;
-  p.W = cfg->window;
-  p.S = cfg->stride;
-  p.win_off = cfg->win_off;
-  p.k = k;
-  p.row_stride = score_row_stride(max_vis);
-  p.q_seq = q_seq;
-  p.q_pos = q_pos;
-  p.q_idx = q_idx;
-  p.w = w;
-  p.idx = idx_view(cfg, idx);
-  p.idx_fp4 = cfg->idx_format == V4A_IDX_FP4;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
   p.scores = scratch;
-  p.topk = topk_out;
-  p.err = dev_err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = launch_index_scores(p, cfg->dtype, max_vis, st))) return rc;
   return launch_topk(p, max_vis, st);

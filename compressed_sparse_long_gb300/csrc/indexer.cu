@@ -501,13 +501,11 @@ int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
     e = launch_pdl(topk_reg_kernel<32, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
   } else if (max_vis <= kTopkSmemMax) {
     const size_t smem = (size_t)max_vis * sizeof(uint32_t);
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kTopkSmemMax * (int)sizeof(uint32_t));
-      attr_set = true;
-    }
-    e = launch_pdl(topk_kernel<true>, dim3(p.n_q), dim3(kTopkThreads), smem, st, p);
+    // the attribute belongs to the current device's copy of the kernel: set it on every
+    // launch (a host call, cheap next to the kernel) so that every device gets it
+    e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkSmemMax * (int)sizeof(uint32_t));
+    if (e == cudaSuccess) e = launch_pdl(topk_kernel<true>, dim3(p.n_q), dim3(kTopkThreads), smem, st, p);
   } else {
     e = launch_pdl(topk_kernel<false>, dim3(p.n_q), dim3(kTopkThreads), 0, st, p);
   }

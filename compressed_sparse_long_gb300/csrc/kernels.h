@@ -71,6 +71,14 @@ struct AttnParams {
   int32_t* err;
 };
 
+// Host-side checks shared by the entry points (V4A_OK or the code the call returns).
+int check_cfg(const v4a_layer_cfg* cfg);
+int check_cache(const v4a_cache* c, int rows_per_block, int width, bool fp8);
+// Validation and parameters of the indexer calls; p->scores is set by the caller.
+int prepare_index(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                  const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
+                  const v4a_cache* idx, int32_t k, int32_t* topk_out, bool with_topk,
+                  int32_t* dev_err, IndexParams* p, int64_t* max_vis);
 // The indexer pool as the kernels see it (width in bytes for packed fp4 rows).
 CacheView idx_view(const v4a_layer_cfg* cfg, const v4a_cache* idx);
 int launch_compress_insert(const CompressParams& p, int dtype, cudaStream_t st);

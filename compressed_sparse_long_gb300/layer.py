@@ -16,7 +16,8 @@ from . import (BF16_FP8, C4A, C128A, FP32, IDX_DEFAULT, IDX_FP4, cache, layer_cf
                v4a_attn_decode_q8, v4a_attn_q8_workspace_size,
                v4a_attn_prefill, v4a_attn_workspace_size, v4a_compress_insert,
                v4a_compress_insert_qnorm,
-               v4a_index_topk, v4a_index_topk_workspace_size)
+               v4a_index_scores, v4a_index_scores_row_stride, v4a_index_topk,
+               v4a_index_topk_workspace_size)
 
 
 def _t(x, dtype, device):
@@ -123,6 +124,16 @@ class Layer:
         ws = self.workspace("index", nb, q_seq.device)
         v4a_index_topk(self.cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, self.idx.c, k, out, ws,
                        dev_err, stream)
+        return out
+
+    def index_scores(self, q_seq, q_pos, max_pos, q_idx, w, dev_err=None, stream=None):
+        """Indexer score rows alone: fp32 [n_q, row stride]; row i is valid up to the
+        number of entries visible at q_pos[i]."""
+        n_q = q_seq.numel()
+        stride = v4a_index_scores_row_stride(self.cfg, max_pos)
+        out = torch.empty((n_q, max(stride, 4)), dtype=torch.float32, device=q_seq.device)
+        v4a_index_scores(self.cfg, n_q, q_seq, q_pos, max_pos, q_idx, w, self.idx.c, out,
+                         dev_err, stream)
         return out
 
     def attention(self, q_seq, q_pos, max_pos, q, topk=None, k=0, out=None, prefill=False,

@@ -199,6 +199,23 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
                    size_t workspace_bytes, int32_t* dev_err, v4a_stream_t stream);
 
 /*
+ * v4a_index_scores — the indexer scores alone (step a6), as v4a_index_topk computes them
+ * before its selection ([blog] DeepSeek Sparse Attention: score_j = sum_h w_h ReLU(q_h . k_j)).
+ * Same arguments and checks as v4a_index_topk without k and the output list. Row i of
+ * `scores` holds score_j of query i in column j for every visible j (j < visible(q_pos[i]));
+ * the other columns of the row are not written.
+ *
+ * scores:       device fp32 [n_q, v4a_index_scores_row_stride(cfg, max_pos)], 16-byte
+ *               aligned, caller-owned; scores_bytes its size (V4A_ERR_ARG if too small)
+ * row stride:   visible(max_pos) rounded up to a multiple of 4 floats (0 for a bad cfg)
+ */
+int64_t v4a_index_scores_row_stride(const v4a_layer_cfg* cfg, int64_t max_pos);
+int v4a_index_scores(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
+                     const int64_t* q_pos, int64_t max_pos, const void* q_idx, const float* w,
+                     const v4a_cache* idx, float* scores, size_t scores_bytes, int32_t* dev_err,
+                     v4a_stream_t stream);
+
+/*
  * v4a_index_topk_noalloc — v4a_index_topk without a workspace argument, for callers that
  * cannot allocate device memory and have none to lend: for example a library embedded in
  * a framework or serving runtime that owns all device memory and gives its kernels no
@@ -214,7 +231,10 @@ int v4a_index_topk(const v4a_layer_cfg* cfg, int32_t n_q, const int32_t* q_seq,
  * (2,097,152; e.g. 64 queries at positions up to 131,072); larger requests return
  * V4A_ERR_TOO_LARGE without enqueuing anything. The call itself allocates nothing.
  * The first call on each device looks up the array's device address while that device
- * is current; make that first call before any stream capture. All calls share the array
+ * is current and keeps it for the life of the process; make that first call before any
+ * stream capture. A device reset (cudaDeviceReset) unloads the library's device image and
+ * makes the kept address invalid: do not call this entry point on a device after resetting
+ * it. The host checks and their return codes are those of v4a_index_topk. All calls share the array
  * and it keeps the previous call's contents (each call writes every score it reads, so no
  * clearing is needed); calls that overlap on the GPU, e.g. on two unordered streams, race
  * on it and must be serialised by the caller.

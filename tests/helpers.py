@@ -53,6 +53,24 @@ def oracle_pools(layer):
     return O.Pools(layer.spec, layer.attn, layer.idx, layer.swa, layer.state)
 
 
+class _HostPool:
+    """Host copy of one device pool, in the shape the oracle's Pools reads."""
+
+    def __init__(self, pool):
+        d = pool.data.cpu()
+        self.data = d.float().numpy() if d.dtype in (torch.bfloat16, torch.float32) else d.numpy()
+        self.scale = None if pool.scale is None else pool.scale.cpu().numpy()
+        self.bt = pool.block_table.cpu().numpy()
+        self.rows_per_block = pool.rows_per_block
+
+
+def device_pools(lay, spec):
+    """The oracle's view of the pools as the GPU left them: indexer and attention parity
+    run on the GPU-written codes and scales (the same dequantised values on both sides)."""
+    return O.Pools(spec, _HostPool(lay.attn), None if lay.idx is None else _HostPool(lay.idx),
+                   _HostPool(lay.swa), _HostPool(lay.state))
+
+
 def oracle_insert(w, layer, pools):
     b = w.batch
     return O.compress_insert(layer.spec, layer.bias, layer.gamma, layer.ibias, pools, b.cu,

@@ -160,3 +160,44 @@ def test_attention_split_plan_on_a_152_sm_gpu():
     # 4 tiles (512 keys) a range, 17 ranges
     assert v4a.v4a_attn_plan(c128a, 8, 1 << 20, 0) == (17, 2)
     assert v4a.v4a_attn_plan(c128a, 8, 1 << 20, 0, True) == (1, 1)
+
+
+def test_indexer_entry_points_share_their_host_checks(lib):
+    """v4a_index_topk, v4a_index_topk_noalloc and v4a_index_scores run the same host checks:
+    for each invalid configuration or cache descriptor they return the same code, and none
+    of them enqueues anything (no GPU is touched here)."""
+    c = v4a.Cache(4096, 8192, 256, 4, 64, 10, 128, 0)
+    bad_cfgs = [_cfg(kind=7), _cfg(rope_dim=3), _cfg(win_off=1), _cfg(window=512),
+                _cfg(head_dim=100), _cfg(swa=0), _cfg(rms_eps=-1.0),
+                _cfg(rope_base=0.0), _cfg(idx_format=7), _cfg(dtype=v4a.FP32, idx_format=1),
+                _cfg(kind=v4a.C128A, window=128, stride=128)]
+    bad_caches = [v4a.Cache(4096, 8192, 256, 4, 64, 10, 96, 0),      # row width
+                  v4a.Cache(4100, 8192, 256, 4, 64, 10, 128, 0),     # misaligned pool
+                  v4a.Cache(4096, None, 256, 4, 64, 10, 128, 0),     # fp8 pool without scales
+                  v4a.Cache(4096, 8192, 256, 4, 32, 10, 128, 0),     # rows per block
+                  v4a.Cache(4096, 8192, 256, 4, 64, 10, 128, 1)]     # reserved field
+    cases = [(cfg, c) for cfg in bad_cfgs] + [(_cfg(), bc) for bc in bad_caches]
+    for cfg, cc in cases:
+        a = lib.v4a_index_topk(ctypes.byref(cfg), 1, 16, 16, 100, 4096, 16, ctypes.byref(cc), 4,
+                               16, 4096, 1 << 20, None, None)
+        b = lib.v4a_index_topk_noalloc(ctypes.byref(cfg), 1, 16, 16, 100, 4096, 16,
+                                       ctypes.byref(cc), 4, 16, None, None)
+        s = lib.v4a_index_scores(ctypes.byref(cfg), 1, 16, 16, 100, 4096, 16, ctypes.byref(cc),
+                                 4096, 1 << 20, None, None)
+        assert a != v4a.OK and a == b == s, (cfg.kind, cfg.rope_dim, a, b, s)
+    # misaligned query operands, and a non-positive k where the call selects
+    for args in ((4100, 16, 4), (4096, 20, 4)):
+        a = lib.v4a_index_topk(ctypes.byref(_cfg()), 1, 16, 16, 100, args[0], args[1],
+                               ctypes.byref(c), args[2], 16, 4096, 1 << 20, None, None)
+        b = lib.v4a_index_topk_noalloc(ctypes.byref(_cfg()), 1, 16, 16, 100, args[0], args[1],
+                                       ctypes.byref(c), args[2], 16, None, None)
+        assert a == b == v4a.ERR_ARG
+    assert lib.v4a_index_topk_noalloc(ctypes.byref(_cfg()), 1, 16, 16, 100, 4096, 16,
+                                      ctypes.byref(c), 0, 16, None, None) == v4a.ERR_ARG
+    # the scores call checks the size of its output rows
+    assert v4a.v4a_index_scores_row_stride(_cfg(), 32768) == 8192
+    assert v4a.v4a_index_scores_row_stride(_cfg(), 100) == 24
+    assert lib.v4a_index_scores(ctypes.byref(_cfg()), 2, 16, 16, 100, 4096, 16, ctypes.byref(c),
+                                4096, 2 * 24 * 4 - 4, None, None) == v4a.ERR_ARG
+    assert lib.v4a_index_scores(ctypes.byref(_cfg()), 2, 16, 16, 100, 4096, 16, ctypes.byref(c),
+                                4100, 2 * 24 * 4, None, None) == v4a.ERR_ARG

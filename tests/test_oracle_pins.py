@@ -426,6 +426,37 @@ def test_window_only_attention_is_sdpa():
     assert np.allclose(out, ref, atol=1e-12)
 
 
+def test_window_edge_is_sdpa_with_a_128_token_band():
+    """The window's edge, pinned away from the oracle's own code: with no rotation and every
+    top-k slot empty, the oracle's attention at each of 320 positions equals torch's fp64
+    SDPA over all tokens with a band mask of the pages' 128 tokens ([notes] 四大核心技术 4,
+    窗口大小 128): a query at p sees t with 0 <= p - t < 128, its own token included (the
+    reading of the window range). A 127- or 129-token band gives a different output, so an
+    off-by-one at either end of the window fails this test."""
+    n = 320
+    w = wl.tiny_prefill(seed=16, L=n, d_r=0)
+    spec = w.layers[0].spec
+    width = GOLD["swa_window"]["value"]
+    pools = _fresh_pools(w)
+    _run_compress(w, pools)
+    qs = w.queries
+    out = O.attention(spec, pools, qs.seq, qs.pos, qs.q, topk=np.full((n, spec.top_k), -1))
+    keys = torch.tensor(w.batch.kv, dtype=torch.float64)              # window rows (d_r = 0)
+    q = torch.tensor(qs.q, dtype=torch.float64).transpose(0, 1)       # [H, n, D]
+    lag = torch.arange(n)[:, None] - torch.arange(n)[None, :]         # p - t
+
+    def sdpa(band):
+        mask = (lag >= 0) & (lag < band)
+        return torch.nn.functional.scaled_dot_product_attention(
+            q, keys.expand(spec.H, n, spec.D), keys.expand(spec.H, n, spec.D),
+            attn_mask=mask, scale=spec.scale).transpose(0, 1).numpy()
+
+    assert np.allclose(out, sdpa(width), atol=1e-12)
+    for wrong in (width - 1, width + 1):
+        d = np.abs(out - sdpa(wrong)).max(axis=(1, 2))
+        assert (d[:wrong - 1] < 1e-12).all() and d[width:].min() > 1e-6
+
+
 def _pipeline(w, permute=False):
     """Whole layer from raw tokens: insert, index + top-k, attention. With permute, every
     pool's pages are shuffled (contents moved, block tables rewritten to match)."""

@@ -63,6 +63,47 @@ def test_noalloc_with_the_fp4_cache():
     assert np.array_equal(got, ref)
 
 
+def test_noalloc_rows_longer_than_32768_entries():
+    """Two queries that each see 39,999 entries: the selection stages each row in shared
+    memory (the path for rows of 32,768 to 49,152 entries). Same lists as the workspace
+    call, and the oracle's within the tie band."""
+    w = wl.c4a_decode(seed=35, B=2, L=160000)
+    got, ref = _both(w)
+    assert np.array_equal(got, ref)
+    h = w.layers[0]
+    q = w.queries
+    o_top, scores = O.index_topk(h.spec, oracle_pools(h), q.seq, q.pos, q.q_idx, q.w, 512)
+    assert len(scores[0]) == 39999
+    check_topk(got, o_top, scores, 512)
+
+
+def test_noalloc_request_exactly_at_capacity():
+    """64 queries whose score rows fill the scratch exactly: max_pos = 131,067 gives 32,765
+    visible entries, rows of 32,768 floats, 64 x 32,768 = the capacity. The chunk's own
+    entries are inserted first, so every visible entry holds a key."""
+    cap = v4a.v4a_index_topk_noalloc_capacity()
+    w = wl.c4a_prefill(seed=36, cached=131004, chunk=64)
+    h = w.layers[0]
+    lay, x = device_layer(h), DevInputs(w)
+    assert x.max_pos == 131067
+    assert 64 * v4a.v4a_index_scores_row_stride(lay.cfg, x.max_pos) == cap
+    lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_)
+    ref = lay.index_topk(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w)
+    got = torch.full_like(ref, -7)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    v4a.v4a_index_topk_noalloc(lay.cfg, 64, x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w,
+                               lay.idx.c, 512, got, err)
+    assert v4a.v4a_get_error(err) == 0
+    assert torch.equal(got, ref)
+    # the next larger row (max_pos 131,080: 32,769 visible entries, rows of 32,772 floats)
+    # no longer fits and is refused
+    assert 64 * v4a.v4a_index_scores_row_stride(lay.cfg, 131080) > cap
+    with pytest.raises(v4a.V4AError) as e:
+        v4a.v4a_index_topk_noalloc(lay.cfg, 64, x.q_seq, x.q_pos, 131080, x.q_idx,
+                                   x.w, lay.idx.c, 512, got)
+    assert e.value.code == -5
+
+
 def test_noalloc_refuses_requests_beyond_the_scratch():
     cap = v4a.v4a_index_topk_noalloc_capacity()
     assert cap == (8 << 20) // 4
