@@ -66,6 +66,42 @@ def attn_bytes_per_query(k: int, swa: int, H: int = 64, D: int = 512) -> int:
     return (k + swa) * (D + 4) + k * 4 + 2 * H * D * 2
 
 
+def compress_bytes_per_token(D: int = 512, d_I: int = 128, S: int = 4, c4a: bool = True) -> int:
+    """Bytes the insert must move per new token: read kv, s (and ik, is) in bf16, write the
+    token's window row (fp8 codes + fp32 scale) and 1/S of an entry (attention row, and the
+    indexer row for c4a); the residual rows of the last window are left out (per call)."""
+    read = (2 * D + (2 * d_I if c4a else 0)) * 2
+    entry = (D + 4) + ((d_I + 4) if c4a else 0)
+    return read + (D + 4) + entry // S
+
+
+def c128a_bytes_per_query(n_vis: int, swa: int, D: int = 512, H: int = 64) -> dict:
+    """Dense c128a decode: every visible entry and window row (fp8 + scale), the query and
+    the output, the sequence's block-table row (one int32 per 2-entry block) and the insert."""
+    parts = {
+        "entry_rows": n_vis * (D + 4),
+        "window_rows": swa * (D + 4),
+        "q_and_out": 2 * H * D * 2,
+        "block_table": ((n_vis + 1) // 2) * 4,
+        "insert": 2 * (2 * D) * 2 + (D + 4),     # new token in, residual + window out
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def mixed_bytes(lens, k: int = 512, swa: int = 128) -> dict:
+    """Exact algorithmic bytes of one mixed decode step from the drawn lengths: the c4a layer
+    (indexer keys of every visible entry, top-k + window rows, query/out, indexer query) and
+    the c128a layer (every visible entry + window rows, query/out)."""
+    c4a = c128 = 0
+    for L in lens:
+        n4 = max(0, (L - 8) // 4 + 1)
+        n128 = max(0, (L - 128) // 128 + 1)
+        c4a += decode_bytes_per_query(n4, min(k, n4), swa)["total"]
+        c128 += c128a_bytes_per_query(n128, swa)["total"]
+    return {"c4a_layer": c4a, "c128a_layer": c128, "total": c4a + c128}
+
+
 def attn_flops_per_query(n_keys: int, H: int = 64, D: int = 512) -> float:
     return 4.0 * H * D * n_keys          # QK^T and PV, 2 flops per multiply-add
 
@@ -231,7 +267,7 @@ def _dev(x, dt, dev):
 
 
 class DecodeReplica:
-    """One copy of the decode workload's device state (pools + step inputs/outputs)."""
+    """One copy of a decode workload's device state (pools + step inputs/outputs)."""
 
     def __init__(self, base_layer, w, dev, clone: bool, side: bool = False):
         import torch
@@ -240,15 +276,17 @@ class DecodeReplica:
         self.side = torch.cuda.Stream(device=dev) if side else None
         b, q = w.batch, w.queries
         bf = torch.bfloat16
+        opt = lambda x, dt: None if x is None else _dev(x, dt, dev)
         self.cu = _dev(b.cu, torch.int32, dev)
         self.start = _dev(b.start, torch.int64, dev)
         self.kv, self.s = _dev(b.kv, bf, dev), _dev(b.s, bf, dev)
-        self.ik, self.is_ = _dev(b.ik, bf, dev), _dev(b.is_, bf, dev)
+        self.ik, self.is_ = opt(b.ik, bf), opt(b.is_, bf)
         self.q_seq, self.q_pos = _dev(q.seq, torch.int32, dev), _dev(q.pos, torch.int64, dev)
-        self.q, self.q_idx = _dev(q.q, bf, dev), _dev(q.q_idx, bf, dev)
-        self.w = _dev(q.w, torch.float32, dev)
+        self.q, self.q_idx = _dev(q.q, bf, dev), opt(q.q_idx, bf)
+        self.w = opt(q.w, torch.float32)
         self.max_pos = int(q.pos.max())
-        self.topk = torch.empty((len(q.pos), self.lay.top_k), dtype=torch.int32, device=dev)
+        k = max(self.lay.top_k, 1)
+        self.topk = torch.empty((len(q.pos), k), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)   # device error bits
         # query-norm weight and output of the fused insert + query RMSNorm call
@@ -259,13 +297,54 @@ class DecodeReplica:
     def step(self):
         self.lay.step(self.cu, self.start, self.kv, self.s, self.ik, self.is_, self.q_seq,
                       self.q_pos, self.max_pos, self.q, self.q_idx, self.w, out=self.out,
-                      dev_err=self.err, side_stream=self.side, topk_out=self.topk)
+                      dev_err=self.err, side_stream=self.side,
+                      topk_out=self.topk if self.lay.top_k else None)
 
     def touched_bytes(self):
         n_vis = (self.max_pos - 8) // 4 + 1
         fp4 = self.lay.cfg.idx_format == 1
         return len(self.q) * decode_bytes_per_query(n_vis, self.lay.top_k, 128,
                                                     idx_fp4=fp4)["total"]
+
+
+def chained_ms_per_step(step_fns, steps, warmup, stream):
+    """Device time per step: one CUDA graph holds one step of every replica in turn (the
+    replicas' steps linked by programmatic dependent launch, as a model's layers run in
+    one graph), replayed; a tail graph of the first steps % n replicas makes the count
+    exactly `steps`. Returns (ms per step, the graphs for reuse)."""
+    import torch
+    n = len(step_fns)
+    for f in step_fns:
+        f()
+    torch.cuda.synchronize()
+
+    def cap(fs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in fs:
+                f()
+        return g
+
+    chain = cap(step_fns)
+    tail = cap(step_fns[:steps % n]) if steps % n else None
+    for _ in range(max(1, -(-warmup // n))):
+        chain.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps // n):
+        chain.replay()
+    if tail is not None:
+        tail.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def n_replicas(bytes_per_step: int, l2: int, fixed: int = 0) -> int:
+    """Pool replicas so that the replicas' working set is at least 4x L2 (every step then
+    reads its pools from HBM)."""
+    return fixed or max(2, int(math.ceil(4.0 * l2 / bytes_per_step)))
 
 
 def gpu_main(args, rank: int, world: int, local_rank: int):
@@ -281,8 +360,20 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or getattr(props, "l2_cache_size", 0) or (126 << 20)
 
-    if args.only == "prefill":          # profiling aid: the prefill chunk alone
+    # profiling aids: one secondary workload alone
+    if args.only == "prefill":
         print(json.dumps({"prefill": _prefill(dev, tf_peak, tf_sus)}), flush=True)
+        return
+    if args.only == "c128a":
+        print(json.dumps({"c128a_decode": _c128a_decode(dev, args, l2, hbm_peak, tf_peak, rank,
+                                                        world)}), flush=True)
+        return
+    if args.only == "mixed":
+        print(json.dumps({"mixed_decode": _mixed_decode(dev, args, l2, hbm_peak, rank, world)}),
+              flush=True)
+        return
+    if args.only == "compress":
+        print(json.dumps({"compressor_aux": _compressor_aux(dev, hbm_peak)}), flush=True)
         return
     w = wl.c4a_decode(seed=rank_seed(rank), B=B, L=L)
     base = Layer.from_host(w.layers[0], dev)
@@ -350,6 +441,14 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     ms_max = _max_over_ranks(ms, world, dev)
+    # a steadier figure beside it: the median over five more windows of the same steps
+    windows = []
+    for _ in range(5):
+        e0.record(stream)
+        run_steps(chain, tails, args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        windows.append(_max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps)
     value = whole_job_rate(B * args.steps, world, ms_max)
     ms_per_step = ms_max / args.steps
     algo_bytes_step = per_step
@@ -400,8 +499,13 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
             ("attention", "v4a_attn_decode (attention + split merge)",
              B * attn_bytes_per_query(512, 128))):
         gbs = nbytes / (calls[call] / 1e3) / 1e9
+        traffic = _profile_traffic(call)
         roof[call] = {"kernel": kern, "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
-                      "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": _profile_traffic(call),
+                      "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": traffic,
+                      "traffic_source": None if traffic is None else
+                      "profile-sourced: dram__bytes_read.sum + dram__bytes_write.sum per call "
+                      "from the committed ncu summary profiles/%s_c4a_decode_B32_L32768.md "
+                      "(same library version), not measured in this run" % call,
                       "peak_source": peak_src, "algorithmic_bytes_per_launch": nbytes,
                       "us_per_launch": calls[call] * 1e3}
     dominant = max(roof, key=lambda c: calls[c])
@@ -428,6 +532,8 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / hbm_peak,
         "ms_per_step_one_graph_per_step": ms_one,
+        "ms_per_step_median_of_5_windows": float(np.median(windows)),
+        "ms_per_step_windows": windows,
         "per_call_ms": calls,
         "side_stream": overlap,
         "fp4_indexer": fp4,
@@ -441,6 +547,16 @@ def gpu_main(args, rank: int, world: int, local_rank: int):
         line["e2e"] = _e2e(reps, w, args.steps, dev, world)
     if not args.skip_prefill:
         line["prefill"] = _prefill(dev, tf_peak, tf_sus)
+    if not args.skip_c128a:
+        line["c128a_decode"] = _c128a_decode(dev, args, l2, hbm_peak, tf_peak, rank, world)
+        err_bits |= line["c128a_decode"]["device_error_bits"]
+    if not args.skip_mixed:
+        line["mixed_decode"] = _mixed_decode(dev, args, l2, hbm_peak, rank, world)
+        err_bits |= line["mixed_decode"]["device_error_bits"]
+    if not args.skip_aux:
+        line["compressor_aux"] = _compressor_aux(dev, hbm_peak)
+        err_bits |= line["compressor_aux"]["device_error_bits"]
+    line["device_error_bits"] = err_bits
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_subprocess(2, args.cpu_budget_s)
     if rank == 0:
@@ -527,7 +643,8 @@ def _per_call_times(reps, steps, stream, only=None):
     calls = {
         "compress_insert": lambda r: r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_),
         "index_topk": lambda r: r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk),
-        "attention": lambda r: r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out),
+        "attention": lambda r: r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q,
+                                               r.topk if r.lay.top_k else None, out=r.out),
         # the same attention with the fp8 output epilogue (e4m3 codes + per-row scales)
         "attention_q8": lambda r: r.lay.attention_q8(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk),
         # the insert with the per-head query RMSNorm in the same launch, and the norm alone
@@ -584,8 +701,9 @@ def _e2e(reps, w, steps, dev, world):
     replica. Inputs are double-buffered the way a serving engine overlaps the next batch's
     upload with the current batch: graph X computes on device buffers X while a copy stream
     uploads the next graph's inputs into buffers Y, and each step's read-back runs on a
-    second copy stream after its calls. Every step of the timed region thus pays one upload
-    and one read-back; the uploads for the first graph happen before the timed region."""
+    second copy stream after its calls. Every step of the timed region pays one upload (the
+    inputs of the same replica's next step) and one read-back; the uploads for the first
+    graph happen before the timed region."""
     import torch
     b, q = w.batch, w.queries
     bf = torch.bfloat16
@@ -653,8 +771,9 @@ def _e2e(reps, w, steps, dev, world):
     torch.cuda.synchronize()
     chains = [capture(0, full, full), capture(1, full, full)]
     n_chain, rem = steps // n, steps % n
-    # the last graph uploads only what a following graph would need (nothing after it)
-    tail = [capture(0, range(rem), []), capture(1, range(rem), [])] if rem else None
+    # the tail graph uploads the next inputs of its replicas too: every timed step pays one
+    # upload and one read-back
+    tail = [capture(0, range(rem), range(rem)), capture(1, range(rem), range(rem))] if rem else None
     for x in range(2):
         chains[x].replay()
     torch.cuda.synchronize()
@@ -671,7 +790,7 @@ def _e2e(reps, w, steps, dev, world):
     if not all(torch.equal(host_out[i], reps[i].out.cpu()) for i in last):
         raise SystemExit("e2e: the read-back output differs from the device output")
     ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
-    uploads = n_chain * n            # copies in the timed region, one per step on average
+    uploads = n_chain * n + rem      # copies in the timed region, one per step
     return {"value": whole_job_rate(B * steps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
             "uploads_in_timed_region": uploads, "read_backs_in_timed_region": steps,
@@ -679,6 +798,132 @@ def _e2e(reps, w, steps, dev, world):
                       "replicas on one device input set while a copy stream uploads the next "
                       "graph's inputs into the other; each step's read-back on a second copy "
                       "stream" % n}
+
+
+def _c128a_decode(dev, args, l2, hbm_peak, tf_peak, rank, world):
+    """Dense c128a decode, B=8 sequences of 2^20 context tokens: insert + attention over
+    every visible entry (8192) and the window, chained over rotating pool replicas like the
+    headline; the attention call alone per replica graph; rooflines for both bounds (the
+    workload sits at the ridge of HBM bandwidth and dense tensor throughput)."""
+    import torch
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+    w = wl.c128a_decode(seed=2 + 1000 * rank)
+    base = Layer.from_host(w.layers[0], dev)
+    nq = len(w.queries.pos)
+    L128 = int(w.queries.pos.max())
+    n_vis = (L128 - 128) // 128 + 1
+    per_q = c128a_bytes_per_query(n_vis, 128)
+    per_step = nq * per_q["total"]
+    n = n_replicas(per_step, l2, args.replicas)
+    reps = [DecodeReplica(base, w, dev, clone=i > 0) for i in range(n)]
+    stream = torch.cuda.current_stream()
+    ms = _max_over_ranks(chained_ms_per_step([r.step for r in reps], args.steps, args.warmup,
+                                             stream), world, dev)
+    ms_attn = _max_over_ranks(_per_call_times(reps, args.steps, stream, only=("attention",))
+                              ["attention"], world, dev)
+    attn_bytes = nq * (per_q["total"] - per_q["insert"])
+    flops = nq * attn_flops_per_query(n_vis + 128)
+    gbs = attn_bytes / (ms_attn / 1e3) / 1e9
+    tfs = flops / (ms_attn / 1e3) / 1e12
+    err = 0
+    for r in reps:
+        err |= int(r.err.item())
+    out = {"workload": "c128a dense decode B=%d L=%d: insert + attention over %d entries + %d "
+                       "window rows" % (nq, L128, n_vis, 128),
+           "value": whole_job_rate(nq, world, ms), "unit": UNIT, "ms_per_step": ms,
+           "bytes_per_step": per_step, "hbm_gbs": per_step / (ms / 1e3) / 1e9,
+           "hbm_frac": per_step / (ms / 1e3) / 1e9 / hbm_peak, "replicas": n,
+           "attention_ms": ms_attn,
+           "attention_roofline": {"kernel": "v4a_attn_decode, dense (attention + split merge)",
+                                  "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                  "unit": "GB/s", "frac": gbs / hbm_peak,
+                                  "algorithmic_bytes_per_launch": attn_bytes,
+                                  "tensor_tflops": tfs, "tensor_frac": tfs / tf_peak,
+                                  "flops_per_launch": flops},
+           "device_error_bits": err}
+    del reps
+    return out
+
+
+def _mixed_decode(dev, args, l2, hbm_peak, rank, world):
+    """Mixed variable-length decode: 64 sequences with log-uniform context lengths in
+    [4096, 2^20), one c4a layer (insert beside indexer + top-512, attention) and one c128a
+    layer (insert, dense attention) per step; bytes exact from the drawn lengths."""
+    import torch
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+    w = wl.mixed_decode(seed=4 + 1000 * rank)
+    lens = w.meta["lens"]
+    l4, l128 = (Layer.from_host(h, dev) for h in w.layers)
+    nb = mixed_bytes(lens)
+    n = n_replicas(nb["total"], l2, args.replicas)
+    reps = [(DecodeReplica(l4, w, dev, clone=i > 0, side=True),
+             DecodeReplica(l128, w, dev, clone=i > 0)) for i in range(n)]
+    stream = torch.cuda.current_stream()
+    both = [(lambda a=a, b=b: (a.step(), b.step())) for a, b in reps]
+    ms = _max_over_ranks(chained_ms_per_step(both, args.steps, args.warmup, stream), world, dev)
+    ms4 = _max_over_ranks(chained_ms_per_step([a.step for a, _ in reps], args.steps, args.warmup,
+                                              stream), world, dev)
+    ms128 = _max_over_ranks(chained_ms_per_step([b.step for _, b in reps], args.steps,
+                                                args.warmup, stream), world, dev)
+    nq = len(lens)
+    err = 0
+    for a, b in reps:
+        err |= int(a.err.item()) | int(b.err.item())
+    out = {"workload": "mixed decode B=%d, lengths log-uniform in [4096, 2^20) (min %d, max %d, "
+                       "mean %.0f): one c4a layer (top-512) + one c128a layer (dense), SWA 128"
+                       % (nq, min(lens), max(lens), float(np.mean(lens))),
+           "value": whole_job_rate(nq, world, ms), "unit": UNIT, "ms_per_step": ms,
+           "bytes_per_step": nb, "hbm_gbs": nb["total"] / (ms / 1e3) / 1e9,
+           "hbm_frac": nb["total"] / (ms / 1e3) / 1e9 / hbm_peak,
+           "c4a_layer": {"ms_per_step": ms4, "hbm_frac": nb["c4a_layer"] / (ms4 / 1e3) / 1e9 / hbm_peak},
+           "c128a_layer": {"ms_per_step": ms128,
+                           "hbm_frac": nb["c128a_layer"] / (ms128 / 1e3) / 1e9 / hbm_peak},
+           "replicas": n, "device_error_bits": err}
+    del reps
+    return out
+
+
+def _compressor_aux(dev, hbm_peak, reps=5):
+    """Auxiliary compressor batch: 32 sequences of 8192 new tokens each after 4096 cached
+    ones (same input distribution as the prefill chunk, seed 5), one insert call; bytes
+    from the per-token count (inputs larger than L2)."""
+    import torch
+    import workloads as wl
+    from compressed_sparse_long_gb300.layer import Layer
+    spec = wl.LayerSpec("c4a", True)
+    rng = np.random.default_rng(5)
+    ctx, new = [4096] * 32, [8192] * 32
+    bias, gamma, ibias = wl.layer_params(rng, spec)
+    h = wl.make_layer(rng, spec, ctx, new, prefill_cache=True)
+    h.bias, h.gamma, h.ibias = bias, gamma, ibias
+    b = wl.make_batch(rng, spec, ctx, new)
+    lay = Layer.from_host(h, dev)
+    bf = torch.bfloat16
+    cu, st = _dev(b.cu, torch.int32, dev), _dev(b.start, torch.int64, dev)
+    kv, sc, ik, is_ = (_dev(x, bf, dev) for x in (b.kv, b.s, b.ik, b.is_))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        lay.compress_insert(cu, st, kv, sc, ik, is_, dev_err=err)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        lay.compress_insert(cu, st, kv, sc, ik, is_, dev_err=err)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    tokens = int(sum(new))
+    nbytes = tokens * compress_bytes_per_token()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "auxiliary: 32 sequences x 8192 new tokens after 4096 cached (c4a, bf16 "
+                        "inputs, fp8 caches)", "ms": ms, "tokens_per_s": tokens / (ms / 1e3),
+            "roofline": {"kernel": "v4a_compress_insert", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "bytes_per_token": compress_bytes_per_token()},
+            "device_error_bits": int(err.item())}
 
 
 def _prefill(dev, tf_peak, tf_sus):
@@ -693,7 +938,8 @@ def _prefill(dev, tf_peak, tf_sus):
     torch.cuda.synchronize()
     reps = 3
     t = {}
-    for name in ("compress_insert", "index_topk", "attention"):
+    scores = None
+    for name in ("compress_insert", "index_topk", "index_scores", "attention"):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
@@ -701,23 +947,41 @@ def _prefill(dev, tf_peak, tf_sus):
                 r.lay.compress_insert(r.cu, r.start, r.kv, r.s, r.ik, r.is_)
             elif name == "index_topk":
                 r.lay.index_topk(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w, r.topk)
+            elif name == "index_scores":
+                scores = r.lay.index_scores(r.q_seq, r.q_pos, r.max_pos, r.q_idx, r.w)
             else:
                 r.lay.attention(r.q_seq, r.q_pos, r.max_pos, r.q, r.topk, out=r.out,
                                 prefill=True)
         e1.record()
         torch.cuda.synchronize()
         t[name] = e0.elapsed_time(e1) / reps
+    del scores
+    t["topk"] = t["index_topk"] - t["index_scores"]
     n_q = len(w.queries.pos)
     flops = n_q * attn_flops_per_query(512 + 128)
     pos = w.queries.pos
     idx_flops = float(sum(((p - 8) // 4 + 1) for p in pos)) * 2 * 64 * 128
-    tot = sum(t.values())
+    step = t["compress_insert"] + t["index_topk"] + t["attention"]
+    cbytes = n_q * compress_bytes_per_token()
+    cgbs = cbytes / (t["compress_insert"] / 1e3) / 1e9
     return {"workload": "c4a prefill: 122880 cached + 8192-token chunk",
             "attn_tflops": flops / (t["attention"] / 1e3) / 1e12,
             "attn_frac_of_bf16_peak": flops / (t["attention"] / 1e3) / 1e12 / tf_peak,
             "indexer_tflops": idx_flops / (t["index_topk"] / 1e3) / 1e12,
-            "tokens_per_s": n_q / (tot / 1e3), "ms": t,
-            "compress_tokens_per_s": n_q / (t["compress_insert"] / 1e3)}
+            "indexer_scores_tflops": idx_flops / (t["index_scores"] / 1e3) / 1e12,
+            "indexer_scores_frac_of_bf16_peak": idx_flops / (t["index_scores"] / 1e3) / 1e12 / tf_peak,
+            "tokens_per_s": n_q / (step / 1e3), "ms": t,
+            "ms_note": "topk = index_topk - index_scores (the call's selection kernel)",
+            "compress_tokens_per_s": n_q / (t["compress_insert"] / 1e3),
+            "compress_roofline": {"kernel": "v4a_compress_insert (8192-token chunk)",
+                                  "bound": "hbm", "achieved": cgbs, "peak": hbm_peak_of(),
+                                  "unit": "GB/s", "frac": cgbs / hbm_peak_of(),
+                                  "algorithmic_bytes_per_launch": cbytes,
+                                  "bytes_per_token": compress_bytes_per_token()}}
+
+
+def hbm_peak_of() -> float:
+    return peaks()[0]
 
 
 def main():
@@ -736,7 +1000,11 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0: enough to exceed 4x L2)")
-    ap.add_argument("--only", choices=["all", "prefill"], default="all")
+    ap.add_argument("--skip-c128a", action="store_true", dest="skip_c128a")
+    ap.add_argument("--skip-mixed", action="store_true", dest="skip_mixed")
+    ap.add_argument("--skip-aux", action="store_true", dest="skip_aux")
+    ap.add_argument("--only", choices=["all", "prefill", "c128a", "mixed", "compress"],
+                    default="all")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
