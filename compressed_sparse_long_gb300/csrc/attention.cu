@@ -238,9 +238,10 @@ __global__ void __launch_bounds__(kThreads) attn_simt(const __grid_constant__ At
 // lanes first reduce the split maxima and denominators (split s on lane s % 32), then lane
 // l owns the rotation pairs (d, d+1), d = 2l + 64i, of that head; all partial loads of a
 // group of splits are issued before they are used.
-// kNorm: the partials are o / l in bf16 (the tensor-core kernel's), else o in fp32; the
-// combine is sum_s w_s o_s / sum_s w_s l_s, with o_s = l_s * (o / l)_s in the first case.
-template <typename OT, int kPairs, bool kNorm = false>
+// The combine is sum_s w_s o_s / sum_s w_s l_s with w_s = 2^(m_s - max): o_s is the range's
+// unnormalised numerator in the scale its (m_s, l_s) state (kBf16: stored as bf16 pairs,
+// the tensor-core kernel's; else fp32).
+template <typename OT, int kPairs, bool kBf16 = false>
 __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnParams p) {
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -259,17 +260,17 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
   }
   // bf16 partials stay packed (one 32-bit word per pair) until they are used, which halves
   // the registers and lets more warps keep loads in flight
-  using VT = typename std::conditional<kNorm, uint32_t, float2>::type;
+  using VT = typename std::conditional<kBf16, uint32_t, float2>::type;
   VT v[4][kPairs];
   auto pair_of = [](const VT& x) -> float2 {
-    if constexpr (kNorm) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+    if constexpr (kBf16) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
     else return x;
   };
   auto load4 = [&](int s0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int s = s0 + u;
-      if constexpr (kNorm) {
+      if constexpr (kBf16) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(p.part_o) + ((row0 + (int64_t)s * H) * D >> 1);
 #pragma unroll
         for (int i = 0; i < kPairs; ++i) v[u][i] = s < p.n_split ? src[lane + 32 * i] : 0u;
@@ -302,13 +303,9 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int s = s0 + u;
-      float ms = -INFINITY, ls = 0.f;
-      if (s < p.n_split) {
-        ms = s < 32 ? __shfl_sync(0xffffffffu, m_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2];
-        if (kNorm) ls = s < 32 ? __shfl_sync(0xffffffffu, l_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2 + 1];
-      }
+      float ms = -INFINITY;
+      if (s < p.n_split) ms = s < 32 ? __shfl_sync(0xffffffffu, m_l, s) : p.part_ml[(row0 + (int64_t)s * H) * 2];
       wg[u] = (s < p.n_split && mx != -INFINITY && ms != -INFINITY) ? exp2f(ms - mx) : 0.f;
-      if (kNorm) wg[u] *= ls;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -384,10 +381,10 @@ int launch_attention(const AttnParams& p, int dtype, cudaStream_t st) {
     if (e == cudaSuccess && p.n_split > 1) {
       // A plain launch (full dependency on the attention kernel): launched early through
       // programmatic dependent launch, the merge's waiting CTAs held SMs during attention
-      // and the next kernels started later (decode step 49.2 -> 47.0 us without it).
+      // and the next kernels started later (decode step 49.2 -> 47.0 us without it); with
+      // the attention CTAs releasing it only as they leave, the step measured 3 us slower.
       attn_merge<__nv_bfloat16, 8, true><<<dim3((unsigned)p.n_q, (unsigned)((p.H + 7) / 8)), dim3(256), 0, st>>>(p);
       e = cudaGetLastError();
-      if (e == cudaSuccess) e = cudaGetLastError();
     }
   }
   else if (dtype == V4A_FP32 && p.H == 8 && p.D == 128)

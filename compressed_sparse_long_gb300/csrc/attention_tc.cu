@@ -33,8 +33,9 @@
 // with the odd tiles), 3 = warp 12 allocates TMEM, walks the items converged and issues
 // the MMAs from lane 0 (warps 13-15 idle).
 // Every hand-off is an mbarrier with a bounded wait (V4A_DEV_TIMEOUT on expiry).
-// Decode split: each key range's CTA writes its partial as o / l in bf16 plus (m, l) in
-// fp32; the merge kernel combines the ranges and applies R^-1.
+// Decode split: each key range's CTA writes its unnormalised numerator O^T in bf16 plus its
+// softmax state (m, l) in fp32, both in the scale of O^T; the merge kernel combines the
+// ranges and applies R^-1.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -335,19 +336,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     bool ok = true, waited = false;
     const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(p.attn.data);   // any valid address
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const Item I = make_item(p, it);
-      if (I.n_tiles == 0) continue;
-      // ---- Q~ of this item; the buffer is free once the previous item's S^T products are
-      if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      // the item's query rows are loaded first, before its position (and whether the item
+      // holds any key) is known: the two loads do not wait for one another
+      uint4 u[16];
       {
         const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                                        ((int64_t)I.qi * kH + 8 * cw) * kD) + 2 * lane;
-        uint4 u[16];
+                                                        ((int64_t)(it / p.n_split) * kH + 8 * cw) * kD) + 2 * lane;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           u[2 * i] = __ldg(q + i * (kD / 8));
           u[2 * i + 1] = __ldg(q + i * (kD / 8) + 1);
         }
+      }
+      const Item I = make_item(p, it);
+      if (I.n_tiles == 0) continue;
+      // ---- Q~ of this item; the buffer is free once the previous item's S^T products are
+      if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      {
         // RoPE of this lane's 8 dim pairs: lane i computes pair i, the tail lanes collect theirs
         const int tail0 = kD - p.rope.d_r;
         float c_l = 1.f, s_l = 0.f;
@@ -697,19 +702,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         if (row < 64) {
           const float4 v = *reinterpret_cast<const float4*>(red_sum + row * 4);
           l_own = (v.x + v.y) + (v.z + v.w);
-          l_fin[(ni & 1) * 64 + row] = l_own > 0.f ? pow2i(-A) / l_own : 0.f;
+          if (!kSplit) l_fin[(ni & 1) * 64 + row] = l_own > 0.f ? pow2i(-A) / l_own : 0.f;
         }
       }
       const float m_final = quad == 0 ? mc0 : mc1;   // used by the owners (row < 64)
-      if (!group_sync()) { ok = false; break; }
+      if (!kSplit && !group_sync()) { ok = false; break; }
       const float* linv = l_fin + (ni & 1) * 64;
       if (!tc::mbar_wait(ofull, ni & 1, abort_flag, p.err)) { ok = false; break; }
       tc::fence_after_sync();
       const bool even = (lane & 1) == 0;
       if (kSplit) {
-        // partial o / l in bf16 (the range's max and denominator go out in fp32): lanes 2i
-        // and 2i+1 hold dims d, d+1; for heads (h, h+1) the even lane stores head h's pair
-        // and the odd lane head h+1's, one 32-bit store each
+        // the range's unnormalised numerator O^T in bf16, with its state (m - A, l 2^A) in
+        // fp32 (O^T carries the factor 2^A of P'): lanes 2i and 2i+1 hold dims d, d+1; for
+        // heads (h, h+1) the even lane stores head h's pair and the odd lane head h+1's, one
+        // 32-bit store each
         const int64_t base = ((int64_t)I.qi * p.n_split + I.split) * kH;
         uint32_t* part = reinterpret_cast<uint32_t*>(p.part_o);
         for (int b = 0; b < 4; ++b) {
@@ -724,18 +730,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
 #pragma unroll
             for (int h = 0; h < 32; h += 2) {
               const int hh = half * 32 + h;
-              const float2 li = *reinterpret_cast<const float2*>(linv + hh);
-              const float a = o[h] * li.x, bb = o[h + 1] * li.y;
-              const float recv = __shfl_xor_sync(0xffffffffu, even ? bb : a, 1);
-              const uint32_t w = even ? pack_bf16(a, recv) : pack_bf16(recv, bb);
+              const float recv = __shfl_xor_sync(0xffffffffu, even ? o[h + 1] : o[h], 1);
+              const uint32_t w = even ? pack_bf16(o[h], recv) : pack_bf16(recv, o[h + 1]);
               const int head = even ? hh : hh + 1, d0 = even ? d : d - 1;
               part[((base + head) * kD + d0) >> 1] = w;
             }
           }
         }
         if (row < 64) {
-          p.part_ml[(base + row) * 2] = m_final;
-          p.part_ml[(base + row) * 2 + 1] = l_own;
+          p.part_ml[(base + row) * 2] = m_final - (float)A;
+          p.part_ml[(base + row) * 2 + 1] = l_own * pow2i(A);
         }
       } else {
         // out = R^-1 (o / l) in bf16: the same pairing, the even lane rotating head h's pair

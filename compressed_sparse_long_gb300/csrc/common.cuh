@@ -26,10 +26,12 @@ struct CacheView {
   int32_t max_blocks;
   int32_t R;
   int32_t width;
+  int32_t shift;     // log2(R) when R is a power of two (every layer pool), else -1
 };
 
 inline CacheView view_of(const v4a_cache* c) {
   CacheView v{};
+  v.shift = -1;
   if (c) {
     v.data = c->data;
     v.scale = c->scale;
@@ -38,6 +40,8 @@ inline CacheView view_of(const v4a_cache* c) {
     v.max_blocks = c->max_blocks;
     v.R = c->rows_per_block;
     v.width = c->row_width;
+    if (v.R > 0 && (v.R & (v.R - 1)) == 0)
+      for (v.shift = 0; (1 << v.shift) < v.R; ++v.shift) {}
   }
   return v;
 }
@@ -46,12 +50,13 @@ inline CacheView view_of(const v4a_cache* c) {
 // page (or r is out of the table), -2 if the page id is outside the pool.
 __device__ __forceinline__ int64_t slot_of(const CacheView& c, int seq, int64_t r) {
   if (r < 0) return -1;
-  int64_t blk = r / c.R;
+  const int64_t blk = c.shift >= 0 ? r >> c.shift : r / c.R;
   if (blk >= c.max_blocks) return -1;
   int32_t page = __ldg(c.bt + (int64_t)seq * c.max_blocks + blk);
   if (page < 0) return -1;
   if (page >= c.n_pages) return -2;
-  return (int64_t)page * c.R + (r % c.R);
+  const int64_t off = c.shift >= 0 ? (r & (int64_t)(c.R - 1)) : r % c.R;
+  return (int64_t)page * c.R + off;
 }
 
 __device__ __forceinline__ void raise_err(int32_t* err, uint32_t bits) {

@@ -18,26 +18,21 @@
 // entries and is re-read from L2 by the neighbouring warp. The kernel is HBM-bound.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace v4a {
 
 namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 struct CompressKernel {
   static constexpr int D = CPL * 32;
   static constexpr int DI = ICPL * 32;
 
-  struct Row {
-    const TIn* kv;
-    const TIn* s;
-    const TIn* ik;
-    const TIn* is;
-    bool ok;
-  };
-
   // fp8 row store: per-row scale amax/448 (1 if the row is zero), e4m3 RNE satfinite of
-  // y/scale; fp32 rows are stored as they are.
+  // y * (1/scale) in fp32; fp32 rows are stored as they are.
   template <int N>
   static __device__ __forceinline__ void store_row(const CacheView& c, int64_t slot, float (&y)[N],
                                                    int lane) {
@@ -47,13 +42,16 @@ struct CompressKernel {
       for (int k = 0; k < N; ++k) amax = fmaxf(amax, fabsf(y[k]));
       amax = warp_max(amax);
       float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+      // y / scale as y * (1 / scale): two fp32 roundings (a relative error below 2^-23),
+      // against one per element for a division
+      const float inv = __frcp_rn(scale);
       uint8_t* dst = reinterpret_cast<uint8_t*>(c.data) + slot * (int64_t)c.width + lane * N;
       if constexpr (N % 4 == 0) {
         uint32_t words[N / 4];
 #pragma unroll
         for (int k = 0; k < N / 4; ++k) {
-          uint32_t lo = e4m3x2_encode(__fdiv_rn(y[4 * k], scale), __fdiv_rn(y[4 * k + 1], scale));
-          uint32_t hi = e4m3x2_encode(__fdiv_rn(y[4 * k + 2], scale), __fdiv_rn(y[4 * k + 3], scale));
+          uint32_t lo = e4m3x2_encode(y[4 * k] * inv, y[4 * k + 1] * inv);
+          uint32_t hi = e4m3x2_encode(y[4 * k + 2] * inv, y[4 * k + 3] * inv);
           words[k] = lo | (hi << 16);
         }
         if constexpr (N == 16) {
@@ -66,10 +64,7 @@ struct CompressKernel {
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float v = __fdiv_rn(y[k], scale);
-          dst[k] = (uint8_t)(e4m3x2_encode(v, 0.f) & 0xFF);
-        }
+        for (int k = 0; k < N; ++k) dst[k] = (uint8_t)(e4m3x2_encode(y[k] * inv, 0.f) & 0xFF);
       }
       if (lane == 0) c.scale[slot] = scale;
     } else {
@@ -90,26 +85,32 @@ struct CompressKernel {
     for (int k = 0; k < N; ++k) amax = fmaxf(amax, fabsf(y[k]));
     amax = warp_max(amax);
     const float scale = amax > 0.f ? __fdiv_rn(amax, kE2m1Max) : 1.0f;
+    const float inv = __frcp_rn(scale);
     uint32_t packed = 0;
 #pragma unroll
-    for (int k = 0; k < N; ++k) packed |= e2m1_encode(__fdiv_rn(y[k], scale)) << (4 * k);
+    for (int k = 0; k < N; ++k) packed |= e2m1_encode(y[k] * inv) << (4 * k);
     uint8_t* dst = reinterpret_cast<uint8_t*>(c.data) + slot * (int64_t)c.width + lane * (N / 2);
     *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
     if (lane == 0) c.scale[slot] = scale;
   }
 
-  // Rotate the lane's channels that fall in the rotated tail (adjacent pairs).
+  // Rotate the lane's channels that fall in the rotated tail (adjacent pairs). Lane i
+  // evaluates the angle of pair i (d_r / 2 <= 32 pairs) and the lanes owning the tail take
+  // theirs by shuffle, so the warp evaluates each angle once and in parallel.
   template <int N>
   static __device__ __forceinline__ void rope_lane(const Rope& rp, float (&y)[N], int lane,
                                                    int64_t pos) {
     const int tail0 = rp.D - rp.d_r;
+    float c_l = 1.f, s_l = 0.f;
+    if (lane < (rp.d_r >> 1)) rope_cs(rp, pos, lane, c_l, s_l);
 #pragma unroll
     for (int k = 0; k < N; k += 2) {
-      int d = lane * N + k;
+      const int d = lane * N + k;
+      const int pi = (d - tail0) >> 1;
+      const float c = __shfl_sync(0xffffffffu, c_l, pi & 31);
+      const float s = __shfl_sync(0xffffffffu, s_l, pi & 31);
       if (d >= tail0) {
-        float c, s;
-        rope_cs(rp, pos, (d - tail0) >> 1, c, s);
-        float a = y[k], b = y[k + 1];
+        const float a = y[k], b = y[k + 1];
         y[k] = a * c - b * s;
         y[k + 1] = a * s + b * c;
       }
@@ -132,6 +133,125 @@ struct CompressKernel {
     for (int k = 0; k < CPL; ++k) x[k] = x[k] * inv * g[k];
     pdl_wait();   // q_out may still be read by the kernel before this one
     store_f<TIn, CPL>(reinterpret_cast<TIn*>(p.q_out) + r * D + lane * CPL, x);
+  }
+
+  // Pointers to the four parts of one window token's row (inputs, residual pool or a
+  // staged copy in shared memory: the loads go through generic addresses).
+  struct WindowRow {
+    const TIn* kv;
+    const TIn* s;
+    const TIn* ik;
+    const TIn* is;
+  };
+
+  template <typename T, int N>
+  static __device__ __forceinline__ void load_g(const T* __restrict__ ptr, float (&out)[N]) {
+    constexpr int kBytes = N * (int)sizeof(T);
+    if constexpr (kBytes % 16 == 0) {
+      constexpr int kPer = 16 / sizeof(T);
+#pragma unroll
+      for (int v = 0; v < kBytes / 16; ++v) {
+        const uint4 u = reinterpret_cast<const uint4*>(ptr)[v];
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) out[v * kPer + k] = Elem<T>::to_f(e[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < N; ++k) out[k] = Elem<T>::to_f(ptr[k]);
+    }
+  }
+
+  // Weighted sum of one window with per-channel softmax weights, as the pages' compressor
+  // defines it: z_o = s_o + bias[o], w_o = exp(z_o - max_o z_o) / sum_o exp(z_o - max_o z_o),
+  // c = sum_o w_o kv_o (max first, then the exponentials, tokens in window order; the
+  // exponentials in base 2 of z log2(e)). N
+  // channels per lane; fetch(o, row) fills token o's row pointers and returns its status
+  // (1 present, 0 absent: a position before the sequence, -1 / -2 a residual row without a
+  // page or with a page outside the pool); kIdx selects the (ik, is) halves instead of
+  // (kv, s). Returns false, after raising the error bit, if a row is missing (the caller
+  // skips the entry).
+  template <int N, bool kIdx, class Fetch>
+  static __device__ __forceinline__ bool window_sum(const CompressParams& p, int lane,
+                                                    const Fetch& fetch, float (&c)[N]) {
+    const int width = kIdx ? DI : D;
+    const float* bias = kIdx ? p.ibias : p.bias;
+    float m[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) m[k] = -INFINITY;
+#pragma unroll 4
+    for (int o = 0; o < p.W; ++o) {
+      WindowRow w;
+      const int st = fetch(o, w);
+      if (st == 0) continue;
+      if (st < 0) {
+        raise_err(p.err, st == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+        return false;
+      }
+      float sv[N], bv[N];
+      load_g<TIn, N>((kIdx ? w.is : w.s) + lane * N, sv);
+      load_f<float, N>(bias + (int64_t)o * width + lane * N, bv);
+#pragma unroll
+      for (int k = 0; k < N; ++k) m[k] = fmaxf(m[k], (sv[k] + bv[k]) * kLog2e);
+    }
+    float l[N], acc[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) { l[k] = 0.f; acc[k] = 0.f; }
+#pragma unroll 4
+    for (int o = 0; o < p.W; ++o) {
+      WindowRow w;
+      if (fetch(o, w) <= 0) continue;
+      float sv[N], bv[N], xv[N];
+      load_g<TIn, N>((kIdx ? w.is : w.s) + lane * N, sv);
+      load_g<TIn, N>((kIdx ? w.ik : w.kv) + lane * N, xv);
+      load_f<float, N>(bias + (int64_t)o * width + lane * N, bv);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float e = exp2f((sv[k] + bv[k]) * kLog2e - m[k]);
+        l[k] += e;
+        acc[k] = fmaf(e, xv[k], acc[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < N; ++k) c[k] = __fdiv_rn(acc[k], l[k]);
+    return true;
+  }
+
+  // Entry j of sequence b: attention row RoPE(gamma * c / rms(c), S*j) and, for c4a, the
+  // indexer row (no norm, no RoPE), each quantised and stored at its slot. Both insert
+  // kernels build entries here, so they write identical bytes.
+  template <class Fetch>
+  static __device__ void build_entry(const CompressParams& p, int b, int64_t j, int lane,
+                                     const Fetch& fetch) {
+    const int64_t e_slot = slot_of(p.attn, b, j);
+    const int64_t i_slot = ICPL > 0 ? slot_of(p.idx, b, j) : -1;
+    if (e_slot == -2 || i_slot == -2) raise_err(p.err, V4A_DEV_BAD_PAGE);
+    if (e_slot >= 0) {
+      float c[CPL], g[CPL];
+      if (!window_sum<CPL, false>(p, lane, fetch, c)) return;
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) ss = fmaf(c[k], c[k], ss);
+      ss = warp_sum(ss);
+      const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)D) + p.eps));
+      load_f<float, CPL>(p.gamma + lane * CPL, g);
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) c[k] = c[k] * inv * g[k];
+      rope_lane<CPL>(p.rope, c, lane, j * p.S);
+      store_row<CPL>(p.attn, e_slot, c, lane);
+    }
+    if constexpr (ICPL > 0) {
+      if (i_slot >= 0) {
+        float c[ICPL];
+        if (!window_sum<ICPL, true>(p, lane, fetch, c)) return;
+        if constexpr (kFp8 && ICPL == 4) {
+          if (p.idx_fp4) store_row_fp4<ICPL>(p.idx, i_slot, c, lane);
+          else store_row<ICPL>(p.idx, i_slot, c, lane);
+        } else {
+          store_row<ICPL>(p.idx, i_slot, c, lane);
+        }
+      }
+    }
   }
 
   static __device__ void run(const CompressParams& p) {
@@ -218,110 +338,308 @@ struct CompressKernel {
       }
     }
 
-    // (3) entry j whose window ends at t
+    // (3) entry j whose window ends at t: window token o at position S*j + win_off + o is a
+    // row of this call's inputs (position >= P0) or of the residual pool (before P0)
     const int64_t first = t - p.win_off - (p.W - 1);   // = S*j
     if (first < 0 || first % p.S != 0) return;
     const int64_t j = first / p.S;
-    const int64_t e_slot = slot_of(p.attn, b, j);
-    const int64_t i_slot = ICPL > 0 ? slot_of(p.idx, b, j) : -1;
-    if (e_slot == -2 || i_slot == -2) raise_err(p.err, V4A_DEV_BAD_PAGE);
-    if (e_slot < 0 && i_slot < 0) return;
-
-    // online per-channel softmax over the window's present tokens
-    float m[CPL], l[CPL], acc[CPL];
-    float im[ICPL > 0 ? ICPL : 1], il[ICPL > 0 ? ICPL : 1], iacc[ICPL > 0 ? ICPL : 1];
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) { m[k] = -INFINITY; l[k] = 0.f; acc[k] = 0.f; }
-#pragma unroll
-    for (int k = 0; k < (ICPL > 0 ? ICPL : 1); ++k) { im[k] = -INFINITY; il[k] = 0.f; iacc[k] = 0.f; }
-
-#pragma unroll 8
-    for (int o = 0; o < p.W; ++o) {
+    const TIn* kv_in = reinterpret_cast<const TIn*>(p.kv);
+    const TIn* s_in = reinterpret_cast<const TIn*>(p.score);
+    const TIn* ik_in = reinterpret_cast<const TIn*>(p.ikv);
+    const TIn* is_in = reinterpret_cast<const TIn*>(p.iscore);
+    build_entry(p, b, j, lane, [&](int o, WindowRow& w) -> int {
       const int64_t pos = j * p.S + p.win_off + o;
-      if (pos < 0) continue;                       // before the sequence: absent
-      const TIn *kvp, *sp, *ikp = nullptr, *isp = nullptr;
+      if (pos < 0) return 0;                       // before the sequence: absent
       if (pos >= P0) {
         const int64_t r = row0 + (pos - P0);
-        kvp = reinterpret_cast<const TIn*>(p.kv) + r * D;
-        sp = reinterpret_cast<const TIn*>(p.score) + r * D;
+        w.kv = kv_in + r * D;
+        w.s = s_in + r * D;
         if constexpr (ICPL > 0) {
-          ikp = reinterpret_cast<const TIn*>(p.ikv) + r * DI;
-          isp = reinterpret_cast<const TIn*>(p.iscore) + r * DI;
+          w.ik = ik_in + r * DI;
+          w.is = is_in + r * DI;
         }
-      } else {
-        const int64_t s = slot_of(p.state, b, pos);
-        if (!slot_ok(s, p.err)) return;            // residual row missing: skip the entry
-        const TIn* base = reinterpret_cast<const TIn*>(p.state.data) + s * (int64_t)p.state.width;
-        kvp = base;
-        sp = base + D;
-        if constexpr (ICPL > 0) {
-          ikp = base + 2 * D;
-          isp = base + 2 * D + DI;
-        }
+        return 1;
       }
-      float kvv[CPL], sv[CPL], bv[CPL];
-      load_f<TIn, CPL>(kvp + lane * CPL, kvv);
-      load_f<TIn, CPL>(sp + lane * CPL, sv);
-      load_f<float, CPL>(p.bias + (int64_t)o * D + lane * CPL, bv);
-#pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        float z = sv[k] + bv[k];
-        float mn = fmaxf(m[k], z);
-        float corr = expf(m[k] - mn);
-        float e = expf(z - mn);
-        l[k] = l[k] * corr + e;
-        acc[k] = acc[k] * corr + e * kvv[k];
-        m[k] = mn;
-      }
+      const int64_t sl = slot_of(p.state, b, pos);
+      if (sl < 0) return (int)sl;                  // -1: no page, -2: page outside the pool
+      const TIn* base = reinterpret_cast<const TIn*>(p.state.data) + sl * (int64_t)p.state.width;
+      w.kv = base;
+      w.s = base + D;
       if constexpr (ICPL > 0) {
-        float a[ICPL], sc[ICPL], bb[ICPL];
-        load_f<TIn, ICPL>(ikp + lane * ICPL, a);
-        load_f<TIn, ICPL>(isp + lane * ICPL, sc);
-        load_f<float, ICPL>(p.ibias + (int64_t)o * DI + lane * ICPL, bb);
-#pragma unroll
-        for (int k = 0; k < ICPL; ++k) {
-          float z = sc[k] + bb[k];
-          float mn = fmaxf(im[k], z);
-          float corr = expf(im[k] - mn);
-          float e = expf(z - mn);
-          il[k] = il[k] * corr + e;
-          iacc[k] = iacc[k] * corr + e * a[k];
-          im[k] = mn;
-        }
+        w.ik = base + 2 * D;
+        w.is = base + 2 * D + DI;
       }
-    }
+      return 1;
+    });
+  }
+};
 
-    if (e_slot >= 0) {
-      float c[CPL], g[CPL];
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        c[k] = __fdiv_rn(acc[k], l[k]);
-        ss = fmaf(c[k], c[k], ss);
-      }
-      ss = warp_sum(ss);
-      const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)D) + p.eps));
-      load_f<float, CPL>(p.gamma + lane * CPL, g);
-#pragma unroll
-      for (int k = 0; k < CPL; ++k) c[k] = c[k] * inv * g[k];
-      rope_lane<CPL>(p.rope, c, lane, j * p.S);
-      store_row<CPL>(p.attn, e_slot, c, lane);
+// Large calls (many new tokens per sequence, windows of at most 8 tokens): one persistent
+// CTA per SM walks tiles of kTT consecutive new tokens of one sequence. A tile's rows and the
+// W - 1 window tokens before them are staged in shared memory by bulk copies (a tile's input
+// rows are contiguous in kv, s, ik and is: one copy per array; rows before the call's first
+// position come from the residual pool, one copy per part of the row), double-buffered so
+// the next tile streams in while this one is computed. Every row is read from memory once
+// per tile (the window overlap between tiles, W - 1 rows, is read twice). The window rows,
+// residual rows and entries are then computed from shared memory: warp w takes tokens
+// w, w + 8, ... and entries w, w + 8, ... of the tile, with the same entry routine as the
+// warp-per-token kernel, so both write identical bytes.
+template <typename TIn, int CPL, int ICPL, bool kFp8>
+struct CompressTile {
+  using K = CompressKernel<TIn, CPL, ICPL, kFp8>;
+  using WindowRow = typename K::WindowRow;
+  static constexpr int D = CPL * 32, DI = ICPL * 32;
+  static constexpr int kTT = 32;                    // new tokens per tile
+  static constexpr int kMaxW = 8;                   // window tokens the staging holds
+  static constexpr int kRows = kTT + kMaxW - 1;     // staged rows
+  static constexpr int kWarps = 8, kThreads = kWarps * 32;
+  static constexpr int kMaxSeq = 1023;              // sequences of a call on this path (the
+                                                    // 256 threads write prefix[0 .. kMaxSeq])
+  static constexpr int kRowBytes = (2 * D + 2 * DI) * (int)sizeof(TIn);
+  // one stage: kv, s [kRows][D] and ik, is [kRows][DI] (input type), row status [kRows]
+  static constexpr int kKv = kRows * D * (int)sizeof(TIn);
+  static constexpr int kIk = kRows * DI * (int)sizeof(TIn);
+  static constexpr int kOffS = kKv, kOffIk = 2 * kKv, kOffIs = 2 * kKv + kIk;
+  static constexpr int kOffSt = 2 * kKv + 2 * kIk;
+  static constexpr int kStage = (kOffSt + kRows * 4 + 127) / 128 * 128;
+  static constexpr int kOffPrefix = 2 * kStage;     // int32 [kMaxSeq + 1] tiles before sequence b
+  static constexpr int kOffBar = (kOffPrefix + (kMaxSeq + 1) * 4 + 7) / 8 * 8;
+  static constexpr int kOffMisc = kOffBar + 2 * 8;
+  static constexpr int kSmem = kOffMisc + 16 + 128;   // + alignment slack
+  static constexpr bool kFits = kSmem <= 227 * 1024;   // fp32 rows of 512 do not fit
+
+  struct Tile {
+    int b;
+    int64_t r0, n, pa, P0, P1;   // input rows [r0, r0 + n) at positions pa .. pa + n - 1
+  };
+
+  static __device__ __forceinline__ bool tile_of(const CompressParams& p, const int* prefix, int k,
+                                                 Tile& t) {
+    if (k >= prefix[p.n_seq]) return false;
+    int lo = 0, hi = p.n_seq - 1;                   // largest b with prefix[b] <= k
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= k) lo = mid;
+      else hi = mid - 1;
     }
-    if constexpr (ICPL > 0) {
-      if (i_slot >= 0) {
-        float c[ICPL];
-#pragma unroll
-        for (int k = 0; k < ICPL; ++k) c[k] = __fdiv_rn(iacc[k], il[k]);
-        if constexpr (kFp8 && ICPL == 4) {
-          if (p.idx_fp4) store_row_fp4<ICPL>(p.idx, i_slot, c, lane);
-          else store_row<ICPL>(p.idx, i_slot, c, lane);
-        } else {
-          store_row<ICPL>(p.idx, i_slot, c, lane);
-        }
+    const int64_t c = k - prefix[lo];
+    const int64_t cu0 = __ldg(p.cu + lo), cu1 = __ldg(p.cu + lo + 1);
+    t.b = lo;
+    t.P0 = __ldg(p.start + lo);
+    t.P1 = t.P0 + (cu1 - cu0);
+    t.r0 = cu0 + c * kTT;
+    t.n = min((int64_t)kTT, cu1 - t.r0);
+    t.pa = t.P0 + c * kTT;
+    return true;
+  }
+
+  // Warp 0: stage tile t (its rows and the W - 1 window tokens before them). Row status:
+  // 1 staged, 0 a position before the sequence (absent), -1 / -2 a residual row without a
+  // page or with a page outside the pool.
+  static __device__ void issue(const CompressParams& p, const Tile& t, uint8_t* st, uint64_t* bar,
+                               int lane) {
+    const int W = p.W;
+    const int64_t base = t.pa - (W - 1);
+    const int n_rows = (int)t.n + W - 1;
+    int* status = reinterpret_cast<int*>(st + kOffSt);
+    const int64_t q_in = max(base, t.P0);          // first position read from the inputs
+    const int k_in = (int)(q_in - base);           // < W: rows before it are residual rows
+    const int n_in = n_rows - k_in;
+    const int64_t r_in = t.r0 - (t.pa - q_in);
+    int64_t slot = -1;
+    int stt = 0;
+    if (lane < k_in) {
+      const int64_t q = base + lane;
+      if (q >= 0) {
+        slot = slot_of(p.state, t.b, q);
+        stt = slot >= 0 ? 1 : (int)slot;
+      }
+      status[lane] = stt;
+    }
+    for (int k = k_in + lane; k < n_rows; k += 32) status[k] = 1;
+    const uint32_t n_state = __popc(__ballot_sync(0xffffffffu, stt > 0));
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive_tx(bar, (uint32_t)(n_in + n_state) * kRowBytes);
+    __syncwarp();
+    constexpr int es = (int)sizeof(TIn);
+    if (lane == 0) {
+      tc::bulk_g2s(st + (size_t)k_in * D * es, reinterpret_cast<const TIn*>(p.kv) + r_in * D,
+                   (uint32_t)(n_in * D * es), bar);
+      tc::bulk_g2s(st + kOffS + (size_t)k_in * D * es, reinterpret_cast<const TIn*>(p.score) + r_in * D,
+                   (uint32_t)(n_in * D * es), bar);
+      if constexpr (ICPL > 0) {
+        tc::bulk_g2s(st + kOffIk + (size_t)k_in * DI * es, reinterpret_cast<const TIn*>(p.ikv) + r_in * DI,
+                     (uint32_t)(n_in * DI * es), bar);
+        tc::bulk_g2s(st + kOffIs + (size_t)k_in * DI * es,
+                     reinterpret_cast<const TIn*>(p.iscore) + r_in * DI, (uint32_t)(n_in * DI * es), bar);
+      }
+    }
+    if (stt > 0) {
+      const TIn* row = reinterpret_cast<const TIn*>(p.state.data) + slot * (int64_t)p.state.width;
+      tc::bulk_g2s(st + (size_t)lane * D * es, row, (uint32_t)(D * es), bar);
+      tc::bulk_g2s(st + kOffS + (size_t)lane * D * es, row + D, (uint32_t)(D * es), bar);
+      if constexpr (ICPL > 0) {
+        tc::bulk_g2s(st + kOffIk + (size_t)lane * DI * es, row + 2 * D, (uint32_t)(DI * es), bar);
+        tc::bulk_g2s(st + kOffIs + (size_t)lane * DI * es, row + 2 * D + DI, (uint32_t)(DI * es), bar);
       }
     }
   }
+
+  // All warps: the window and residual rows of the tile's tokens, then its entries.
+  static __device__ void compute(const CompressParams& p, const Tile& t, const uint8_t* st, int warp,
+                                 int lane) {
+    const int W = p.W, S = p.S;
+    const TIn* kv_s = reinterpret_cast<const TIn*>(st);
+    const TIn* s_s = reinterpret_cast<const TIn*>(st + kOffS);
+    const TIn* ik_s = reinterpret_cast<const TIn*>(st + kOffIk);
+    const TIn* is_s = reinterpret_cast<const TIn*>(st + kOffIs);
+    const int* status = reinterpret_cast<const int*>(st + kOffSt);
+    for (int i = warp; i < t.n; i += kWarps) {
+      const int64_t pos = t.pa + i;
+      const int k = i + W - 1;
+      const int64_t sw = slot_of(p.swa, t.b, pos);
+      if (sw >= 0) {
+        float y[CPL];
+        K::template load_g<TIn, CPL>(kv_s + k * D + lane * CPL, y);
+        K::template rope_lane<CPL>(p.rope, y, lane, pos);
+        K::template store_row<CPL>(p.swa, sw, y, lane);
+      } else if (sw == -2) {
+        raise_err(p.err, V4A_DEV_BAD_PAGE);
+      }
+      if (pos >= t.P1 - W) {                       // raw residual row for the last W positions
+        const int64_t ss = slot_of(p.state, t.b, pos);
+        if (ss >= 0) {
+          TIn* dst = reinterpret_cast<TIn*>(p.state.data) + ss * (int64_t)p.state.width;
+          constexpr int kV = CPL * (int)sizeof(TIn) / 16;   // 16-byte vectors per lane
+          static_assert(CPL * sizeof(TIn) % 16 == 0, "whole vectors per lane");
+#pragma unroll
+          for (int v = 0; v < kV; ++v) {
+            reinterpret_cast<uint4*>(dst + lane * CPL)[v] =
+                reinterpret_cast<const uint4*>(kv_s + k * D + lane * CPL)[v];
+            reinterpret_cast<uint4*>(dst + D + lane * CPL)[v] =
+                reinterpret_cast<const uint4*>(s_s + k * D + lane * CPL)[v];
+          }
+          if constexpr (ICPL > 0) {
+#pragma unroll
+            for (int e = 0; e < ICPL; ++e) {
+              dst[2 * D + lane * ICPL + e] = ik_s[k * DI + lane * ICPL + e];
+              dst[2 * D + DI + lane * ICPL + e] = is_s[k * DI + lane * ICPL + e];
+            }
+          }
+        } else if (ss == -2) {
+          raise_err(p.err, V4A_DEV_BAD_PAGE);
+        }
+      }
+    }
+    // entries completed by the tile's tokens: position tt completes entry (tt - c0) / S
+    const int64_t c0 = p.win_off + W - 1;
+    int64_t tt0 = max(t.pa, c0);
+    tt0 += (S - (tt0 - c0) % S) % S;
+    for (int64_t tt = tt0 + (int64_t)warp * S; tt < t.pa + t.n; tt += (int64_t)kWarps * S) {
+      const int64_t j = (tt - c0) / S;
+      const int ko = (int)(tt - t.pa);            // staged row of the window's first token
+      K::build_entry(p, t.b, j, lane, [&](int o, WindowRow& w) -> int {
+        const int k = ko + o;
+        const int sk = status[k];
+        if (sk <= 0) return sk;
+        w.kv = kv_s + k * D;
+        w.s = s_s + k * D;
+        if constexpr (ICPL > 0) {
+          w.ik = ik_s + k * DI;
+          w.is = is_s + k * DI;
+        }
+        return 1;
+      });
+    }
+  }
+
+  static __device__ void run(const CompressParams& p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = tc::smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
+    int* prefix = reinterpret_cast<int*>(sm + kOffPrefix);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    volatile int* abort_flag = reinterpret_cast<int*>(sm + kOffMisc);
+    __shared__ int warp_tot[kWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+      tc::mbar_init(full, 1);
+      tc::mbar_init(full + 1, 1);
+      *abort_flag = 0;
+      tc::fence_mbar_init();
+    }
+    // tiles before each sequence: thread tid counts sequences 4 tid .. 4 tid + 3 (inputs
+    // only, before waiting for the previous kernel)
+    int cnt[4], sum = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b = 4 * tid + u;
+      cnt[u] = 0;
+      if (b < p.n_seq) {
+        const int64_t n = (int64_t)__ldg(p.cu + b + 1) - __ldg(p.cu + b);
+        cnt[u] = n > 0 ? (int)((n + kTT - 1) / kTT) : 0;
+      }
+      sum += cnt[u];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) before += w < warp ? warp_tot[w] : 0;
+    int run_sum = before + incl - sum;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b = 4 * tid + u;
+      if (b <= p.n_seq) prefix[b] = run_sum;      // prefix[n_seq] is the total
+      run_sum += cnt[u];
+    }
+    __syncthreads();
+    const int total = prefix[p.n_seq];
+    pdl_wait();   // residual rows may come from the previous kernel; every pool write waits
+
+    Tile t;
+    if (warp == 0) {
+      for (int i = 0; i < 2; ++i) {
+        const int k = blockIdx.x + i * gridDim.x;
+        if (tile_of(p, prefix, k, t)) issue(p, t, sm + i * kStage, full + i, lane);
+      }
+    }
+    int i = 0;
+    bool ok = true;
+    for (int k = blockIdx.x; k < total; k += gridDim.x, ++i) {
+      tile_of(p, prefix, k, t);
+      // every thread takes the same decision, so the block barriers below always pair up
+      const bool got = tc::mbar_wait(full + (i & 1), (i >> 1) & 1, abort_flag, p.err);
+      if (!__syncthreads_and(got)) { ok = false; break; }
+      compute(p, t, sm + (i & 1) * kStage, warp, lane);
+      __syncthreads();                             // every warp is done with the stage
+      if (warp == 0) {
+        const int k2 = k + 2 * gridDim.x;
+        tc::fence_proxy_async();                  // reads of the stage before the next copy
+        if (tile_of(p, prefix, k2, t)) issue(p, t, sm + (i & 1) * kStage, full + (i & 1), lane);
+      }
+    }
+    if (!ok && tid == 0) {                         // copies still in flight land before exit
+      for (int u = 0; u < 2; ++u) {
+        const int k = blockIdx.x + (i + u) * gridDim.x;
+        if (k < total) tc::mbar_wait_drain(full + ((i + u) & 1), ((i + u) >> 1) & 1);
+      }
+    }
+    __syncthreads();
+  }
 };
+
+template <typename TIn, int CPL, int ICPL, bool kFp8>
+__global__ void __launch_bounds__(256, 1) compress_tile_kernel(const __grid_constant__ CompressParams p) {
+  pdl_trigger();
+  CompressTile<TIn, CPL, ICPL, kFp8>::run(p);
+}
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_constant__ CompressParams p) {
@@ -331,6 +649,25 @@ __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_const
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 cudaError_t launch(const CompressParams& p, cudaStream_t st) {
+  using Tile = CompressTile<TIn, CPL, ICPL, kFp8>;
+  // Many tokens per sequence, small windows, no query rows: the tile kernel (one persistent
+  // CTA per SM, rows staged in shared memory).
+  if constexpr (Tile::kFits) {
+  if (p.n_qrows == 0 && p.W <= Tile::kMaxW && p.n_tokens >= 256 && p.n_seq <= Tile::kMaxSeq &&
+      p.n_tokens >= 8 * (int64_t)p.n_seq) {
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t max_tiles = p.n_tokens / Tile::kTT + p.n_seq;   // bound on the tile count
+    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+    cudaError_t e = cudaFuncSetAttribute(compress_tile_kernel<TIn, CPL, ICPL, kFp8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Tile::kSmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(compress_tile_kernel<TIn, CPL, ICPL, kFp8>, dim3(grid), dim3(Tile::kThreads), Tile::kSmem,
+                   st, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  }
   // One warp per block (the c4a bf16 kernel compiles to 128 registers a thread): such a
   // block fits on an SM beside a persistent indexer CTA, so a small insert never holds
   // an SM the indexer is waiting for.

@@ -6,8 +6,12 @@ Acceptance rules:
   * top-k sets: identical except entries whose oracle score lies within 1e-3 (relative)
     of the oracle's k-th score;
   * fp8 cache rows: scales within 1e-6 relative; codes equal except a one-step rounding
-    difference where the oracle's y/scale is within 1e-3 of a rounding midpoint
-    (in grid-step units);
+    difference where the oracle's y/scale lies near a rounding midpoint: within 1e-3 of a
+    grid step, or within 448 x 2^-20 in code units. The second bound is the kernel's own
+    error: it evaluates y in fp32 (a chain of about sixteen operations, each within 2^-24
+    of the row's largest value), so |y_gpu - y| <= 2^-20 amax, i.e. 448 x 2^-20 after the
+    division by scale = amax / 448. It matters only near zero, where an e4m3 step is 2^-9
+    (subnormal codes); fp4 rows use 6 x 2^-20 the same way;
   * fp32 cache rows: within 1e-5 absolute;
   * attention output: max-abs 1e-4 (fp32 layer), max-abs 3e-2 and mean-abs 3e-3
     (bf16 / fp8 layers), against the oracle run on the same stored values.
@@ -21,6 +25,7 @@ from compressed_sparse_long_gb300.layer import Layer
 from oracle import v4a_oracle as O
 
 TIE_BAND = 1e-3
+FP32_Y_ERR = 2.0 ** -20      # bound on the kernel's fp32 error in y, relative to the row amax
 FP32_OUT_TOL = 1e-4
 BF16_MAX_TOL = 3e-2
 BF16_MEAN_TOL = 3e-3
@@ -121,7 +126,9 @@ def check_fp8_rows(gpu_data, gpu_scale, ref_pool, slots):
         lo = np.maximum(hi - 1, 0)
         sgn = np.where(np.signbit(v), -1.0, 1.0)
         neighbour = (dg == sgn * grid[lo]) | (dg == sgn * grid[hi])
-        ok = same_value | (neighbour & (O.e4m3_midpoint_distance(v) < 1e-3))
+        dist = O.e4m3_midpoint_distance(v)                  # in grid steps
+        near = (dist < 1e-3) | (dist * (grid[hi] - grid[lo]) <= 448.0 * FP32_Y_ERR)
+        ok = same_value | (neighbour & near)
         assert ok.all(), "row %d: codes %s vs %s at y/scale %s" % (s, cg[bad][~ok], co[bad][~ok],
                                                                    v[~ok])
         n_close += int((~same_value).sum())
@@ -151,7 +158,9 @@ def check_fp4_rows(gpu_data, gpu_scale, ref_pool, slots):
         lo = np.maximum(hi - 1, 0)
         sgn = np.where(np.signbit(v), -1.0, 1.0)
         neighbour = (dg == sgn * grid[lo]) | (dg == sgn * grid[hi])
-        ok = same_value | (neighbour & (O.e2m1_midpoint_distance(v) < 1e-3))
+        dist = O.e2m1_midpoint_distance(v)                  # in grid steps
+        near = (dist < 1e-3) | (dist * (grid[hi] - grid[lo]) <= 6.0 * FP32_Y_ERR)
+        ok = same_value | (neighbour & near)
         assert ok.all(), "row %d: codes %s vs %s at y/scale %s" % (s, cg[bad][~ok], co[bad][~ok],
                                                                    v[~ok])
         n_close += int((~same_value).sum())
