@@ -25,6 +25,7 @@ namespace v4a {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxWindow = 256;   // the largest window a layer may have (host-checked)
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
 struct CompressKernel {
@@ -179,7 +180,7 @@ struct CompressKernel {
     float m[N];
 #pragma unroll
     for (int k = 0; k < N; ++k) m[k] = -INFINITY;
-#pragma unroll 4
+#pragma unroll 8
     for (int o = 0; o < p.W; ++o) {
       WindowRow w;
       const int st = fetch(o, w);
@@ -197,7 +198,7 @@ struct CompressKernel {
     float l[N], acc[N];
 #pragma unroll
     for (int k = 0; k < N; ++k) { l[k] = 0.f; acc[k] = 0.f; }
-#pragma unroll 4
+#pragma unroll 8
     for (int o = 0; o < p.W; ++o) {
       WindowRow w;
       if (fetch(o, w) <= 0) continue;
@@ -347,27 +348,45 @@ struct CompressKernel {
     const TIn* s_in = reinterpret_cast<const TIn*>(p.score);
     const TIn* ik_in = reinterpret_cast<const TIn*>(p.ikv);
     const TIn* is_in = reinterpret_cast<const TIn*>(p.iscore);
-    build_entry(p, b, j, lane, [&](int o, WindowRow& w) -> int {
+    // the window's rows are resolved once, lane o taking tokens o, o + 32, ... (the residual
+    // rows' block-table lookups in parallel): status 0 absent, 1 an input row, 2 a residual
+    // row, < 0 a residual row without a usable page; ref = input row or pool row
+    __shared__ int64_t s_ref[kMaxWindow];
+    __shared__ int8_t s_st[kMaxWindow];
+    for (int o = lane; o < p.W; o += 32) {
       const int64_t pos = j * p.S + p.win_off + o;
-      if (pos < 0) return 0;                       // before the sequence: absent
+      int st = 0;
+      int64_t ref = 0;
       if (pos >= P0) {
-        const int64_t r = row0 + (pos - P0);
-        w.kv = kv_in + r * D;
-        w.s = s_in + r * D;
-        if constexpr (ICPL > 0) {
-          w.ik = ik_in + r * DI;
-          w.is = is_in + r * DI;
-        }
-        return 1;
+        st = 1;
+        ref = row0 + (pos - P0);
+      } else if (pos >= 0) {
+        ref = slot_of(p.state, b, pos);
+        st = ref >= 0 ? 2 : (int)ref;
       }
-      const int64_t sl = slot_of(p.state, b, pos);
-      if (sl < 0) return (int)sl;                  // -1: no page, -2: page outside the pool
-      const TIn* base = reinterpret_cast<const TIn*>(p.state.data) + sl * (int64_t)p.state.width;
-      w.kv = base;
-      w.s = base + D;
-      if constexpr (ICPL > 0) {
-        w.ik = base + 2 * D;
-        w.is = base + 2 * D + DI;
+      s_st[o] = (int8_t)st;
+      s_ref[o] = ref;
+    }
+    __syncwarp();
+    build_entry(p, b, j, lane, [&](int o, WindowRow& w) -> int {
+      const int st = s_st[o];
+      if (st <= 0) return st;                      // absent, or -1 / -2 (page errors)
+      const int64_t ref = s_ref[o];
+      if (st == 1) {
+        w.kv = kv_in + ref * D;
+        w.s = s_in + ref * D;
+        if constexpr (ICPL > 0) {
+          w.ik = ik_in + ref * DI;
+          w.is = is_in + ref * DI;
+        }
+      } else {
+        const TIn* base = reinterpret_cast<const TIn*>(p.state.data) + ref * (int64_t)p.state.width;
+        w.kv = base;
+        w.s = base + D;
+        if constexpr (ICPL > 0) {
+          w.ik = base + 2 * D;
+          w.is = base + 2 * D + DI;
+        }
       }
       return 1;
     });

@@ -9,10 +9,11 @@
 // The per-row scale is applied after the head sum: ReLU is positively homogeneous and the
 // scale is positive, so sum_h w_h ReLU(q_h . (c*k)) = c * sum_h w_h ReLU(q_h . k).
 //
-// Top-k: MSB-first radix select on the order-preserving uint32 image of the fp32 scores
-// (4 passes of 8-bit digits, per-warp shared-memory histograms) finds the k-th
-// largest key; an ordered block compaction then emits every entry above it plus the
-// lowest-index entries equal to it, in ascending index order.
+// Top-k, on the order-preserving uint32 image of the fp32 scores: rows of up to 8192 entries
+// in registers (topk_reg_kernel), longer rows in three streaming passes (topk_stream_kernel);
+// both find the k-th largest key from score-linear buckets and the exact key inside the
+// boundary bucket, with radix passes for rows whose scores cannot be bucketed, and emit
+// every entry above it plus the lowest-index entries equal to it, in ascending index order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -81,147 +82,20 @@ __global__ void __launch_bounds__(128) index_scores_simt(const __grid_constant__
 }
 
 // ------------------------------------------------------------------------------ top-k
+__device__ __forceinline__ float warp_min_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t b = __float_as_uint(x + 0.0f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkSmemMax = 49152;   // rows up to this length are staged in shared memory
-
-// Exclusive block-wide prefix sum of one value per thread; the total through *total.
-__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t w = lane < (kTopkThreads / 32) ? warp_tot[lane] : 0u;
-    uint32_t z = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
-    }
-    warp_tot[lane] = z - w;
-    if (lane == 31) *total = z;
-  }
-  __syncthreads();
-  const uint32_t r = warp_tot[warp] + incl - v;
-  __syncthreads();
-  return r;
-}
-
-template <bool kSmem>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ IndexParams p) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ uint32_t row_keys[];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t whist[kTopkWarps][256];   // per-warp histograms (no cross-warp contention)
-  __shared__ uint32_t warp_tot[32];
-  __shared__ uint32_t s_digit, s_remaining, s_total;
-  const int qi = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int64_t pos = __ldg(p.q_pos + qi);
-  const int64_t n = min(visible_entries(pos, p.S, p.W, p.win_off), p.row_stride);
-  int32_t* out = p.topk + (int64_t)qi * p.k;
-  if (n <= p.k) {
-    for (int i = tid; i < p.k; i += kTopkThreads) out[i] = i < n ? i : -1;
-    return;
-  }
-  const float* row = p.scores + (int64_t)qi * p.row_stride;
-  if constexpr (kSmem) {
-    for (int64_t i = tid; i < n; i += kTopkThreads) row_keys[i] = order_key(row[i]);
-    __syncthreads();
-  }
-  auto key_at = [&](int64_t i) -> uint32_t {
-    if constexpr (kSmem) return row_keys[i];
-    else return order_key(__ldg(row + i));
-  };
-
-  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    uint32_t* my = whist[tid >> 5];
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&whist[0][0])[i] = 0;
-    __syncthreads();
-    for (int64_t i = tid; i < n; i += kTopkThreads) {
-      const uint32_t u = key_at(i);
-      if ((u & mask) == prefix) atomicAdd(&my[(u >> shift) & 0xFFu], 1u);
-    }
-    __syncthreads();
-    for (int b = tid; b < 256; b += kTopkThreads) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) t += whist[w][b];
-      hist[b] = t;
-    }
-    __syncthreads();
-    if (tid < 32) {
-      // lane l owns digits [255-8l-7, 255-8l], scanned from the top
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) { c[k] = hist[255 - 8 * tid - k]; sum += c[k]; }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += y;
-      }
-      const uint32_t before = incl - sum;
-      const bool here = before < remaining && incl >= remaining;
-      if (here) {
-        uint32_t cum = before;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (cum + c[k] >= remaining) {
-            s_digit = 255 - 8 * tid - k;
-            s_remaining = remaining - cum;
-            break;
-          }
-          cum += c[k];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= 0xFFu << shift;
-    remaining = s_remaining;
-    __syncthreads();
-  }
-
-  // prefix is the key of the k-th largest score; take all keys above it and the first
-  // `remaining` keys equal to it, in index order. Thread t owns the contiguous chunk
-  // [t*C, (t+1)*C): one block scan of its (ties, above) counts gives where its selected
-  // entries go, and it writes them in order.
-  const uint32_t kth = prefix;
-  const int64_t C = (n + kTopkThreads - 1) / kTopkThreads;
-  const int64_t c0 = (int64_t)tid * C, c1 = min(n, c0 + C);
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int64_t i = c0; i < c1; ++i) {
-    const uint32_t u = key_at(i);
-    n_gt += u > kth;
-    n_eq += u == kth;
-  }
-  const uint32_t ex_gt = block_excl_sum(n_gt, warp_tot, &s_total);
-  const uint32_t ex_eq = block_excl_sum(n_eq, warp_tot, &s_total);
-  uint32_t at = ex_gt + min(ex_eq, remaining);
-  uint32_t tie = ex_eq;
-  for (int64_t i = c0; i < c1; ++i) {
-    const uint32_t u = key_at(i);
-    if (u > kth || (u == kth && tie < remaining)) {
-      if (at < (uint32_t)p.k) out[at] = (int32_t)i;
-      ++at;
-    }
-    tie += u == kth;
-  }
 }
 
 __device__ __forceinline__ float key_value(uint32_t u) {   // inverse of order_key
@@ -469,6 +343,303 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------------------------------- streaming top-k
+// Every row of a call whose rows may exceed what the register-resident kernel holds: 256
+// threads a row, several rows per SM. Three coalesced passes over the row: its extremes; a
+// histogram of 2048 buckets linear in the score between them (a monotone map, so every
+// entry of a higher bucket scores strictly higher); the entries of the buckets at and above
+// the one where the count from the top reaches k, collected with their indices in shared
+// memory (at most kStreamCap). The exact k-th key among the boundary bucket's entries comes
+// from 8-bit radix passes over shared memory; the selected entries (those above it and the
+// smallest-index ties equal to it) are placed by their index rank. A row with non-finite or
+// constant scores, or too many collected entries, takes radix passes over the whole row
+// instead (four histogram passes, then an ordered compaction of per-thread chunks).
+constexpr int kStreamThreads = 256;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamBuckets = 2048;
+constexpr int kStreamCap = 2048;
+
+// Exclusive block-wide sum of one value per thread; the total through *total.
+__device__ __forceinline__ uint32_t stream_excl_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kStreamWarps; ++w) {
+    const uint32_t t = warp_tot[w];
+    before += w < warp ? t : 0u;
+    all += t;
+  }
+  __syncthreads();
+  if (total) *total = all;
+  return before + incl - v;
+}
+
+// The digit (scanning from the top) where the running count of h[] reaches `need`, and the
+// count still needed inside it; warp 0 only (lane l owns digits 255-8l-7 .. 255-8l).
+__device__ __forceinline__ void top_digit(const uint32_t* h, uint32_t need, uint32_t* s_digit,
+                                          uint32_t* s_need) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8], sum = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = h[255 - 8 * lane - k];
+    sum += c[k];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t before = incl - sum;
+  if (before < need && incl >= need) {
+    uint32_t cum = before;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (cum + c[k] >= need) {
+        *s_digit = 255 - 8 * lane - k;
+        *s_need = need - cum;
+        break;
+      }
+      cum += c[k];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __grid_constant__ IndexParams p) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ uint32_t bh[kStreamBuckets];           // bucket histogram; radix histograms after
+  __shared__ uint32_t ckey[kStreamCap];             // collected entries: order key,
+  __shared__ int32_t cidx[kStreamCap];              // entry index,
+  __shared__ uint8_t cin[kStreamCap];               // 1 = in the boundary bucket
+  __shared__ int32_t sel[kStreamCap];               // selected entry indices
+  __shared__ float s_lo[kStreamWarps], s_hi[kStreamWarps];
+  __shared__ uint32_t warp_tot[kStreamWarps];
+  __shared__ uint32_t s_bucket, s_above, s_nc, s_digit, s_need, s_total;
+  const int qi = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  const int64_t n = min(visible_entries(pos, p.S, p.W, p.win_off), p.row_stride);
+  int32_t* out = p.topk + (int64_t)qi * p.k;
+  const uint32_t k = (uint32_t)p.k;
+  if (n <= p.k) {
+    for (int i = tid; i < p.k; i += kStreamThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  const float* row = p.scores + (int64_t)qi * p.row_stride;
+  // row starts are 16-byte aligned and the stride is a multiple of 4: whole float4 groups
+  // are inside the row's allocation; entries >= n are masked. Each thread keeps kUnroll
+  // 16-byte loads in flight (they are issued before any is used).
+  constexpr int kUnroll = 8;
+  constexpr int64_t kStep = 4 * kStreamThreads;
+  auto for_each4 = [&](auto&& f) {
+    for (int64_t i0 = (int64_t)tid * 4; i0 < n; i0 += kStep * kUnroll) {
+      float4 x[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * kStep;
+        x[u] = i < n ? __ldg(reinterpret_cast<const float4*>(row + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * kStep;
+        if (i < n) f(i, x[u].x);
+        if (i + 1 < n) f(i + 1, x[u].y);
+        if (i + 2 < n) f(i + 2, x[u].z);
+        if (i + 3 < n) f(i + 3, x[u].w);
+      }
+    }
+  };
+  // ---- pass 1: extremes (a NaN score sends the row to the radix passes)
+  float lo = INFINITY, hi = -INFINITY;
+  for_each4([&](int64_t, float x) {
+    lo = fminf(lo, x);
+    hi = x != x ? INFINITY : fmaxf(hi, x);
+  });
+  lo = warp_min_f(lo);
+  hi = warp_max_f(hi);
+  if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  for (int i = tid; i < kStreamBuckets; i += kStreamThreads) bh[i] = 0u;
+  if (tid == 0) s_nc = 0u;
+  __syncthreads();
+  lo = INFINITY;
+  hi = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kStreamWarps; ++w) {
+    lo = fminf(lo, s_lo[w]);
+    hi = fmaxf(hi, s_hi[w]);
+  }
+  const float span = hi - lo;
+  bool bucketed = span > 0.f && span <= 3.0e38f;   // block-uniform
+  uint32_t kth = 0, remaining = 0;
+  if (bucketed) {
+    const float inv = (float)kStreamBuckets / span;
+    auto bucket = [&](float x) -> int {
+      return max(0, min((int)((x - lo) * inv), kStreamBuckets - 1));
+    };
+    // ---- pass 2: histogram
+    for_each4([&](int64_t, float x) { atomicAdd(&bh[bucket(x)], 1u); });
+    __syncthreads();
+    // boundary bucket: thread t owns buckets 2047-8t-7 .. 2047-8t, from the top
+    {
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = bh[kStreamBuckets - 1 - 8 * tid - j];
+        sum += c[j];
+      }
+      const uint32_t before = stream_excl_sum(sum, warp_tot, nullptr);
+      if (before < k && before + sum >= k) {
+        uint32_t cum = before;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + c[j] >= k) {
+            s_bucket = (uint32_t)(kStreamBuckets - 1 - 8 * tid - j);
+            s_above = cum;
+            break;
+          }
+          cum += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    const int bstar = (int)s_bucket;
+    const uint32_t above = s_above;
+    bucketed = above + bh[bstar] <= (uint32_t)kStreamCap;   // block-uniform
+    if (bucketed) {
+      // ---- pass 3: collect the entries of buckets >= bstar (warp-aggregated appends)
+      // (the loop bound is the warp's first index, so every lane of a warp runs the same
+      // iterations and the ballots are warp-wide)
+      for (int64_t i0 = (int64_t)tid * 4; i0 - (int64_t)lane * 4 < n; i0 += kStep * kUnroll) {
+        float4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t i = i0 + u * kStep;
+          x[u] = i < n ? __ldg(reinterpret_cast<const float4*>(row + i))
+                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t i = i0 + u * kStep + e;
+            const bool in = i < n && bucket(v[e]) >= bstar;
+            const uint32_t m = __ballot_sync(0xffffffffu, in);
+            uint32_t base = 0;
+            if (lane == 0 && m) base = atomicAdd(&s_nc, (uint32_t)__popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (in) {
+              const uint32_t at = base + __popc(m & ((1u << lane) - 1u));
+              ckey[at] = order_key(v[e]);
+              cidx[at] = (int32_t)i;
+              cin[at] = bucket(v[e]) == bstar ? 1 : 0;
+            }
+          }
+        }
+      }
+      __syncthreads();
+      const int nc = (int)s_nc;
+      // ---- exact k-th key among the boundary bucket's entries: 8-bit radix passes
+      uint32_t prefix = 0, mask = 0, need = k - above;
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += kStreamThreads) bh[i] = 0u;
+        __syncthreads();
+        for (int c = tid; c < nc; c += kStreamThreads)
+          if (cin[c] && (ckey[c] & mask) == prefix) atomicAdd(&bh[(ckey[c] >> shift) & 0xFFu], 1u);
+        __syncthreads();
+        if (warp == 0) top_digit(bh, need, &s_digit, &s_need);
+        __syncthreads();
+        prefix |= s_digit << shift;
+        mask |= 0xFFu << shift;
+        need = s_need;
+      }
+      kth = prefix;
+      remaining = need;              // ties equal to kth still to take, smallest indices first
+      // ---- selection: contiguous chunks of the collected entries, one block scan
+      const int per = (nc + kStreamThreads - 1) / kStreamThreads;
+      const int c0 = tid * per, c1 = min(nc, c0 + per);
+      auto selected = [&](int c) -> bool {
+        const uint32_t key = ckey[c];
+        if (!cin[c] || key > kth) return true;
+        if (key != kth) return false;
+        uint32_t rank = 0;           // ties equal to kth with a smaller index
+        for (int d = 0; d < nc; ++d) rank += (cin[d] && ckey[d] == kth && cidx[d] < cidx[c]) ? 1u : 0u;
+        return rank < remaining;
+      };
+      uint32_t cnt = 0;
+      for (int c = c0; c < c1; ++c) cnt += selected(c) ? 1u : 0u;
+      uint32_t at = stream_excl_sum(cnt, warp_tot, &s_total);
+      for (int c = c0; c < c1; ++c)
+        if (selected(c)) sel[at++] = cidx[c];
+      __syncthreads();
+      // ---- output in ascending index order: the rank of each selected index
+      const int ns = (int)s_total;   // == k
+      for (int sidx = tid; sidx < ns; sidx += kStreamThreads) {
+        const int32_t v = sel[sidx];
+        int rank = 0;
+        for (int d = 0; d < ns; ++d) rank += sel[d] < v ? 1 : 0;
+        if (rank < p.k) out[rank] = v;
+      }
+      return;
+    }
+  }
+  // ---- radix passes over the whole row: the k-th key, then an ordered compaction
+  uint32_t* h = bh;
+  uint32_t prefix = 0, mask = 0, need = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kStreamThreads) h[i] = 0u;
+    __syncthreads();
+    for_each4([&](int64_t, float x) {
+      const uint32_t u = order_key(x);
+      if ((u & mask) == prefix) atomicAdd(&h[(u >> shift) & 0xFFu], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) top_digit(h, need, &s_digit, &s_need);
+    __syncthreads();
+    prefix |= s_digit << shift;
+    mask |= 0xFFu << shift;
+    need = s_need;
+  }
+  kth = prefix;
+  remaining = need;
+  // thread t owns the contiguous chunk [t C, (t+1) C): one block scan of its (above, equal)
+  // counts places its selected entries
+  const int64_t C = (n + kStreamThreads - 1) / kStreamThreads;
+  const int64_t r0 = (int64_t)tid * C, r1 = min(n, r0 + C);
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int64_t i = r0; i < r1; ++i) {
+    const uint32_t u = order_key(__ldg(row + i));
+    n_gt += u > kth;
+    n_eq += u == kth;
+  }
+  const uint32_t ex_gt = stream_excl_sum(n_gt, warp_tot, nullptr);
+  const uint32_t ex_eq = stream_excl_sum(n_eq, warp_tot, nullptr);
+  uint32_t at = ex_gt + min(ex_eq, remaining);
+  uint32_t tie = ex_eq;
+  for (int64_t i = r0; i < r1; ++i) {
+    const uint32_t u = order_key(__ldg(row + i));
+    if (u > kth || (u == kth && tie < remaining)) {
+      if (at < k) out[at] = (int32_t)i;
+      ++at;
+    }
+    tie += u == kth;
+  }
+}
+
 template <typename T, bool kFp8, int HI, int DI>
 cudaError_t launch_simt(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   dim3 grid((unsigned)((max_vis + 127) / 128), (unsigned)p.n_q);
@@ -495,20 +666,10 @@ int launch_index_scores(const IndexParams& p, int dtype, int64_t max_vis, cudaSt
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.n_q == 0) return V4A_OK;
   cudaError_t e;
-  if (max_vis <= 8 * 1024) {
+  if (max_vis <= 8 * 1024)   // decode-sized rows: register-resident, one CTA of 1024 threads a row
     e = launch_pdl(topk_reg_kernel<8, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
-  } else if (max_vis <= 32 * 1024) {
-    e = launch_pdl(topk_reg_kernel<32, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
-  } else if (max_vis <= kTopkSmemMax) {
-    const size_t smem = (size_t)max_vis * sizeof(uint32_t);
-    // the attribute belongs to the current device's copy of the kernel: set it on every
-    // launch (a host call, cheap next to the kernel) so that every device gets it
-    e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTopkSmemMax * (int)sizeof(uint32_t));
-    if (e == cudaSuccess) e = launch_pdl(topk_kernel<true>, dim3(p.n_q), dim3(kTopkThreads), smem, st, p);
-  } else {
-    e = launch_pdl(topk_kernel<false>, dim3(p.n_q), dim3(kTopkThreads), 0, st, p);
-  }
+  else                       // longer rows: streaming passes, 256 threads a row
+    e = launch_pdl(topk_stream_kernel, dim3(p.n_q), dim3(kStreamThreads), 0, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

@@ -310,9 +310,12 @@ def test_index_topk_prefill_positions(n_q, k):
     check_topk(topk.cpu().numpy(), ref, scores, k)
 
 
-def test_topk_ties_take_smaller_index():
-    """Equal scores: identical keys tie exactly; the smaller entry indices win."""
-    w = wl.c4a_decode(seed=7, B=2, L=4096)
+@pytest.mark.parametrize("L", [4096, 65536])
+def test_topk_ties_take_smaller_index(L):
+    """Equal scores: identical keys tie exactly; the smaller entry indices win (rows held in
+    registers at L=4096; at L=65536 the streaming selection, whose constant rows take the
+    radix passes)."""
+    w = wl.c4a_decode(seed=7, B=2, L=L)
     h = w.layers[0]
     h.idx.data[:] = h.idx.data[0]
     h.idx.scale[:] = h.idx.scale[0]
@@ -322,12 +325,14 @@ def test_topk_ties_take_smaller_index():
         assert np.array_equal(topk[i], np.arange(512))
 
 
-@pytest.mark.parametrize("n_tied,rank", [(300, 0), (300, 412), (1200, 0)])
-def test_topk_tied_block(n_tied, rank):
+@pytest.mark.parametrize("n_tied,rank,L", [(300, 0, 16384), (300, 412, 16384), (1200, 0, 16384),
+                                           (300, 0, 65536), (300, 412, 65536), (1200, 0, 65536)])
+def test_topk_tied_block(n_tied, rank, L):
     """A block of identical indexer keys (so identical scores) placed wholly above the k-th
     score, across it, or larger than k at the top of the row: the output holds every entry
-    scoring above the block and exactly the smallest-index members of the block."""
-    w = wl.c4a_decode(seed=11, B=2, L=16384)
+    scoring above the block and exactly the smallest-index members of the block (rows of
+    4095 entries held in registers, rows of 16383 in the streaming selection)."""
+    w = wl.c4a_decode(seed=11, B=2, L=L)
     h = w.layers[0]
     q = w.queries
     rng = np.random.default_rng(17)
@@ -749,7 +754,7 @@ def test_index_scores_elementwise(case):
     lay.compress_insert(x.cu, x.start, x.kv, x.s, x.ik, x.is_, dev_err=err)
     got = lay.index_scores(x.q_seq, x.q_pos, x.max_pos, x.q_idx, x.w, dev_err=err)
     assert v4a.v4a_get_error(err) == 0
-    got = got.cpu().numpy().astype(np.float64)
+    got = got.cpu().numpy()               # columns past a row's visible count are not written
     dp = device_pools(lay, h.spec)
     q = w.queries
     _, scores = O.index_topk(h.spec, dp, q.seq, q.pos, q.q_idx, q.w, h.spec.top_k)
@@ -757,7 +762,7 @@ def test_index_scores_elementwise(case):
     for i in range(len(q.pos)):
         n = len(scores[i])
         bound = _score_bound(h.spec, dp, q.seq[i], q.pos[i], q.q_idx[i], q.w[i])
-        d = np.abs(got[i, :n] - scores[i])
+        d = np.abs(got[i, :n].astype(np.float64) - scores[i])
         assert (d <= 3e-5 * bound + 1e-30).all(), (i, d.max(), bound[np.argmax(d)])
         if n:
             worst = max(worst, float((d / np.maximum(bound, 1e-300)).max()))
