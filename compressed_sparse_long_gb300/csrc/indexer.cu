@@ -461,10 +461,30 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
   };
   // ---- pass 1: extremes (a NaN score sends the row to the radix passes)
   float lo = INFINITY, hi = -INFINITY;
-  for_each4([&](int64_t, float x) {
-    lo = fminf(lo, x);
-    hi = x != x ? INFINITY : fmaxf(hi, x);
-  });
+  bool nan = false;
+  for (int64_t i0 = (int64_t)tid * 4; i0 < n; i0 += kStep * kUnroll) {
+    float4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * kStep;
+      x[u] = i < n ? __ldg(reinterpret_cast<const float4*>(row + i))
+                   : make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+      // entries past n within the last group take a value that changes neither extreme
+      if (i < n && i + 3 >= n) {
+        if (i + 1 >= n) x[u].y = x[u].x;
+        if (i + 2 >= n) x[u].z = x[u].x;
+        x[u].w = x[u].x;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (i0 + u * kStep >= n) continue;
+      lo = fminf(lo, fminf(fminf(x[u].x, x[u].y), fminf(x[u].z, x[u].w)));
+      hi = fmaxf(hi, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+      nan |= (x[u].x != x[u].x) | (x[u].y != x[u].y) | (x[u].z != x[u].z) | (x[u].w != x[u].w);
+    }
+  }
+  if (nan) hi = INFINITY;
   lo = warp_min_f(lo);
   hi = warp_max_f(hi);
   if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
@@ -530,6 +550,9 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+          // (masked entries are -inf: bucket 0 < bstar unless bstar is 0, checked below)
+          const bool any4 = bucket(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]))) >= bstar;
+          if (!__any_sync(0xffffffffu, any4)) continue;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int64_t i = i0 + u * kStep + e;
@@ -567,6 +590,12 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
       }
       kth = prefix;
       remaining = need;              // ties equal to kth still to take, smallest indices first
+      // entries equal to kth: when all of them are taken (the usual case, one entry), no
+      // tie needs its index rank
+      uint32_t n_tie = 0;
+      for (int c = tid; c < nc; c += kStreamThreads) n_tie += (cin[c] && ckey[c] == kth) ? 1u : 0u;
+      stream_excl_sum(n_tie, warp_tot, &s_total);
+      const bool all_ties = s_total <= remaining;
       // ---- selection: contiguous chunks of the collected entries, one block scan
       const int per = (nc + kStreamThreads - 1) / kStreamThreads;
       const int c0 = tid * per, c1 = min(nc, c0 + per);
@@ -574,6 +603,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
         const uint32_t key = ckey[c];
         if (!cin[c] || key > kth) return true;
         if (key != kth) return false;
+        if (all_ties) return true;
         uint32_t rank = 0;           // ties equal to kth with a smaller index
         for (int d = 0; d < nc; ++d) rank += (cin[d] && ckey[d] == kth && cidx[d] < cidx[c]) ? 1u : 0u;
         return rank < remaining;
@@ -584,14 +614,27 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
       for (int c = c0; c < c1; ++c)
         if (selected(c)) sel[at++] = cidx[c];
       __syncthreads();
-      // ---- output in ascending index order: the rank of each selected index
+      // ---- output in ascending index order: a bitonic sort of the selected indices, padded
+      // to a power of two with INT32_MAX
       const int ns = (int)s_total;   // == k
-      for (int sidx = tid; sidx < ns; sidx += kStreamThreads) {
-        const int32_t v = sel[sidx];
-        int rank = 0;
-        for (int d = 0; d < ns; ++d) rank += sel[d] < v ? 1 : 0;
-        if (rank < p.k) out[rank] = v;
+      int np2 = 1;
+      while (np2 < ns) np2 <<= 1;
+      for (int i = ns + tid; i < np2; i += kStreamThreads) sel[i] = INT32_MAX;
+      __syncthreads();
+      for (int size = 2; size <= np2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int t = tid; t < (np2 >> 1); t += kStreamThreads) {
+            const int a = 2 * t - (t & (stride - 1)), b = a + stride;
+            const int32_t x0 = sel[a], x1 = sel[b];
+            if ((x0 > x1) == ((a & size) == 0)) {
+              sel[a] = x1;
+              sel[b] = x0;
+            }
+          }
+          __syncthreads();
+        }
       }
+      for (int i = tid; i < ns && i < p.k; i += kStreamThreads) out[i] = sel[i];
       return;
     }
   }

@@ -734,12 +734,14 @@ def _score_bound(spec, dp, seq, pos, q_idx, w):
     return np.abs(keys).sum(axis=1) * float((np.abs(np.asarray(w, np.float64)) * qa).sum())
 
 
-@pytest.mark.parametrize("case", ["fp8_decode", "fp4_decode", "fp8_prefill", "fp32_tiny"])
+@pytest.mark.parametrize("case", ["fp8_decode", "fp4_decode", "fp8_prefill", "fp8_prefill_pairs",
+                                  "fp4_prefill_pairs", "fp32_tiny"])
 def test_index_scores_elementwise(case):
     """v4a_index_scores against the oracle's scores, element by element, for every visible
     entry of every query: |gpu - oracle| <= 3e-5 x the row's a-priori rounding bound (fp32
     accumulation of exact products, 2^-17 relative loss of the split query below the e4m3
-    subnormal step)."""
+    subnormal step). The pair cases run the kernel that takes two queries per key tile and
+    accumulates the query's two e4m3 terms in one product."""
     if case == "fp8_decode":
         w = wl.c4a_decode(seed=51, B=8, L=8192)
         _inject_subnormal_keys(w.layers[0], np.random.default_rng(52))
@@ -747,6 +749,10 @@ def test_index_scores_elementwise(case):
         w = wl.c4a_decode(seed=53, B=8, L=8192, idx_fp4=True)
     elif case == "fp8_prefill":
         w = wl.c4a_prefill(seed=54, cached=8192, chunk=300)
+    elif case == "fp8_prefill_pairs":        # >= 1024 queries: two queries per key tile
+        w = wl.c4a_prefill(seed=56, cached=8192, chunk=1024)
+    elif case == "fp4_prefill_pairs":
+        w = wl.c4a_prefill(seed=57, cached=8192, chunk=1024, idx_fp4=True)
     else:
         w = wl.tiny_prefill(seed=55, L=700)
     h = w.layers[0]
