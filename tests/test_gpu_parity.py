@@ -392,53 +392,63 @@ def test_attention_fp8_c4a_lists(prefill):
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
 
-@pytest.mark.parametrize("B,L,plan", [(32, 4096, (3, 2)), (64, 4096, (2, 2)), (16, 4096, (5, 2)),
-                                      (32, 600, (3, 2)), (160, 4096, (1, 1))])
-def test_attention_split_merge_modes(B, L, plan):
-    """Decode attention with 3, 2 or 5 key ranges per query (bf16 o / l partials combined by
-    the merge kernel) and without a split; at L=600 a query sees 149 entries, so its third
-    range holds no key and must not enter the combine."""
+@pytest.mark.parametrize("B,L,width,plan", [
+    (32, 4096, 512, (3, 2)), (40, 4096, 128, (2, 2)), (24, 8192, 896, (4, 2)),
+    (32, 600, 512, (3, 2)), (16, 4096, 512, (5, 2)), (160, 4096, 512, (1, 1)),
+    (16, 8192, 1024, (9, 2)), (8, 600, 1024, (9, 2))])
+def test_attention_split_merge_modes(B, L, width, plan):
+    """Decode attention with 2, 3, 4, 5 or 9 key ranges per query (partials combined by the
+    merge kernel) and without a split. At L=600 a query sees 149 entries: its middle range
+    of three (512-wide lists), or most of its nine (1024-wide lists), hold only masked
+    entries."""
     w = wl.c4a_decode(seed=17, B=B, L=L)
     h = w.layers[0]
     _fill_query_window_row(h, w)
     q = w.queries
-    lists = _random_lists(np.random.default_rng(5), q.pos, h.spec, 512)
+    lists = _random_lists(np.random.default_rng(5), q.pos, h.spec, width)
     lay, x, err = device_layer(h), DevInputs(w), _err()
-    assert v4a.v4a_attn_plan(lay.cfg, B, x.max_pos, 512) == plan
-    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32), dev_err=err)
+    assert v4a.v4a_attn_plan(lay.cfg, B, x.max_pos, width) == plan
+    tk = T(lists, torch.int32)
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, tk, dev_err=err)
     assert v4a.v4a_get_error(err) == 0
+    again = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, tk, dev_err=err)
+    assert torch.equal(again, out)                  # the same bytes on a second call
     ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
 
-def _lists_with_masked_blocks(rng, pos, spec):
-    """Top-512 lists whose key blocks 0-127 and 256-383 are all -1 (masked) and whose blocks
-    128-255 and 384-511 hold distinct visible entries: with 128-key tiles, a key range may
-    then begin with a tile that has no key."""
-    out = np.full((len(pos), 512), -1, np.int32)
+def _lists_with_masked_blocks(rng, pos, spec, width=512, masked=(0, 2)):
+    """Top-`width` lists whose 128-entry blocks named in `masked` are all -1 and whose other
+    blocks hold distinct visible entries, each block sorted: with 128-key tiles, a key range
+    may then begin with a tile that has no key."""
+    out = np.full((len(pos), width), -1, np.int32)
+    keep = [t for t in range(width // 128) if t not in masked]
     for i, p in enumerate(pos):
         n = O.visible_entries(spec.S, spec.W, spec.win_off, int(p))
-        e = rng.choice(n, 256, replace=False)
-        out[i, 128:256] = np.sort(e[:128])
-        out[i, 384:512] = np.sort(e[128:])
+        e = rng.choice(n, 128 * len(keep), replace=False)
+        for j, t in enumerate(keep):
+            out[i, 128 * t:128 * (t + 1)] = np.sort(e[128 * j:128 * (j + 1)])
     return out
 
 
-@pytest.mark.parametrize("prefill", [False, True])
-def test_attention_key_range_starting_with_a_masked_tile(prefill):
-    """Decode (3 key ranges of 256/256/128 keys) and prefill (one range of 5 tiles) where
-    tiles 0 and 2 hold only masked list entries: the per-range scaling of P' must be set by
-    the first tile that has a key, not by the range's first tile."""
-    w = wl.c4a_decode(seed=23, B=32, L=4096)
+@pytest.mark.parametrize("mode", ["split", "split_wide", "prefill"])
+def test_attention_key_range_starting_with_a_masked_tile(mode):
+    """Attention where key ranges begin with tiles that hold only masked list entries:
+    decode with 3 ranges of 2/2/1 tiles (tiles 0 and 2 masked), decode with 3 ranges of 3
+    tiles over 1024-wide lists (tiles 0, 3 and 6 masked: every range) and prefill (one range
+    of 5 tiles, tiles 0 and 2 masked). The scaling of P' must be set by the first tile that
+    has a key, not by the range's first tile."""
+    L, width, masked = (8192, 1024, (0, 3, 6)) if mode == "split_wide" else (4096, 512, (0, 2))
+    w = wl.c4a_decode(seed=23, B=32, L=L)
     h = w.layers[0]
     _fill_query_window_row(h, w)
     q = w.queries
-    lists = _lists_with_masked_blocks(np.random.default_rng(8), q.pos, h.spec)
+    lists = _lists_with_masked_blocks(np.random.default_rng(8), q.pos, h.spec, width, masked)
     lay, x, err = device_layer(h), DevInputs(w), _err()
-    if not prefill:
-        assert v4a.v4a_attn_plan(lay.cfg, 32, x.max_pos, 512) == (3, 2)
+    if mode != "prefill":
+        assert v4a.v4a_attn_plan(lay.cfg, 32, x.max_pos, width) == (3, 2)
     out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, T(lists, torch.int32),
-                        prefill=prefill, dev_err=err)
+                        prefill=mode == "prefill", dev_err=err)
     assert v4a.v4a_get_error(err) == 0
     ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, lists)
     check_out(out.float().cpu().numpy(), ref, fp8=True)
@@ -452,18 +462,24 @@ def _e4m3_step(v):
     return g[hi] - g[hi - 1]
 
 
-@pytest.mark.parametrize("B,L,width", [(8, 8192, 512), (4, 48, 64)])
-def test_attention_q8_output(B, L, width):
+@pytest.mark.parametrize("B,L", [(8, 8192), (4, 48)])
+def test_attention_q8_output(B, L):
     """fp8 output epilogue ([notes] 融合 2：Inverse RoPE + FP8 Quant): per (query, head) row the
     scale is amax/448 and the codes are e4m3 RNE of out/scale. The rule is checked against the
-    same attention's bf16 output, the values against the oracle. The short contexts leave the
-    second key range empty (the merge must skip it)."""
+    same attention's bf16 output, the values against the oracle. The lists are 1024 wide (9 key
+    tiles), so the bf16 call and the fp8 one split the keys into the same 9 ranges and share
+    their arithmetic up to the merge; the short context leaves most ranges empty (the merge
+    must skip them)."""
     w = wl.c4a_decode(seed=21, B=B, L=L)
     h = w.layers[0]
     q = w.queries
+    width = 1024
     lists = _random_lists(np.random.default_rng(5), q.pos, h.spec, width)
     _fill_query_window_row(h, w)
     lay, x = device_layer(h), DevInputs(w)
+    assert v4a.v4a_attn_plan(lay.cfg, B, x.max_pos, width) == (9, 2)
+    assert (v4a.v4a_attn_q8_workspace_size(lay.cfg, B, x.max_pos, width)
+            == v4a.v4a_attn_workspace_size(lay.cfg, B, x.max_pos, width, False))
     tk = torch.from_numpy(lists).cuda()
     err = _err()
     out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, tk, dev_err=err)
@@ -518,6 +534,29 @@ def test_attention_fp8_c128a_dense():
     q = w.queries
     lay, x = device_layer(h), DevInputs(w)
     out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, None)
+    ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, None)
+    check_out(out.float().cpu().numpy(), ref, fp8=True)
+
+
+def test_attention_split_with_empty_ranges():
+    """Dense c128a decode of sequences of 32768, 256, 100 and 20000 tokens: 3 key tiles at
+    the longest, so 3 ranges per query. The 256-token query has one entry and 128 window
+    rows (its third range is empty), the 100-token query only its 101 window rows (two
+    empty ranges): an empty range writes no partial and must not enter the merge."""
+    spec = wl.LayerSpec("c128a", True)
+    rng = np.random.default_rng(31)
+    ctx = [32768, 256, 100, 20000]
+    h = wl.make_layer(rng, spec, ctx, [1] * 4, prefill_cache=True)
+    h.bias, h.gamma, _ = wl.layer_params(rng, spec)
+    b = wl.make_batch(rng, spec, ctx, [1] * 4)
+    w = wl.Workload("c128a mixed", [h], b, wl.make_queries(rng, spec, np.arange(4),
+                                                           np.array(ctx), False))
+    _fill_query_window_row(h, w)
+    q = w.queries
+    lay, x, err = device_layer(h), DevInputs(w), _err()
+    assert v4a.v4a_attn_plan(lay.cfg, 4, x.max_pos, 0) == (3, 2)
+    out = lay.attention(x.q_seq, x.q_pos, x.max_pos, x.q, None, dev_err=err)
+    assert v4a.v4a_get_error(err) == 0
     ref = O.attention(h.spec, oracle_pools(h), q.seq, q.pos, q.q, None)
     check_out(out.float().cpu().numpy(), ref, fp8=True)
 
