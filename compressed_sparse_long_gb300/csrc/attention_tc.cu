@@ -50,9 +50,9 @@ constexpr int kQBytes = 2 * kH * kD;           // 64 KB Q~ hi (rows 0-63) and lo
 constexpr int kPBytes = kH * kTile;            // 8 KB per P' term, [128 keys][64 heads]
 constexpr int kOffK = 0, kOffQ = 2 * kKBytes, kOffP = kOffQ + kQBytes;
 // floats: l_fin[2][64] red_max[2][256] red_sum[256] sscale[2][128] mwarp[4][128] qamax[8]
-// qinv[3] red_sc[2][4]
+// qinv[3] red_sc[2][4] rope_tab[4][kMaxRopePairs]
 constexpr int kOffF = kOffP + 2 * kPBytes;
-constexpr int kNFloats = 128 + 512 + 256 + 256 + 512 + 8 + 4 + 8;
+constexpr int kNFloats = 128 + 512 + 256 + 256 + 512 + 8 + 4 + 8 + 4 * kMaxRopePairs;
 constexpr int kOffBar = kOffF + kNFloats * 4;
 constexpr int kNBar = 15;
 constexpr int kOffMisc = kOffBar + kNBar * 8;
@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
   float* qamax = mwarp + 512;                             // [8] raw |q| max of each build warp
   float* qinv = qamax + 8;                                // [3] 1 / s by item % 3 (+1 pad)
   float* red_sc = qinv + 4;                               // [2][4] tile max of the row scales
+  float* rope_tab = red_sc + 8;                           // RoPE angle constants (stage_rope)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* kfull = bars;                                 // [2] by key buffer
   uint64_t* kempty = bars + 2;                            // [2]
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
+  stage_rope(p.rope, rope_tab, tid, kThreads);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         // RoPE of this lane's 8 dim pairs: lane i computes pair i, the tail lanes collect theirs
         const int tail0 = kD - p.rope.d_r;
         float c_l = 1.f, s_l = 0.f;
-        if (lane < p.rope.d_r / 2) rope_cs(p.rope, I.pos, lane, c_l, s_l);
+        if (lane < p.rope.d_r / 2) rope_cs_tab(rope_tab, I.pos, lane, c_l, s_l);
         float rc[8], rsn[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
         for (int b = 0; b < 4; ++b) {
           const int d = b * 128 + row, d0 = even ? d : d - 1;
           float c = 1.f, sn = 0.f;
-          if (d0 >= tail0) rope_cs(p.rope, I.pos, (d0 - tail0) >> 1, c, sn);
+          if (d0 >= tail0) rope_cs_tab(rope_tab, I.pos, (d0 - tail0) >> 1, c, sn);
           float ob[2][32];
           tc::tmem_ld32(tmem + lane_base + kOCol + b * 64, ob[0]);
           tc::tmem_ld32(tmem + lane_base + kOCol + b * 64 + 32, ob[1]);

@@ -91,8 +91,26 @@ __device__ __forceinline__ float frac_prod(float x, float yh, float yl) {
 // cos/sin of pos * theta_i. With pos = hi * 4096 + lo the angle in turns is
 // frac(hi * psi_i + lo * phi_i), reduced exactly in fp32 (error ~1e-7 turn for positions up
 // to 2^31); sincospif then evaluates the reduced angle.
+// Pair i's four angle constants read with a per-thread index come from the constant bank
+// one address at a time; kernels that evaluate many angles stage them in shared memory
+// first ([4][kMaxRopePairs]: phi_hi, phi_lo, psi_hi, psi_lo) and use rope_cs_tab.
+__device__ __forceinline__ void stage_rope(const Rope& rp, float* tab, int tid, int nthreads) {
+  for (int k = tid; k < 4 * kMaxRopePairs; k += nthreads) {
+    const int a = k / kMaxRopePairs, i = k % kMaxRopePairs;
+    tab[k] = a == 0 ? rp.phi_hi[i] : a == 1 ? rp.phi_lo[i] : a == 2 ? rp.psi_hi[i] : rp.psi_lo[i];
+  }
+}
+__device__ __forceinline__ void rope_cs_tab(const float* tab, int64_t pos, int i, float& c, float& s) {
+  const float hi = (float)(int32_t)(pos >> 12), lo = (float)(int32_t)(pos & 4095);
+  float a = frac_prod(hi, tab[2 * kMaxRopePairs + i], tab[3 * kMaxRopePairs + i]) +
+            frac_prod(lo, tab[i], tab[kMaxRopePairs + i]);
+  a -= rintf(a);
+  sincospif(2.0f * a, &s, &c);
+}
+
 __device__ __forceinline__ void rope_cs(const Rope& rp, int64_t pos, int i, float& c, float& s) {
-  const float hi = (float)(pos >> 12), lo = (float)(pos & 4095);
+  // (positions below 2^43: both parts convert from 32-bit integers)
+  const float hi = (float)(int32_t)(pos >> 12), lo = (float)(int32_t)(pos & 4095);
   float a = frac_prod(hi, rp.psi_hi[i], rp.psi_lo[i]) + frac_prod(lo, rp.phi_hi[i], rp.phi_lo[i]);
   a -= rintf(a);
   sincospif(2.0f * a, &s, &c);

@@ -98,12 +98,16 @@ struct CompressKernel {
   // Rotate the lane's channels that fall in the rotated tail (adjacent pairs). Lane i
   // evaluates the angle of pair i (d_r / 2 <= 32 pairs) and the lanes owning the tail take
   // theirs by shuffle, so the warp evaluates each angle once and in parallel.
+  // tab: the angle constants staged in shared memory (stage_rope), or nullptr.
   template <int N>
   static __device__ __forceinline__ void rope_lane(const Rope& rp, float (&y)[N], int lane,
-                                                   int64_t pos) {
+                                                   int64_t pos, const float* tab = nullptr) {
     const int tail0 = rp.D - rp.d_r;
     float c_l = 1.f, s_l = 0.f;
-    if (lane < (rp.d_r >> 1)) rope_cs(rp, pos, lane, c_l, s_l);
+    if (lane < (rp.d_r >> 1)) {
+      if (tab) rope_cs_tab(tab, pos, lane, c_l, s_l);
+      else rope_cs(rp, pos, lane, c_l, s_l);
+    }
 #pragma unroll
     for (int k = 0; k < N; k += 2) {
       const int d = lane * N + k;
@@ -163,6 +167,13 @@ struct CompressKernel {
     }
   }
 
+  // 2^x by the hardware approximation (ex2.approx.ftz: relative error ~2^-22, 0 for -inf).
+  static __device__ __forceinline__ float exp2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+  }
+
   // Weighted sum of one window with per-channel softmax weights, as the pages' compressor
   // defines it: z_o = s_o + bias[o], w_o = exp(z_o - max_o z_o) / sum_o exp(z_o - max_o z_o),
   // c = sum_o w_o kv_o (max first, then the exponentials, tokens in window order; the
@@ -208,13 +219,14 @@ struct CompressKernel {
       load_f<float, N>(bias + (int64_t)o * width + lane * N, bv);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float e = exp2f((sv[k] + bv[k]) * kLog2e - m[k]);
+        const float e = exp2_approx((sv[k] + bv[k]) * kLog2e - m[k]);
         l[k] += e;
         acc[k] = fmaf(e, xv[k], acc[k]);
       }
     }
+    // l >= 1 (the window's largest weight is 2^0): an approximate division (~2 ulp)
 #pragma unroll
-    for (int k = 0; k < N; ++k) c[k] = __fdiv_rn(acc[k], l[k]);
+    for (int k = 0; k < N; ++k) c[k] = __fdividef(acc[k], l[k]);
     return true;
   }
 
@@ -223,7 +235,7 @@ struct CompressKernel {
   // kernels build entries here, so they write identical bytes.
   template <class Fetch>
   static __device__ void build_entry(const CompressParams& p, int b, int64_t j, int lane,
-                                     const Fetch& fetch) {
+                                     const Fetch& fetch, const float* rope_tab = nullptr) {
     const int64_t e_slot = slot_of(p.attn, b, j);
     const int64_t i_slot = ICPL > 0 ? slot_of(p.idx, b, j) : -1;
     if (e_slot == -2 || i_slot == -2) raise_err(p.err, V4A_DEV_BAD_PAGE);
@@ -238,7 +250,7 @@ struct CompressKernel {
       load_f<float, CPL>(p.gamma + lane * CPL, g);
 #pragma unroll
       for (int k = 0; k < CPL; ++k) c[k] = c[k] * inv * g[k];
-      rope_lane<CPL>(p.rope, c, lane, j * p.S);
+      rope_lane<CPL>(p.rope, c, lane, j * p.S, rope_tab);
       store_row<CPL>(p.attn, e_slot, c, lane);
     }
     if constexpr (ICPL > 0) {
@@ -411,7 +423,10 @@ struct CompressTile {
   static constexpr int kTT = 32;                    // new tokens per tile
   static constexpr int kMaxW = 8;                   // window tokens the staging holds
   static constexpr int kRows = kTT + kMaxW - 1;     // staged rows
-  static constexpr int kWarps = 8, kThreads = kWarps * 32;
+  // Two groups of 8 warps, each with its own staging buffer: while one group computes a
+  // tile the other computes the next (or waits for its copy), so each SM issues from 16
+  // warps; group g takes the CTA's tiles j = g, g + 2, ...
+  static constexpr int kWarps = 8, kGroups = 2, kThreads = kGroups * kWarps * 32;
   static constexpr int kMaxSeq = 1023;              // sequences of a call on this path (the
                                                     // 256 threads write prefix[0 .. kMaxSeq])
   static constexpr int kRowBytes = (2 * D + 2 * DI) * (int)sizeof(TIn);
@@ -506,7 +521,7 @@ struct CompressTile {
 
   // All warps: the window and residual rows of the tile's tokens, then its entries.
   static __device__ void compute(const CompressParams& p, const Tile& t, const uint8_t* st, int warp,
-                                 int lane) {
+                                 int lane, const float* rope_tab) {
     const int W = p.W, S = p.S;
     const TIn* kv_s = reinterpret_cast<const TIn*>(st);
     const TIn* s_s = reinterpret_cast<const TIn*>(st + kOffS);
@@ -520,7 +535,7 @@ struct CompressTile {
       if (sw >= 0) {
         float y[CPL];
         K::template load_g<TIn, CPL>(kv_s + k * D + lane * CPL, y);
-        K::template rope_lane<CPL>(p.rope, y, lane, pos);
+        K::template rope_lane<CPL>(p.rope, y, lane, pos, rope_tab);
         K::template store_row<CPL>(p.swa, sw, y, lane);
       } else if (sw == -2) {
         raise_err(p.err, V4A_DEV_BAD_PAGE);
@@ -554,8 +569,9 @@ struct CompressTile {
     const int64_t c0 = p.win_off + W - 1;
     int64_t tt0 = max(t.pa, c0);
     tt0 += (S - (tt0 - c0) % S) % S;
-    for (int64_t tt = tt0 + (int64_t)warp * S; tt < t.pa + t.n; tt += (int64_t)kWarps * S) {
-      const int64_t j = (tt - c0) / S;
+    const int64_t j0 = (tt0 - c0) / S;            // entry completed at tt0 (one division a tile)
+    int64_t j = j0 + warp;
+    for (int64_t tt = tt0 + (int64_t)warp * S; tt < t.pa + t.n; tt += (int64_t)kWarps * S, j += kWarps) {
       const int ko = (int)(tt - t.pa);            // staged row of the window's first token
       K::build_entry(p, t.b, j, lane, [&](int o, WindowRow& w) -> int {
         const int k = ko + o;
@@ -568,7 +584,7 @@ struct CompressTile {
           w.is = is_s + k * DI;
         }
         return 1;
-      });
+      }, rope_tab);
     }
   }
 
@@ -579,7 +595,9 @@ struct CompressTile {
     int* prefix = reinterpret_cast<int*>(sm + kOffPrefix);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBar);
     volatile int* abort_flag = reinterpret_cast<int*>(sm + kOffMisc);
-    __shared__ int warp_tot[kWarps];
+    __shared__ int warp_tot[kGroups * kWarps];
+    __shared__ float rope_tab[4 * kMaxRopePairs];
+    stage_rope(p.rope, rope_tab, threadIdx.x, kThreads);   // read after the barriers below
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
       tc::mbar_init(full, 1);
@@ -610,7 +628,7 @@ struct CompressTile {
     __syncthreads();
     int before = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) before += w < warp ? warp_tot[w] : 0;
+    for (int w = 0; w < kGroups * kWarps; ++w) before += w < warp ? warp_tot[w] : 0;
     int run_sum = before + incl - sum;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -622,40 +640,48 @@ struct CompressTile {
     const int total = prefix[p.n_seq];
     pdl_wait();   // residual rows may come from the previous kernel; every pool write waits
 
+    const int grp = warp / kWarps, gw = warp % kWarps;
+    uint8_t* stage = sm + grp * kStage;
+    uint64_t* bar = full + grp;
+    // barrier of the group's 256 threads (ids 1 and 2; 0 is __syncthreads); reports whether
+    // every thread of the group passed `pred`
+    auto group_sync_and = [&](bool pred) -> bool {
+      uint32_t r;
+      asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+                   : "=r"(r)
+                   : "r"((uint32_t)pred), "r"(1 + grp), "r"(kWarps * 32)
+                   : "memory");
+      return r != 0;
+    };
     Tile t;
-    if (warp == 0) {
-      for (int i = 0; i < 2; ++i) {
-        const int k = blockIdx.x + i * gridDim.x;
-        if (tile_of(p, prefix, k, t)) issue(p, t, sm + i * kStage, full + i, lane);
-      }
+    if (gw == 0) {
+      const int k = blockIdx.x + grp * gridDim.x;
+      if (tile_of(p, prefix, k, t)) issue(p, t, stage, bar, lane);
     }
-    int i = 0;
+    int i = 0;                                     // tiles of this group so far
     bool ok = true;
-    for (int k = blockIdx.x; k < total; k += gridDim.x, ++i) {
+    for (int k = blockIdx.x + grp * gridDim.x; k < total; k += kGroups * gridDim.x, ++i) {
       tile_of(p, prefix, k, t);
-      // every thread takes the same decision, so the block barriers below always pair up
-      const bool got = tc::mbar_wait(full + (i & 1), (i >> 1) & 1, abort_flag, p.err);
-      if (!__syncthreads_and(got)) { ok = false; break; }
-      compute(p, t, sm + (i & 1) * kStage, warp, lane);
-      __syncthreads();                             // every warp is done with the stage
-      if (warp == 0) {
-        const int k2 = k + 2 * gridDim.x;
+      // every thread of the group takes the same decision, so its barriers always pair up
+      const bool got = tc::mbar_wait(bar, i & 1, abort_flag, p.err);
+      if (!group_sync_and(got)) { ok = false; break; }
+      compute(p, t, stage, gw, lane, rope_tab);
+      group_sync_and(true);                        // every warp of the group is done with the stage
+      if (gw == 0) {
+        const int k2 = k + kGroups * gridDim.x;
         tc::fence_proxy_async();                  // reads of the stage before the next copy
-        if (tile_of(p, prefix, k2, t)) issue(p, t, sm + (i & 1) * kStage, full + (i & 1), lane);
+        if (tile_of(p, prefix, k2, t)) issue(p, t, stage, bar, lane);
       }
     }
-    if (!ok && tid == 0) {                         // copies still in flight land before exit
-      for (int u = 0; u < 2; ++u) {
-        const int k = blockIdx.x + (i + u) * gridDim.x;
-        if (k < total) tc::mbar_wait_drain(full + ((i + u) & 1), ((i + u) >> 1) & 1);
-      }
+    if (!ok && gw == 0 && lane == 0) {             // a copy still in flight lands before exit
+      if (blockIdx.x + (int64_t)(grp + kGroups * i) * gridDim.x < total) tc::mbar_wait_drain(bar, i & 1);
     }
     __syncthreads();
   }
 };
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
-__global__ void __launch_bounds__(256, 1) compress_tile_kernel(const __grid_constant__ CompressParams p) {
+__global__ void __launch_bounds__(512, 1) compress_tile_kernel(const __grid_constant__ CompressParams p) {
   pdl_trigger();
   CompressTile<TIn, CPL, ICPL, kFp8>::run(p);
 }

@@ -69,11 +69,13 @@ constexpr int threads_of() { return kFp4 ? 512 : 480; }
 
 // A stage: the e4m3 operand of a tile (swizzled, fed to the product), for fp4 the two
 // packed pages it is expanded from, then the two pages' ids (-1: no page, -2: id outside
-// the pool). Stages stay 1 KB aligned for the swizzled layout.
+// the pool) and, from kScaleOff, the two pages' 64 row scales each (copied with the codes).
+// Stages stay 1 KB aligned for the swizzled layout.
 template <bool kFp4>
 struct StageGeo {
   static constexpr int kPackOff = kStageBytes;                          // fp4 only
   static constexpr int kMetaOff = kFp4 ? kStageBytes + 2 * kPackedPageBytes : kStageBytes;
+  static constexpr int kScaleOff = kMetaOff + 16;
   static constexpr int kStride = kMetaOff + 1024;
 };
 
@@ -421,14 +423,22 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
     const int ph = pw & 1, parity = kFp4 ? 0 : pw >> 1;
     // The whole warp keeps the page ids of 32 consecutive blocks (16 tiles) of the current
     // sequence in registers, one per lane; lane 0 waits on the ring and issues the copy.
+    // Block tables are caller inputs that no kernel of this library writes: the first
+    // slice is read before waiting for the previous kernel, the pages after.
+    int cache_seq = -1;
+    int64_t cache_blk0 = 0;
+    int32_t cache_page = -1;
+    if (n_units > 0 && start.g < n_groups) {
+      cache_seq = start.seq;
+      cache_blk0 = 2 * (int64_t)start.t;
+      const int64_t b = cache_blk0 + lane;
+      cache_page = b < p.idx.max_blocks ? __ldg(p.idx.bt + (int64_t)cache_seq * p.idx.max_blocks + b) : -1;
+    }
     pdl_wait();
     if (n_units > 0) {
       Walk<NQ> w = start;
       int issued = 0;
       uint32_t had_copy = 0;
-      int cache_seq = -1;
-      int64_t cache_blk0 = 0;
-      int32_t cache_page = -1;
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         if (w.g >= n_groups) break;                    // every role stops at the same tile
@@ -459,15 +469,17 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
           const bool valid = page >= 0 && page < p.idx.n_pages;
           reinterpret_cast<int*>(sb + Geo::kMetaOff)[ph] = valid ? page : (page >= p.idx.n_pages ? -2 : -1);
           if (valid) {
+            // the page's codes, and its 64 row scales (256 bytes) beside them
             if constexpr (kFp4) {
-              tc::mbar_arrive_tx(full + st, kPackedPageBytes);
+              tc::mbar_arrive_tx(full + st, kPackedPageBytes + 256);
               tc::bulk_g2s(sb + Geo::kPackOff + ph * kPackedPageBytes,
                            reinterpret_cast<const uint8_t*>(p.idx.data) + (int64_t)page * kPackedPageBytes,
                            kPackedPageBytes, full + st);
             } else {
-              tc::mbar_arrive_tx(full + st, kPageBytes);
+              tc::mbar_arrive_tx(full + st, kPageBytes + 256);
               tma_load_2d(sb + ph * kPageBytes, &pages, 0, page * 64, full + st);
             }
+            tc::bulk_g2s(sb + Geo::kScaleOff + ph * 256, p.idx.scale + (int64_t)page * 64, 256, full + st);
             copied = true;
           } else {
             tc::mbar_arrive(full + st);
@@ -662,12 +674,11 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
         continue;
       }
       const int tb = i % Lay::kAcc, st = i % Lay::kStages, b = gc & 1;
-      // the tile's page ids arrive with its codes; the row scale load is issued now and
-      // used after the product
+      // the tile's page ids and row scales arrive with its codes
       if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
       const uint8_t* sb = stage + st * Geo::kStride;
       const int page = reinterpret_cast<const int*>(sb + Geo::kMetaOff)[row >> 6];
-      const float sc = page >= 0 ? __ldg(p.idx.scale + (int64_t)page * 64 + (row & 63)) : 0.f;
+      const float sc = page >= 0 ? reinterpret_cast<const float*>(sb + Geo::kScaleOff)[row] : 0.f;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty + st);
       if (!tc::mbar_wait(bfull + b, (gc >> 1) & 1, abort_flag, p.err)) break;   // w / s of the group
