@@ -246,9 +246,17 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x, h = blockIdx.y * 8 + warp;
+  const int64_t pos = __ldg(p.q_pos + qi);
+  // the query's rotation angles, once for the block's eight heads (inputs only)
+  __shared__ float2 cs[kMaxRopePairs];
+  if (threadIdx.x < (p.rope.d_r >> 1)) {
+    float c, sn;
+    rope_cs(p.rope, pos, threadIdx.x, c, sn);
+    cs[threadIdx.x] = make_float2(c, sn);
+  }
+  __syncthreads();
   if (h >= p.H) return;
   const int H = p.H, D = p.D, tail0 = D - p.rope.d_r;
-  const int64_t pos = __ldg(p.q_pos + qi);
   const int64_t row0 = (int64_t)qi * p.n_split * H + h;          // (qi, split 0, h)
   pdl_wait();
   // One round of loads: every split's (m, l) (lane s holds split s, s < 32) and the first
@@ -325,8 +333,8 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
     x[i] = a[i] * inv;
     y[i] = b[i] * inv;
     if (d >= tail0) {
-      float c, sn;
-      rope_cs(p.rope, pos, (d - tail0) >> 1, c, sn);
+      const float2 r = cs[(d - tail0) >> 1];
+      const float c = r.x, sn = r.y;
       const float rx = x[i] * c + y[i] * sn, ry = -x[i] * sn + y[i] * c;
       x[i] = rx;
       y[i] = ry;

@@ -748,6 +748,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+bool encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t n_rows, uint32_t row_bytes,
+                          uint32_t box_bytes, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)n_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 template <int NQ, bool kFp4>
 cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   using Lay = Layout<NQ, kFp4>;
@@ -759,15 +776,8 @@ cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
   if (!kFp4) {
-    auto enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)kDI, (cuuint64_t)p.idx.n_pages * 64};
-    const cuuint64_t strides[1] = {(cuuint64_t)kDI};
-    const cuuint32_t box[2] = {(cuuint32_t)kDI, 64};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.idx.data, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!encode_fn()) return cudaErrorNotSupported;
+    if (!encode_byte_rows_map(&map, p.idx.data, (uint64_t)p.idx.n_pages * 64, kDI, kDI, 64))
       return cudaErrorInvalidValue;
   }
   const int64_t n_groups = (p.n_q + NQ - 1) / NQ;

@@ -1,6 +1,7 @@
 // Launch parameters and launchers of the v4a kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -87,6 +88,11 @@ cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaSt
 int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st);
 int launch_attention(const AttnParams& p, int dtype, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st);
+// A 2-D byte tensor map over n_rows rows of row_bytes at base (16-byte aligned), boxes of
+// box_rows x box_bytes, 128-byte swizzle, elements outside the tensor read as zero. False
+// when the driver entry point is missing or the driver refuses the map.
+bool encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t n_rows, uint32_t row_bytes,
+                          uint32_t box_bytes, uint32_t box_rows);
 int launch_slot_mapping(const CacheView& c, int32_t n, const int32_t* seq, const int64_t* row,
                         int32_t* slots, int32_t* err, cudaStream_t st);
 
