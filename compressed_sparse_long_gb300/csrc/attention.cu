@@ -360,8 +360,12 @@ __global__ void __launch_bounds__(256) attn_merge(const __grid_constant__ AttnPa
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) {
     const int d = 2 * lane + 64 * i;
-    out[d] = Elem<OT>::from_f(x[i]);
-    out[d + 1] = Elem<OT>::from_f(y[i]);
+    if constexpr (std::is_same<OT, __nv_bfloat16>::value) {   // the pair as one 32-bit store
+      *reinterpret_cast<__nv_bfloat162*>(out + d) = __floats2bfloat162_rn(x[i], y[i]);
+    } else {
+      out[d] = Elem<OT>::from_f(x[i]);
+      out[d + 1] = Elem<OT>::from_f(y[i]);
+    }
   }
 }
 

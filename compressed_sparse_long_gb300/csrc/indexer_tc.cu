@@ -428,6 +428,9 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
     int cache_seq = -1;
     int64_t cache_blk0 = 0;
     int32_t cache_page = -1;
+    // the pages' tensor map into the descriptor cache before the first copy needs it
+    if (!kFp4 && lane == 0)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pages)) : "memory");
     if (n_units > 0 && start.g < n_groups) {
       cache_seq = start.seq;
       cache_blk0 = 2 * (int64_t)start.t;
