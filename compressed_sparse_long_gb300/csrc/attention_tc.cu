@@ -352,6 +352,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc(const __grid_constant__ A
       }
       const Item I = make_item(p, it);
       if (I.n_tiles == 0) continue;
+      // ---- before the wait for the previous kernel (which the copies must await), the
+      // window rows into L2: their slots need no top-k list. A prefetch only moves lines
+      // into L2, where the insert's later writes to them land as well. (Prefetching the rows
+      // of later tiles, or every row of a dense item, measured slower.)
+      for (int t = 0; t < I.n_tiles && !waited; ++t) {
+        if (((gi + t) & 1) != gb) continue;
+        const int64_t x = I.x0 + (int64_t)t * kTile + wg * 32 + lane;
+        if (x < I.n_ent) continue;
+        bool is_swa;
+        const int64_t slot = key_slot(p, I, x, is_swa, false);
+        if (slot >= 0) {
+          const CacheView& cv = is_swa ? p.swa : p.attn;
+          const uint8_t* rowp = reinterpret_cast<const uint8_t*>(cv.data) + slot * (int64_t)cv.width;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp), "r"(kD) : "memory");
+        }
+      }
       // ---- Q~ of this item; the buffer is free once the previous item's S^T products are
       if (ni > 0 && !tc::mbar_wait(qempty, (ni - 1) & 1, abort_flag, p.err)) { ok = false; break; }
       {
