@@ -81,24 +81,35 @@ struct StageGeo {
 
 template <int NQ, bool kFp4>
 struct Layout {
-  static constexpr int N = NQ * 2 * kHI;    // hi and lo rows of each query
+  static constexpr int N = NQ * 2 * kHI;    // B rows: hi and lo rows of each query
+  // NQ = 4 (long prefill chunks): each query's hi and lo products accumulate into the same
+  // 64 columns (B rows: the four queries' hi rows, then their lo rows; two N = 256 products
+  // per K step), so a tile's accumulator is 256 columns and two fit in TMEM. A key tile then
+  // feeds four queries: half the key copies of NQ = 2, whose tile period was set by the
+  // copies (~0.77 us a tile with the 8-stage ring full and ~5 us from issue to landing).
+  static constexpr bool kFused = NQ == 4;
+  static constexpr int NC = kFused ? NQ * kHI : N;   // accumulator columns of a tile
   // fp8: even, tiles alternate producer pairs; fp4: the stage holds the packed pages too.
   // Shallow rings measured faster for the decode grid (a CTA streams only ~14 tiles and a
   // deep ring floods DRAM with requests that delay its first tiles): fp8 with one query
   // per group 4 stages (49.6 us per decode step against 51.0 with 10), fp4 6.
-  static constexpr int kStages = kFp4 ? 6 : (NQ == 1 ? 4 : 8);
+  // NQ = 4: two 64 KB query operands leave room for 4 stages (8 stages and one operand
+  // buffer measured the same on long rows and stall at every group change on short ones).
+  static constexpr int kStages = kFp4 ? 6 : (NQ == 1 || NQ == 4 ? 4 : 8);
+  static constexpr int kBBuf = 2;   // query operand buffers (the next group's is built meanwhile)
   static constexpr int kBBytes = N * kDI;   // fp8 B operand of one group
-  static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators (512 columns)
-  static constexpr int kTmemCols = kAcc * N;
+  static constexpr int kAcc = kFused ? 512 / NC : (NQ == 1 ? 4 : 2);   // TMEM accumulators
+  static constexpr int kTmemCols = kAcc * NC;
   static constexpr int off_stage = 0;
   static constexpr int off_b = kStages * StageGeo<kFp4>::kStride;  // 1 KB aligned
-  static constexpr int off_w = off_b + 2 * kBBytes;               // w_h / s_h [2][NQ * 64]
+  static constexpr int off_w = off_b + kBBuf * kBBytes;           // w_h / s_h [kBBuf][NQ * 64]
   static constexpr int off_bar = off_w + 2 * NQ * kHI * 4;
   static constexpr int n_bar = (kFp4 ? 3 : 2) * kStages + 2 * kAcc + 6 + 1;
   static constexpr int off_misc = off_bar + n_bar * 8;
   static constexpr int bytes = off_misc + 128 + 1024;  // + alignment slack
   static_assert(off_b % 1024 == 0, "swizzled operands need 1 KB alignment");
   static_assert(bytes <= 227 * 1024, "shared memory of one CTA");
+  static_assert(kFp4 || kStages % 2 == 0, "a stage's tiles keep one parity (producer pair, epilogue set)");
 };
 
 // tcgen05.mma kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format
@@ -299,11 +310,11 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
   if (tid == 0) {
     for (int i = 0; i < Lay::kStages; ++i) {
       tc::mbar_init(full + i, 2);           // the tile's two page producers
-      tc::mbar_init(empty + i, 5);          // the tile's products + its four epilogue warps
+      tc::mbar_init(empty + i, Lay::kFused ? 9 : 5);   // the tile's products + its epilogue warps
     }
     for (int i = 0; i < Lay::kAcc; ++i) {
       tc::mbar_init(tfull + i, 1);
-      tc::mbar_init(tempty + i, 4);
+      tc::mbar_init(tempty + i, Lay::kFused ? 8 : 4);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bfull + i, kProd1 - kPrep0);   // the preparation warps
@@ -413,7 +424,8 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
     }
   }
 
-  constexpr uint32_t idesc = idesc_e4m3(kTile, N);
+  constexpr int NC = Lay::NC;
+  constexpr uint32_t idesc = idesc_e4m3(kTile, Lay::kFused ? NQ * kHI : N);
 
   if (warp == 0 || (warp >= kProd1 && warp < (kFp4 ? kProd1 + 1 : kProd1 + 3))) {
     // ------------------------------------------------------------------ producers
@@ -510,7 +522,7 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
         if (w.g >= n_groups) break;
         if (w.g != prev_g) {
           ++gc;
-          if (!__all_sync(0xffffffffu, tc::mbar_wait(bfull + (gc & 1), (gc >> 1) & 1, abort_flag, p.err))) break;
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(bfull + gc % Lay::kBBuf, (gc / Lay::kBBuf) & 1, abort_flag, p.err))) break;
           prev_g = w.g;
         }
         const int st = i % Lay::kStages, tb = i % Lay::kAcc;
@@ -522,15 +534,26 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
         const int g_here = w.g;
         w.next(p, n_groups);
         if (lane == 0) {
-          const uint32_t d = tmem + tb * N;
+          const uint32_t d = tmem + tb * NC;
           const uint64_t ad0 = tc::sdesc_sw128(s0 + st * Geo::kStride, 16, 1024);
-          const uint64_t bd0 = tc::sdesc_sw128(b0 + (gc & 1) * Lay::kBBytes, 16, 1024);
+          const uint64_t bd0 = tc::sdesc_sw128(b0 + (gc % Lay::kBBuf) * Lay::kBBytes, 16, 1024);
+          if constexpr (Lay::kFused) {
+            // the hi rows then the lo rows (NQ * 64 rows each; 128-byte rows in 1 KB atoms of
+            // 8, so row r starts 8 r descriptor units in), both into the same columns
 #pragma unroll
-          for (int k = 0; k < kDI / 32; ++k)   // K = 32 codes = 32 bytes = 2 descriptor units
-            mma_e4m3(d, ad0 + (uint64_t)(2 * k), bd0 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int k = 0; k < kDI / 32; ++k)
+                mma_e4m3(d, ad0 + (uint64_t)(2 * k), bd0 + (uint64_t)(part * NQ * kHI * 8 + 2 * k), idesc,
+                         (k > 0 || part > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < kDI / 32; ++k)   // K = 32 codes = 32 bytes = 2 descriptor units
+              mma_e4m3(d, ad0 + (uint64_t)(2 * k), bd0 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+          }
           tc::mma_commit(empty + st);
           tc::mma_commit(tfull + tb);
-          if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty + (gc & 1));
+          if (w.g != g_here || i == n_units - 1) tc::mma_commit(bempty + gc % Lay::kBBuf);
         }
         __syncwarp();
       }
@@ -589,9 +612,9 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
       if (w.g != prev_g) {
         ++gc;
         prev_g = w.g;
-        const int b = gc & 1;
-        if (gc >= 2) {   // the buffer's previous group: its products and epilogue are done
-          const uint32_t par = ((gc >> 1) - 1) & 1;
+        const int b = gc % Lay::kBBuf;
+        if (gc >= Lay::kBBuf) {   // the buffer's previous group: its products and epilogue are done
+          const uint32_t par = ((gc / Lay::kBBuf) - 1) & 1;
           if (!tc::mbar_wait(bempty + b, par, abort_flag, p.err)) break;
           if (!tc::mbar_wait(egone + b, par, abort_flag, p.err)) break;
         }
@@ -646,8 +669,10 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
               lw[k] = lp;
             }
             const int chunk = dh * 4 + c;               // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4*>(bb + tc::sw128_off(qq * 128 + h, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(bb + tc::sw128_off(qq * 128 + 64 + h, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            const int r_hi = Lay::kFused ? qq * kHI + h : qq * 128 + h;
+            const int r_lo = Lay::kFused ? (NQ + qq) * kHI + h : qq * 128 + 64 + h;
+            *reinterpret_cast<uint4*>(bb + tc::sw128_off(r_hi, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(bb + tc::sw128_off(r_lo, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
           if (dh == 0) wsm[b * NQ * kHI + qq * kHI + h] = wh * inv_s;
         }
@@ -668,15 +693,15 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
     for (int i = 0; i < n_units; ++i) {
       if (w.g >= n_groups) break;
       if (w.g != prev_g) {
-        if (gc >= 0 && lane == 0) tc::mbar_arrive(egone + (gc & 1));   // left the previous group
+        if (gc >= 0 && lane == 0) tc::mbar_arrive(egone + gc % Lay::kBBuf);   // left the previous group
         ++gc;
         prev_g = w.g;
       }
-      if ((i & 1) != es) {
+      if (!Lay::kFused && (i & 1) != es) {
         w.next(p, n_groups);
         continue;
       }
-      const int tb = i % Lay::kAcc, st = i % Lay::kStages, b = gc & 1;
+      const int tb = i % Lay::kAcc, st = i % Lay::kStages, b = gc % Lay::kBBuf;
       // the tile's page ids and row scales arrive with its codes
       if (!tc::mbar_wait(full + st, (i / Lay::kStages) & 1, abort_flag, p.err)) break;
       const uint8_t* sb = stage + st * Geo::kStride;
@@ -684,48 +709,107 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
       const float sc = page >= 0 ? reinterpret_cast<const float*>(sb + Geo::kScaleOff)[row] : 0.f;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty + st);
-      if (!tc::mbar_wait(bfull + b, (gc >> 1) & 1, abort_flag, p.err)) break;   // w / s of the group
+      if (!tc::mbar_wait(bfull + b, (gc / Lay::kBBuf) & 1, abort_flag, p.err)) break;   // w / s of the group
       if (!tc::mbar_wait(tfull + tb, (i / Lay::kAcc) & 1, abort_flag, p.err)) break;
       tc::fence_after_sync();
       const int seq = w.seq;
       const int64_t j = (int64_t)w.t * kTile + row;
       const float* wq = wsm + b * NQ * kHI;
-#pragma unroll
-      for (int qq = 0; qq < NQ; ++qq) {
-        if (w.G.seq[qq] != seq) continue;           // warp-uniform
+      if constexpr (Lay::kFused) {
+        // Both sets take every tile, set es queries 2 es and 2 es + 1, so an accumulator is
+        // free after half the epilogue time (the products of tile i + 2 wait for it), and
+        // it is released as soon as its last columns are in registers. Queries of another
+        // sequence are computed and dropped (their columns hold products with this
+        // sequence's keys). Four chunks of 32 heads (query 2 es: chunks 0, 1; query 2 es + 1:
+        // chunks 2, 3), each chunk's load in flight while the previous one is reduced.
+        const uint32_t c0 = tmem + ((uint32_t)(quad * 32) << 16) + tb * NC + 2 * es * kHI;
+        const float* wc = wq + 2 * es * kHI;
         float s4[4] = {0.f, 0.f, 0.f, 0.f};       // four chains instead of one
+        float sq[2];
+        auto reduce = [&](const float (&v)[32], int c) {
+          const float4* w4 = reinterpret_cast<const float4*>(wc + c * 32);
 #pragma unroll
-        for (int qt = 0; qt < 4; ++qt) {          // 16 heads at a time (fewer live registers)
-          float hi[16], lo[16];
-          const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + tb * N + qq * 128 + qt * 16;
-          tc::tmem_ld16(col, hi);
-          tc::tmem_ld16(col + 64, lo);
-          tc::tmem_wait_ld();
-          const float4* w4 = reinterpret_cast<const float4*>(wq + qq * kHI + qt * 16);
-#pragma unroll
-          for (int h4 = 0; h4 < 4; ++h4) {
+          for (int h4 = 0; h4 < 8; ++h4) {
             const float4 ww = w4[h4];
-            s4[0] = fmaf(ww.x, fmaxf(hi[4 * h4] + lo[4 * h4], 0.f), s4[0]);
-            s4[1] = fmaf(ww.y, fmaxf(hi[4 * h4 + 1] + lo[4 * h4 + 1], 0.f), s4[1]);
-            s4[2] = fmaf(ww.z, fmaxf(hi[4 * h4 + 2] + lo[4 * h4 + 2], 0.f), s4[2]);
-            s4[3] = fmaf(ww.w, fmaxf(hi[4 * h4 + 3] + lo[4 * h4 + 3], 0.f), s4[3]);
+            s4[0] = fmaf(ww.x, fmaxf(v[4 * h4], 0.f), s4[0]);
+            s4[1] = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), s4[1]);
+            s4[2] = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), s4[2]);
+            s4[3] = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), s4[3]);
+          }
+        };
+        {
+          float va[32], vb[32];
+          tc::tmem_ld32(c0, va);
+          tc::tmem_wait_ld();
+          tc::tmem_ld32(c0 + 32, vb);
+          reduce(va, 0);
+          tc::tmem_wait_ld();
+          tc::tmem_ld32(c0 + 64, va);
+          reduce(vb, 1);
+          sq[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+          tc::tmem_wait_ld();
+          tc::tmem_ld32(c0 + 96, vb);
+          reduce(va, 2);
+          tc::tmem_wait_ld();
+          tc::fence_before_sync();                // every column of the tile is in registers
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tempty + tb);
+          reduce(vb, 3);
+          sq[1] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int qq = 2 * es + u;
+          if (pick4(w.G.seq, qq) == seq && j < pick4(w.G.nvis, qq) && w.g * NQ + qq < p.n_q) {
+            float out;
+            if (page >= 0) {
+              out = sq[u] * sc + 0.0f;
+            } else {
+              raise_err(p.err, page == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+              out = -INFINITY;
+            }
+            p.scores[(int64_t)(w.g * NQ + qq) * p.row_stride + j] = out;
           }
         }
-        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        if (j < w.G.nvis[qq] && w.g * NQ + qq < p.n_q) {
-          float out;
-          if (page >= 0) {
-            out = s * sc + 0.0f;
-          } else {
-            raise_err(p.err, page == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
-            out = -INFINITY;
+      } else {
+#pragma unroll
+        for (int qq = 0; qq < NQ; ++qq) {
+          if (w.G.seq[qq] != seq) continue;         // warp-uniform
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};     // four chains instead of one
+#pragma unroll
+          for (int qt = 0; qt < 4; ++qt) {        // 16 heads at a time (fewer live registers)
+            float hi[16], lo[16];
+            const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + tb * NC + qq * 128 + qt * 16;
+            tc::tmem_ld16(col, hi);
+            tc::tmem_ld16(col + 64, lo);
+            tc::tmem_wait_ld();
+            const float4* w4 = reinterpret_cast<const float4*>(wq + qq * kHI + qt * 16);
+#pragma unroll
+            for (int h4 = 0; h4 < 4; ++h4) {
+              const float4 ww = w4[h4];
+              s4[0] = fmaf(ww.x, fmaxf(hi[4 * h4] + lo[4 * h4], 0.f), s4[0]);
+              s4[1] = fmaf(ww.y, fmaxf(hi[4 * h4 + 1] + lo[4 * h4 + 1], 0.f), s4[1]);
+              s4[2] = fmaf(ww.z, fmaxf(hi[4 * h4 + 2] + lo[4 * h4 + 2], 0.f), s4[2]);
+              s4[3] = fmaf(ww.w, fmaxf(hi[4 * h4 + 3] + lo[4 * h4 + 3], 0.f), s4[3]);
+            }
           }
-          p.scores[(int64_t)(w.g * NQ + qq) * p.row_stride + j] = out;
+          const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          if (j < w.G.nvis[qq] && w.g * NQ + qq < p.n_q) {
+            float out;
+            if (page >= 0) {
+              out = s * sc + 0.0f;
+            } else {
+              raise_err(p.err, page == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+              out = -INFINITY;
+            }
+            p.scores[(int64_t)(w.g * NQ + qq) * p.row_stride + j] = out;
+          }
         }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tempty + tb);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty + tb);
       w.next(p, n_groups);
     }
   }
@@ -797,13 +881,15 @@ cudaError_t launch_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
 }  // namespace
 
 // Tensor-core path for bf16 queries and fp8 keys with 64 heads of dim 128. Many queries
-// (prefill) are taken two at a time (N = 256) so each key tile feeds two queries.
+// (prefill) are taken two at a time (N = 256), or four (two N = 256 products per K step,
+// hi and lo terms summed in the accumulator), so that each key tile feeds several queries.
 cudaError_t launch_index_scores_tc(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   if (p.idx.n_pages <= 0 || p.idx.n_pages * 64 > INT32_MAX) return cudaErrorInvalidValue;
   if (p.idx_fp4) {
     if (p.n_q >= 1024) return launch_tc<2, true>(p, max_vis, st);
     return launch_tc<1, true>(p, max_vis, st);
   }
+  if (p.n_q >= 4096) return launch_tc<4, false>(p, max_vis, st);
   if (p.n_q >= 1024) return launch_tc<2, false>(p, max_vis, st);
   return launch_tc<1, false>(p, max_vis, st);
 }

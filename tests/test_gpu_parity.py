@@ -774,13 +774,16 @@ def _score_bound(spec, dp, seq, pos, q_idx, w):
 
 
 @pytest.mark.parametrize("case", ["fp8_decode", "fp4_decode", "fp8_prefill", "fp8_prefill_pairs",
-                                  "fp4_prefill_pairs", "fp32_tiny"])
+                                  "fp8_prefill_quads", "fp4_prefill_pairs", "fp32_tiny"])
 def test_index_scores_elementwise(case):
     """v4a_index_scores against the oracle's scores, element by element, for every visible
     entry of every query: |gpu - oracle| <= 3e-5 x the row's a-priori rounding bound (fp32
     accumulation of exact products, 2^-17 relative loss of the split query below the e4m3
     subnormal step). The pair cases run the kernel that takes two queries per key tile and
-    accumulates the query's two e4m3 terms in one product."""
+    accumulates the query's two e4m3 terms in one product; the quads case (>= 4096 queries over
+    four sequences with ragged chunks, so groups of four straddle sequence boundaries) runs the
+    kernel that takes four queries per key tile and accumulates each query's two terms in the
+    same accumulator columns."""
     if case == "fp8_decode":
         w = wl.c4a_decode(seed=51, B=8, L=8192)
         _inject_subnormal_keys(w.layers[0], np.random.default_rng(52))
@@ -790,6 +793,17 @@ def test_index_scores_elementwise(case):
         w = wl.c4a_prefill(seed=54, cached=8192, chunk=300)
     elif case == "fp8_prefill_pairs":        # >= 1024 queries: two queries per key tile
         w = wl.c4a_prefill(seed=56, cached=8192, chunk=1024)
+    elif case == "fp8_prefill_quads":        # >= 4096 queries: four queries per key tile
+        spec = wl.LayerSpec("c4a", True)
+        rng = np.random.default_rng(58)
+        ctx, new = [1000, 37, 127, 2048], [1501, 1, 1298, 1303]
+        h = wl.make_layer(rng, spec, ctx, new, prefill_cache=True)
+        h.bias, h.gamma, h.ibias = wl.layer_params(rng, spec)
+        seq = np.repeat(np.arange(4), new)
+        pos = np.concatenate([c + np.arange(n) for c, n in zip(ctx, new)])
+        w = wl.Workload("ragged quads", [h], wl.make_batch(rng, spec, ctx, new),
+                        wl.make_queries(rng, spec, seq, pos, False))
+        assert len(seq) >= 4096 and len(seq) % 4 != 0
     elif case == "fp4_prefill_pairs":
         w = wl.c4a_prefill(seed=57, cached=8192, chunk=1024, idx_fp4=True)
     else:
