@@ -414,7 +414,7 @@ __device__ __forceinline__ void top_digit(const uint32_t* h, uint32_t need, uint
   }
 }
 
-__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __grid_constant__ IndexParams p) {
+__global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __grid_constant__ IndexParams p) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bh[kStreamBuckets];           // bucket histogram; radix histograms after
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
   __shared__ int32_t cidx[kStreamCap];              // entry index,
   __shared__ uint8_t cin[kStreamCap];               // 1 = in the boundary bucket
   __shared__ int32_t sel[kStreamCap];               // selected entry indices
-  __shared__ float s_lo[kStreamWarps], s_hi[kStreamWarps];
+  __shared__ float s_lo[kStreamWarps], s_hi[kStreamWarps], s_fl[kStreamWarps];
   __shared__ uint32_t warp_tot[kStreamWarps];
   __shared__ uint32_t s_bucket, s_above, s_nc, s_digit, s_need, s_total;
   const int qi = blockIdx.x;
@@ -459,8 +459,33 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
       }
     }
   };
-  // ---- pass 1: extremes (a NaN score sends the row to the radix passes)
+  // ---- pass 1: extremes (a NaN score sends the row to the radix passes), and the four
+  // largest of each thread's group maxima (each group of four loaded entries gives one,
+  // a distinct entry). Warp w's candidates (four per lane) give its key T_w: the
+  // ceil(k / warps)-th largest among them; the warp has that many entries at or above T_w,
+  // so at least k entries of the row score at or above the floor min_w T_w, and the k
+  // largest are among them (usually a few hundred beyond k; needs k <= 4 x 256).
   float lo = INFINITY, hi = -INFINITY;
+  float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
+  auto top4 = [&](float x) {
+    if (x > t3) {
+      if (x > t1) {
+        t3 = t2;
+        t2 = t1;
+        if (x > t0) {
+          t1 = t0;
+          t0 = x;
+        } else {
+          t1 = x;
+        }
+      } else if (x > t2) {
+        t3 = t2;
+        t2 = x;
+      } else {
+        t3 = x;
+      }
+    }
+  };
   bool nan = false;
   for (int64_t i0 = (int64_t)tid * 4; i0 < n; i0 += kStep * kUnroll) {
     float4 x[kUnroll];
@@ -478,30 +503,103 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (i0 + u * kStep >= n) continue;
+      const int64_t i = i0 + u * kStep;
+      if (i >= n) continue;
       lo = fminf(lo, fminf(fminf(x[u].x, x[u].y), fminf(x[u].z, x[u].w)));
-      hi = fmaxf(hi, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+      const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+      hi = fmaxf(hi, m4);
       nan |= (x[u].x != x[u].x) | (x[u].y != x[u].y) | (x[u].z != x[u].z) | (x[u].w != x[u].w);
+      top4(m4);   // one entry of each group of four (the copies past n repeat its first)
     }
+  }
+  float fl = -INFINITY;
+  if (k <= 4u * kStreamThreads) {
+    const uint32_t need_w = (k + kStreamWarps - 1) / kStreamWarps;
+    const uint32_t u0 = order_key(t0), u1 = order_key(t1), u2 = order_key(t2), u3 = order_key(t3);
+    uint32_t T = 0;                                 // bitwise search from the top bit
+#pragma unroll 1
+    for (int b = 31; b >= 0; --b) {
+      const uint32_t c = T | (1u << b);
+      const uint32_t cnt = __popc(__ballot_sync(0xffffffffu, u0 >= c)) + __popc(__ballot_sync(0xffffffffu, u1 >= c)) +
+                           __popc(__ballot_sync(0xffffffffu, u2 >= c)) + __popc(__ballot_sync(0xffffffffu, u3 >= c));
+      if (cnt >= need_w) T = c;
+    }
+    fl = key_value(T);                              // -inf when the warp lacks candidates
   }
   if (nan) hi = INFINITY;
   lo = warp_min_f(lo);
   hi = warp_max_f(hi);
-  if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; s_fl[warp] = fl; }
   for (int i = tid; i < kStreamBuckets; i += kStreamThreads) bh[i] = 0u;
   if (tid == 0) s_nc = 0u;
   __syncthreads();
   lo = INFINITY;
   hi = -INFINITY;
+  fl = INFINITY;
 #pragma unroll
   for (int w = 0; w < kStreamWarps; ++w) {
     lo = fminf(lo, s_lo[w]);
     hi = fmaxf(hi, s_hi[w]);
+    fl = fminf(fl, s_fl[w]);
   }
   const float span = hi - lo;
   bool bucketed = span > 0.f && span <= 3.0e38f;   // block-uniform
-  uint32_t kth = 0, remaining = 0;
-  if (bucketed) {
+  uint32_t kth = 0, remaining = 0, above = 0;
+  int bstar = 0;
+  // ---- pass 2: collect every entry at or above the floor (usually a few percent of the
+  // row) with warp-aggregated appends, one shared-memory atomic per warp and iteration
+  bool have = false;                                // candidates collected (block-uniform)
+  if (!nan && fl > -INFINITY) {
+    constexpr int kU2 = 4;                          // (fewer live registers than kUnroll)
+    for (int64_t i0 = (int64_t)tid * 4; i0 - (int64_t)lane * 4 < n; i0 += kStep * kU2) {
+      float4 x[kU2];
+#pragma unroll
+      for (int u = 0; u < kU2; ++u) {
+        const int64_t i = i0 + u * kStep;
+        x[u] = i < n ? __ldg(reinterpret_cast<const float4*>(row + i))
+                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int u = 0; u < kU2; ++u) {
+        const int64_t i = i0 + u * kStep;
+        cnt += (i < n && x[u].x >= fl) + (i + 1 < n && x[u].y >= fl) + (i + 2 < n && x[u].z >= fl) +
+               (i + 3 < n && x[u].w >= fl);
+      }
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t base = 0;
+      if (lane == 31 && incl) base = atomicAdd(&s_nc, incl);
+      uint32_t at = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      if (cnt) {
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+          const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t i = i0 + u * kStep + e;
+            if (i < n && v[e] >= fl) {
+              if (at < (uint32_t)kStreamCap) {
+                ckey[at] = order_key(v[e]);
+                cidx[at] = (int32_t)i;
+                cin[at] = 1;
+              }
+              ++at;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    have = s_nc <= (uint32_t)kStreamCap;
+    __syncthreads();
+    if (!have && tid == 0) s_nc = 0u;               // ordered before pass 4 by its barriers
+  }
+  if (!have && bucketed) {
     const float inv = (float)kStreamBuckets / span;
     auto bucket = [&](float x) -> int {
       return max(0, min((int)((x - lo) * inv), kStreamBuckets - 1));
@@ -532,11 +630,11 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
       }
     }
     __syncthreads();
-    const int bstar = (int)s_bucket;
-    const uint32_t above = s_above;
+    bstar = (int)s_bucket;
+    above = s_above;
     bucketed = above + bh[bstar] <= (uint32_t)kStreamCap;   // block-uniform
     if (bucketed) {
-      // ---- pass 3: collect the entries of buckets >= bstar (warp-aggregated appends)
+      // ---- pass 4: collect the entries of buckets >= bstar (warp-aggregated appends)
       // (the loop bound is the warp's first index, so every lane of a warp runs the same
       // iterations and the ballots are warp-wide)
       for (int64_t i0 = (int64_t)tid * 4; i0 - (int64_t)lane * 4 < n; i0 += kStep * kUnroll) {
@@ -571,72 +669,114 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const __gri
         }
       }
       __syncthreads();
-      const int nc = (int)s_nc;
-      // ---- exact k-th key among the boundary bucket's entries: 8-bit radix passes
-      uint32_t prefix = 0, mask = 0, need = k - above;
+      have = true;
+    }
+  }
+  if (have) {
+    const int nc = (int)s_nc;
+    // ---- exact k-th key among the collected entries flagged in cin (pass 2: all of them;
+    // pass 4: the boundary bucket's, those above it being selected already): 8-bit radix
+    uint32_t prefix = 0, mask = 0, need = k - above;
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += kStreamThreads) bh[i] = 0u;
-        __syncthreads();
-        for (int c = tid; c < nc; c += kStreamThreads)
-          if (cin[c] && (ckey[c] & mask) == prefix) atomicAdd(&bh[(ckey[c] >> shift) & 0xFFu], 1u);
-        __syncthreads();
-        if (warp == 0) top_digit(bh, need, &s_digit, &s_need);
-        __syncthreads();
-        prefix |= s_digit << shift;
-        mask |= 0xFFu << shift;
-        need = s_need;
-      }
-      kth = prefix;
-      remaining = need;              // ties equal to kth still to take, smallest indices first
-      // entries equal to kth: when all of them are taken (the usual case, one entry), no
-      // tie needs its index rank
-      uint32_t n_tie = 0;
-      for (int c = tid; c < nc; c += kStreamThreads) n_tie += (cin[c] && ckey[c] == kth) ? 1u : 0u;
-      stream_excl_sum(n_tie, warp_tot, &s_total);
-      const bool all_ties = s_total <= remaining;
-      // ---- selection: contiguous chunks of the collected entries, one block scan
-      const int per = (nc + kStreamThreads - 1) / kStreamThreads;
-      const int c0 = tid * per, c1 = min(nc, c0 + per);
-      auto selected = [&](int c) -> bool {
-        const uint32_t key = ckey[c];
-        if (!cin[c] || key > kth) return true;
-        if (key != kth) return false;
-        if (all_ties) return true;
-        uint32_t rank = 0;           // ties equal to kth with a smaller index
-        for (int d = 0; d < nc; ++d) rank += (cin[d] && ckey[d] == kth && cidx[d] < cidx[c]) ? 1u : 0u;
-        return rank < remaining;
-      };
-      uint32_t cnt = 0;
-      for (int c = c0; c < c1; ++c) cnt += selected(c) ? 1u : 0u;
-      uint32_t at = stream_excl_sum(cnt, warp_tot, &s_total);
-      for (int c = c0; c < c1; ++c)
-        if (selected(c)) sel[at++] = cidx[c];
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = tid; i < 256; i += kStreamThreads) bh[i] = 0u;
       __syncthreads();
-      // ---- output in ascending index order: a bitonic sort of the selected indices, padded
-      // to a power of two with INT32_MAX
-      const int ns = (int)s_total;   // == k
-      int np2 = 1;
-      while (np2 < ns) np2 <<= 1;
-      for (int i = ns + tid; i < np2; i += kStreamThreads) sel[i] = INT32_MAX;
+      for (int c = tid; c < nc; c += kStreamThreads)
+        if (cin[c] && (ckey[c] & mask) == prefix) atomicAdd(&bh[(ckey[c] >> shift) & 0xFFu], 1u);
       __syncthreads();
-      for (int size = 2; size <= np2; size <<= 1) {
+      if (warp == 0) top_digit(bh, need, &s_digit, &s_need);
+      __syncthreads();
+      prefix |= s_digit << shift;
+      mask |= 0xFFu << shift;
+      need = s_need;
+    }
+    kth = prefix;
+    remaining = need;              // ties equal to kth still to take, smallest indices first
+    // entries equal to kth: when all of them are taken (the usual case, one entry), no
+    // tie needs its index rank
+    uint32_t n_tie = 0;
+    for (int c = tid; c < nc; c += kStreamThreads) n_tie += (cin[c] && ckey[c] == kth) ? 1u : 0u;
+    stream_excl_sum(n_tie, warp_tot, &s_total);
+    const bool all_ties = s_total <= remaining;
+    // ---- selection: contiguous chunks of the collected entries, one block scan
+    const int per = (nc + kStreamThreads - 1) / kStreamThreads;
+    const int c0 = tid * per, c1 = min(nc, c0 + per);
+    auto selected = [&](int c) -> bool {
+      const uint32_t key = ckey[c];
+      if (!cin[c] || key > kth) return true;
+      if (key != kth) return false;
+      if (all_ties) return true;
+      uint32_t rank = 0;           // ties equal to kth with a smaller index
+      for (int d = 0; d < nc; ++d) rank += (cin[d] && ckey[d] == kth && cidx[d] < cidx[c]) ? 1u : 0u;
+      return rank < remaining;
+    };
+    uint32_t cnt = 0;
+    for (int c = c0; c < c1; ++c) cnt += selected(c) ? 1u : 0u;
+    uint32_t at = stream_excl_sum(cnt, warp_tot, &s_total);
+    for (int c = c0; c < c1; ++c)
+      if (selected(c)) sel[at++] = cidx[c];
+    __syncthreads();
+    // ---- output in ascending index order: a bitonic sort of the selected indices, padded
+    // to a power of two with INT32_MAX
+    const int ns = (int)s_total;   // == k
+    if (ns <= 2 * kStreamThreads) {
+      // 512 slots, thread t holding slots 2t and 2t + 1 in registers: strides below 64 pair
+      // threads of one warp (shuffles), the longer ones exchange through shared memory.
+      int32_t a0 = 2 * tid < ns ? sel[2 * tid] : INT32_MAX;
+      int32_t a1 = 2 * tid + 1 < ns ? sel[2 * tid + 1] : INT32_MAX;
+#pragma unroll 1
+      for (int size = 2; size <= 2 * kStreamThreads; size <<= 1) {
+        const bool asc = ((2 * tid) & size) == 0;
+#pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int t = tid; t < (np2 >> 1); t += kStreamThreads) {
-            const int a = 2 * t - (t & (stride - 1)), b = a + stride;
-            const int32_t x0 = sel[a], x1 = sel[b];
-            if ((x0 > x1) == ((a & size) == 0)) {
-              sel[a] = x1;
-              sel[b] = x0;
-            }
+          if (stride == 1) {
+            const int32_t lo2 = min(a0, a1), hi2 = max(a0, a1);
+            a0 = asc ? lo2 : hi2;
+            a1 = asc ? hi2 : lo2;
+            continue;
           }
-          __syncthreads();
+          const int tp = stride >> 1;                 // partner thread: tid ^ tp
+          int32_t w0, w1;
+          if (tp < 32) {
+            w0 = __shfl_xor_sync(0xffffffffu, a0, tp);
+            w1 = __shfl_xor_sync(0xffffffffu, a1, tp);
+          } else {
+            __syncthreads();                          // the previous exchange was read
+            sel[2 * tid] = a0;
+            sel[2 * tid + 1] = a1;
+            __syncthreads();
+            w0 = sel[(2 * tid) ^ stride];
+            w1 = sel[(2 * tid + 1) ^ stride];
+          }
+          const bool lower = (tid & tp) == 0;         // this thread's slots are the pairs' lower
+          a0 = lower == asc ? min(a0, w0) : max(a0, w0);
+          a1 = lower == asc ? min(a1, w1) : max(a1, w1);
         }
       }
-      for (int i = tid; i < ns && i < p.k; i += kStreamThreads) out[i] = sel[i];
+      if (2 * tid < ns) out[2 * tid] = a0;
+      if (2 * tid + 1 < ns) out[2 * tid + 1] = a1;
       return;
     }
+    int np2 = 1;
+    while (np2 < ns) np2 <<= 1;
+    for (int i = ns + tid; i < np2; i += kStreamThreads) sel[i] = INT32_MAX;
+    __syncthreads();
+    for (int size = 2; size <= np2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int t = tid; t < (np2 >> 1); t += kStreamThreads) {
+          const int a = 2 * t - (t & (stride - 1)), b = a + stride;
+          const int32_t x0 = sel[a], x1 = sel[b];
+          if ((x0 > x1) == ((a & size) == 0)) {
+            sel[a] = x1;
+            sel[b] = x0;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < ns && i < p.k; i += kStreamThreads) out[i] = sel[i];
+    return;
   }
   // ---- radix passes over the whole row: the k-th key, then an ordered compaction
   uint32_t* h = bh;
