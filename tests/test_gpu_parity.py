@@ -310,6 +310,25 @@ def test_index_topk_prefill_positions(n_q, k):
     check_topk(topk.cpu().numpy(), ref, scores, k)
 
 
+@pytest.mark.parametrize("k", [64, 512, 1024, 1025, 2048])
+def test_index_topk_streaming_rows(k):
+    """Rows longer than the register-resident selection holds (up to 16,383 entries): the
+    streaming selection with its candidate floor (k <= 1024, each warp's ceil(k / 8)-th
+    largest candidate; 1024 takes every candidate) and without it (k > 1024, the bucket
+    histogram), against the oracle's lists; one row is shorter than k."""
+    w = wl.c4a_prefill(seed=61, cached=65536, chunk=5)
+    h = w.layers[0]
+    q = w.queries
+    q.pos = np.array([65536 + 4, 60001, 40000, 33000, 900], np.int64)
+    lay, x = device_layer(h), DevInputs(w)
+    assert O.visible_entries(h.spec.S, h.spec.W, h.spec.win_off, 65540) > 8192
+    topk = lay.index_topk(x.q_seq, x.q_pos, int(q.pos.max()), x.q_idx, x.w, k=k)
+    pools = oracle_pools(h)
+    ref, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, k)
+    same = check_topk(topk.cpu().numpy(), ref, scores, k)
+    assert len(same) >= len(q.pos) - 1
+
+
 @pytest.mark.parametrize("L", [4096, 65536])
 def test_topk_ties_take_smaller_index(L):
     """Equal scores: identical keys tie exactly; the smaller entry indices win (rows held in
@@ -326,12 +345,15 @@ def test_topk_ties_take_smaller_index(L):
 
 
 @pytest.mark.parametrize("n_tied,rank,L", [(300, 0, 16384), (300, 412, 16384), (1200, 0, 16384),
-                                           (300, 0, 65536), (300, 412, 65536), (1200, 0, 65536)])
+                                           (300, 0, 65536), (300, 412, 65536), (1200, 0, 65536),
+                                           (3000, 0, 65536)])
 def test_topk_tied_block(n_tied, rank, L):
     """A block of identical indexer keys (so identical scores) placed wholly above the k-th
     score, across it, or larger than k at the top of the row: the output holds every entry
     scoring above the block and exactly the smallest-index members of the block (rows of
-    4095 entries held in registers, rows of 16383 in the streaming selection)."""
+    4095 entries held in registers, rows of 16383 in the streaming selection; a block of
+    3000 puts more entries at the streaming selection's floor than its 2048-entry buffer
+    holds, so that row takes the whole-row radix passes)."""
     w = wl.c4a_decode(seed=11, B=2, L=L)
     h = w.layers[0]
     q = w.queries
