@@ -441,6 +441,18 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
   // 16-byte loads in flight (they are issued before any is used).
   constexpr int kUnroll = 8;
   constexpr int64_t kStep = 4 * kStreamThreads;
+  {
+    // the whole row is requested into L2 at once (16 KB per copy), so the first pass's
+    // loads wait on fills already in flight rather than on their own DRAM round trips
+    const int64_t bytes = ((n + 3) & ~(int64_t)3) * 4;
+    const int64_t off = (int64_t)tid * 16384;
+    if (off < bytes) {
+      const uint32_t len = (uint32_t)min((int64_t)16384, bytes - off);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const char*>(row) + off),
+                   "r"(len)
+                   : "memory");
+    }
+  }
   auto for_each4 = [&](auto&& f) {
     for (int64_t i0 = (int64_t)tid * 4; i0 < n; i0 += kStep * kUnroll) {
       float4 x[kUnroll];
