@@ -724,17 +724,18 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
         // chunks 2, 3), each chunk's load in flight while the previous one is reduced.
         const uint32_t c0 = tmem + ((uint32_t)(quad * 32) << 16) + tb * NC + 2 * es * kHI;
         const float* wc = wq + 2 * es * kHI;
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};       // four chains instead of one
+        // four chains (heads h mod 4) in two packed pairs: one paired FMA per two heads
+        float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float sq[2];
         auto reduce = [&](const float (&v)[32], int c) {
           const float4* w4 = reinterpret_cast<const float4*>(wc + c * 32);
 #pragma unroll
           for (int h4 = 0; h4 < 8; ++h4) {
             const float4 ww = w4[h4];
-            s4[0] = fmaf(ww.x, fmaxf(v[4 * h4], 0.f), s4[0]);
-            s4[1] = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), s4[1]);
-            s4[2] = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), s4[2]);
-            s4[3] = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), s4[3]);
+            s2[0] = __ffma2_rn(make_float2(ww.x, ww.y),
+                               make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), s2[0]);
+            s2[1] = __ffma2_rn(make_float2(ww.z, ww.w),
+                               make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), s2[1]);
           }
         };
         {
@@ -746,8 +747,8 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
           tc::tmem_wait_ld();
           tc::tmem_ld32(c0 + 64, va);
           reduce(vb, 1);
-          sq[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-          s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+          sq[0] = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
+          s2[0] = s2[1] = make_float2(0.f, 0.f);
           tc::tmem_wait_ld();
           tc::tmem_ld32(c0 + 96, vb);
           reduce(va, 2);
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(threads_of<kFp4>(), 1) index_scores_tc(const _
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(tempty + tb);
           reduce(vb, 3);
-          sq[1] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          sq[1] = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
