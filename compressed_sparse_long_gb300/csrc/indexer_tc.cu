@@ -16,19 +16,22 @@
 //
 // Tile: M = 128 consecutive c4a entries of one sequence (two 64-entry pages), N = 128 rows
 // per query (64 heads x {hi, lo}) x NQ queries of the same sequence, K = d_I = 128 (four
-// MMAs of K = 32). Entries sit on the M axis so each TMEM lane holds one entry's head dot
-// products and the head sum is a per-thread loop in the epilogue.
+// MMAs of K = 32). With NQ = 4 the hi rows of the four queries and then their lo rows are
+// two N = 256 products per K step accumulating into the same 256 columns (the epilogue's
+// hi + lo is done by the accumulator). Entries sit on the M axis so each TMEM lane holds
+// one entry's head dot products and the head sum is a per-thread loop in the epilogue.
 //
 // One persistent CTA per SM, warp-specialised, every hand-off an mbarrier:
 //   warps 0,12-14 producers: a tile's two pages are copied into one ring stage by two
 //               warps, one per page; even tiles go to warps 0 and 12, odd tiles to 13 and
 //               14 (a warp serialises its bulk copies, ~0.3 us each). Each warp arms the
 //               stage barrier with its own bytes and leaves its page id (or status) there.
-//   warp 1      MMA: allocates TMEM, one thread issues 4 tcgen05.mma per tile into one of
-//               four accumulators (two for two queries per group); commits release the
-//               stage and hand the tile over
+//   warp 1      MMA: allocates TMEM, one thread issues 4 tcgen05.mma per tile (8 with four
+//               queries) into one of four accumulators (two for two or four queries per
+//               group); commits release the stage and hand the tile over
 //   warps 2-9   epilogue, two sets of four (one per TMEM lane quadrant) taking even and
-//               odd tiles: tcgen05.ld, hi + lo, ReLU, weighted head sum, row scale, store
+//               odd tiles (with four queries: both sets every tile, two queries each):
+//               tcgen05.ld, hi + lo, ReLU, weighted head sum, row scale, store
 //   warps 10-11 query preparation: the hi/lo B operand and w/s of each query group, double
 //               buffered across groups
 // fp4 indexer cache (packed e2m1 rows, one fp32 scale a row): warps 0 and 12 bulk-copy a
