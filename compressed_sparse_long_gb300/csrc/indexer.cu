@@ -520,7 +520,10 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
       lo = fminf(lo, fminf(fminf(x[u].x, x[u].y), fminf(x[u].z, x[u].w)));
       const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
       hi = fmaxf(hi, m4);
-      nan |= (x[u].x != x[u].x) | (x[u].y != x[u].y) | (x[u].z != x[u].z) | (x[u].w != x[u].w);
+      // a NaN makes the sum NaN (so can +inf beside -inf: such a row takes the radix passes,
+      // which are exact for it too)
+      const float sum4 = (x[u].x + x[u].y) + (x[u].z + x[u].w);
+      nan |= sum4 != sum4;
       top4(m4);   // one entry of each group of four (the copies past n repeat its first)
     }
   }
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
   // row) with warp-aggregated appends, one shared-memory atomic per warp and iteration
   bool have = false;                                // candidates collected (block-uniform)
   if (!nan && fl > -INFINITY) {
-    constexpr int kU2 = 4;                          // (fewer live registers than kUnroll)
+    constexpr int kU2 = 8;                          // 16-byte loads in flight per thread
     for (int64_t i0 = (int64_t)tid * 4; i0 - (int64_t)lane * 4 < n; i0 += kStep * kU2) {
       float4 x[kU2];
 #pragma unroll
@@ -572,11 +575,17 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
       uint32_t cnt = 0;
+      if (i0 + (kU2 - 1) * kStep + 3 < n) {         // every group of this iteration is whole
 #pragma unroll
-      for (int u = 0; u < kU2; ++u) {
-        const int64_t i = i0 + u * kStep;
-        cnt += (i < n && x[u].x >= fl) + (i + 1 < n && x[u].y >= fl) + (i + 2 < n && x[u].z >= fl) +
-               (i + 3 < n && x[u].w >= fl);
+        for (int u = 0; u < kU2; ++u)
+          cnt += (x[u].x >= fl) + (x[u].y >= fl) + (x[u].z >= fl) + (x[u].w >= fl);
+      } else {                                      // (groups past n were loaded as -inf)
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+          const int64_t i = i0 + u * kStep;
+          cnt += (i < n && x[u].x >= fl) + (i + 1 < n && x[u].y >= fl) + (i + 2 < n && x[u].z >= fl) +
+                 (i + 3 < n && x[u].w >= fl);
+        }
       }
       uint32_t incl = cnt;
 #pragma unroll
