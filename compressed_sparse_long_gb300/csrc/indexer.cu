@@ -354,12 +354,12 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const __grid_const
 // smallest-index ties equal to it) are placed by their index rank. A row with non-finite or
 // constant scores, or too many collected entries, takes radix passes over the whole row
 // instead (four histogram passes, then an ordered compaction of per-thread chunks).
-constexpr int kStreamThreads = 256;
-constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamMaxThreads = 1024;
 constexpr int kStreamBuckets = 2048;
 constexpr int kStreamCap = 2048;
 
-// Exclusive block-wide sum of one value per thread; the total through *total.
+// Exclusive block-wide sum of one value per thread (WARPS warps); the total through *total.
+template <int WARPS>
 __device__ __forceinline__ uint32_t stream_excl_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
@@ -372,7 +372,7 @@ __device__ __forceinline__ uint32_t stream_excl_sum(uint32_t v, uint32_t* warp_t
   __syncthreads();
   uint32_t before = 0, all = 0;
 #pragma unroll
-  for (int w = 0; w < kStreamWarps; ++w) {
+  for (int w = 0; w < WARPS; ++w) {
     const uint32_t t = warp_tot[w];
     before += w < warp ? t : 0u;
     all += t;
@@ -414,7 +414,11 @@ __device__ __forceinline__ void top_digit(const uint32_t* h, uint32_t need, uint
   }
 }
 
-__global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __grid_constant__ IndexParams p) {
+template <int kStreamThreads>
+__global__ void __launch_bounds__(kStreamThreads, 1024 / kStreamThreads)
+    topk_stream_kernel(const __grid_constant__ IndexParams p) {
+  constexpr int kStreamWarps = kStreamThreads / 32;
+  constexpr int kBpt = kStreamBuckets / kStreamThreads;   // histogram buckets a thread scans
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bh[kStreamBuckets];           // bucket histogram; radix histograms after
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     }
   }
   float fl = -INFINITY;
-  if (k <= 4u * kStreamThreads) {
+  if (k <= 4u * kStreamThreads && k <= (uint32_t)kStreamCap) {
     const uint32_t need_w = (k + kStreamWarps - 1) / kStreamWarps;
     const uint32_t u0 = order_key(t0), u1 = order_key(t1), u2 = order_key(t2), u3 = order_key(t3);
     uint32_t T = 0;                                 // bitwise search from the top bit
@@ -628,21 +632,21 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     // ---- pass 2: histogram
     for_each4([&](int64_t, float x) { atomicAdd(&bh[bucket(x)], 1u); });
     __syncthreads();
-    // boundary bucket: thread t owns buckets 2047-8t-7 .. 2047-8t, from the top
+    // boundary bucket: thread t owns the kBpt buckets below 2047 - kBpt t, from the top
     {
-      uint32_t c[8], sum = 0;
+      uint32_t c[kBpt], sum = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = bh[kStreamBuckets - 1 - 8 * tid - j];
+      for (int j = 0; j < kBpt; ++j) {
+        c[j] = bh[kStreamBuckets - 1 - kBpt * tid - j];
         sum += c[j];
       }
-      const uint32_t before = stream_excl_sum(sum, warp_tot, nullptr);
+      const uint32_t before = stream_excl_sum<kStreamWarps>(sum, warp_tot, nullptr);
       if (before < k && before + sum >= k) {
         uint32_t cum = before;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kBpt; ++j) {
           if (cum + c[j] >= k) {
-            s_bucket = (uint32_t)(kStreamBuckets - 1 - 8 * tid - j);
+            s_bucket = (uint32_t)(kStreamBuckets - 1 - kBpt * tid - j);
             s_above = cum;
             break;
           }
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     // tie needs its index rank
     uint32_t n_tie = 0;
     for (int c = tid; c < nc; c += kStreamThreads) n_tie += (cin[c] && ckey[c] == kth) ? 1u : 0u;
-    stream_excl_sum(n_tie, warp_tot, &s_total);
+    stream_excl_sum<kStreamWarps>(n_tie, warp_tot, &s_total);
     const bool all_ties = s_total <= remaining;
     // ---- selection: contiguous chunks of the collected entries, one block scan
     const int per = (nc + kStreamThreads - 1) / kStreamThreads;
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     };
     uint32_t cnt = 0;
     for (int c = c0; c < c1; ++c) cnt += selected(c) ? 1u : 0u;
-    uint32_t at = stream_excl_sum(cnt, warp_tot, &s_total);
+    uint32_t at = stream_excl_sum<kStreamWarps>(cnt, warp_tot, &s_total);
     for (int c = c0; c < c1; ++c)
       if (selected(c)) sel[at++] = cidx[c];
     __syncthreads();
@@ -742,12 +746,16 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     // to a power of two with INT32_MAX
     const int ns = (int)s_total;   // == k
     if (ns <= 2 * kStreamThreads) {
-      // 512 slots, thread t holding slots 2t and 2t + 1 in registers: strides below 64 pair
+      // n2 = the power of two >= ns (at least 64) slots, thread t < n2 / 2 holding slots 2t
+      // and 2t + 1 in registers (the others only pass the barriers): strides below 64 pair
       // threads of one warp (shuffles), the longer ones exchange through shared memory.
-      int32_t a0 = 2 * tid < ns ? sel[2 * tid] : INT32_MAX;
-      int32_t a1 = 2 * tid + 1 < ns ? sel[2 * tid + 1] : INT32_MAX;
+      int n2 = 64;
+      while (n2 < ns) n2 <<= 1;
+      const bool act = 2 * tid < n2;                // warp-uniform (n2 >= 64)
+      int32_t a0 = act && 2 * tid < ns ? sel[2 * tid] : INT32_MAX;
+      int32_t a1 = act && 2 * tid + 1 < ns ? sel[2 * tid + 1] : INT32_MAX;
 #pragma unroll 1
-      for (int size = 2; size <= 2 * kStreamThreads; size <<= 1) {
+      for (int size = 2; size <= n2; size <<= 1) {
         const bool asc = ((2 * tid) & size) == 0;
 #pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -758,25 +766,31 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
             continue;
           }
           const int tp = stride >> 1;                 // partner thread: tid ^ tp
-          int32_t w0, w1;
+          int32_t w0 = a0, w1 = a1;
           if (tp < 32) {
-            w0 = __shfl_xor_sync(0xffffffffu, a0, tp);
-            w1 = __shfl_xor_sync(0xffffffffu, a1, tp);
+            if (act) {
+              w0 = __shfl_xor_sync(0xffffffffu, a0, tp);
+              w1 = __shfl_xor_sync(0xffffffffu, a1, tp);
+            }
           } else {
             __syncthreads();                          // the previous exchange was read
-            sel[2 * tid] = a0;
-            sel[2 * tid + 1] = a1;
+            if (act) {
+              sel[2 * tid] = a0;
+              sel[2 * tid + 1] = a1;
+            }
             __syncthreads();
-            w0 = sel[(2 * tid) ^ stride];
-            w1 = sel[(2 * tid + 1) ^ stride];
+            if (act) {
+              w0 = sel[(2 * tid) ^ stride];
+              w1 = sel[(2 * tid + 1) ^ stride];
+            }
           }
           const bool lower = (tid & tp) == 0;         // this thread's slots are the pairs' lower
           a0 = lower == asc ? min(a0, w0) : max(a0, w0);
           a1 = lower == asc ? min(a1, w1) : max(a1, w1);
         }
       }
-      if (2 * tid < ns) out[2 * tid] = a0;
-      if (2 * tid + 1 < ns) out[2 * tid + 1] = a1;
+      if (act && 2 * tid < ns) out[2 * tid] = a0;
+      if (act && 2 * tid + 1 < ns) out[2 * tid + 1] = a1;
       return;
     }
     int np2 = 1;
@@ -830,8 +844,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(const __
     n_gt += u > kth;
     n_eq += u == kth;
   }
-  const uint32_t ex_gt = stream_excl_sum(n_gt, warp_tot, nullptr);
-  const uint32_t ex_eq = stream_excl_sum(n_eq, warp_tot, nullptr);
+  const uint32_t ex_gt = stream_excl_sum<kStreamWarps>(n_gt, warp_tot, nullptr);
+  const uint32_t ex_eq = stream_excl_sum<kStreamWarps>(n_eq, warp_tot, nullptr);
   uint32_t at = ex_gt + min(ex_eq, remaining);
   uint32_t tie = ex_eq;
   for (int64_t i = r0; i < r1; ++i) {
@@ -872,8 +886,15 @@ int launch_topk(const IndexParams& p, int64_t max_vis, cudaStream_t st) {
   cudaError_t e;
   if (max_vis <= 8 * 1024)   // decode-sized rows: register-resident, one CTA of 1024 threads a row
     e = launch_pdl(topk_reg_kernel<8, 1024>, dim3(p.n_q), dim3(1024), 0, st, p);
-  else                       // longer rows: streaming passes, 256 threads a row
-    e = launch_pdl(topk_stream_kernel, dim3(p.n_q), dim3(kStreamThreads), 0, st, p);
+  else {                     // longer rows: streaming passes, 256 threads a row (four rows an
+    int dev = 0, sms = 152;    // SM), or 1024 when the call has too few rows to fill the SMs
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (p.n_q <= 2 * (int64_t)sms)
+      e = launch_pdl(topk_stream_kernel<kStreamMaxThreads>, dim3(p.n_q), dim3(kStreamMaxThreads), 0, st, p);
+    else
+      e = launch_pdl(topk_stream_kernel<256>, dim3(p.n_q), dim3(256), 0, st, p);
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

@@ -312,10 +312,10 @@ def test_index_topk_prefill_positions(n_q, k):
 
 @pytest.mark.parametrize("k", [64, 512, 1024, 1025, 2048])
 def test_index_topk_streaming_rows(k):
-    """Rows longer than the register-resident selection holds (up to 16,383 entries): the
-    streaming selection with its candidate floor (k <= 1024, each warp's ceil(k / 8)-th
-    largest candidate; 1024 takes every candidate) and without it (k > 1024, the bucket
-    histogram), against the oracle's lists; one row is shorter than k."""
+    """Rows longer than the register-resident selection holds (up to 16,383 entries), five
+    rows (1024 threads a row): the streaming selection with its candidate floor (each warp's
+    ceil(k / 32)-th largest candidate; k <= 2048) against the oracle's lists; one row is
+    shorter than k."""
     w = wl.c4a_prefill(seed=61, cached=65536, chunk=5)
     h = w.layers[0]
     q = w.queries
@@ -327,6 +327,24 @@ def test_index_topk_streaming_rows(k):
     ref, scores = O.index_topk(h.spec, pools, q.seq, q.pos, q.q_idx, q.w, k)
     same = check_topk(topk.cpu().numpy(), ref, scores, k)
     assert len(same) >= len(q.pos) - 1
+
+
+def test_index_topk_streaming_many_rows():
+    """A call with more rows (320) than two per SM, each longer than the register-resident
+    selection holds: the streaming selection with 256 threads a row (calls with fewer rows
+    use 1024); sampled rows against the oracle's lists."""
+    w = wl.c4a_prefill(seed=62, cached=40000, chunk=320)
+    h = w.layers[0]
+    q = w.queries
+    q.pos = np.linspace(33000, 40000, 320).astype(np.int64)
+    lay, x = device_layer(h), DevInputs(w)
+    assert O.visible_entries(h.spec.S, h.spec.W, h.spec.win_off, 33000) > 8192
+    topk = lay.index_topk(x.q_seq, x.q_pos, int(q.pos.max()), x.q_idx, x.w).cpu().numpy()
+    sample = np.array([0, 1, 77, 150, 151, 200, 318, 319])
+    ref, scores = O.index_topk(h.spec, oracle_pools(h), q.seq[sample], q.pos[sample],
+                               q.q_idx[sample], q.w[sample], 512)
+    same = check_topk(topk[sample], ref, scores, 512)
+    assert len(same) >= len(sample) - 1
 
 
 @pytest.mark.parametrize("L", [4096, 65536])
