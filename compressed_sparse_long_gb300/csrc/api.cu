@@ -10,7 +10,7 @@ using namespace v4a;
 
 namespace {
 
-constexpr int32_t kVersion = 20;
+constexpr int32_t kVersion = 21;
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
