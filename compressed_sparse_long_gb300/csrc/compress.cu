@@ -267,9 +267,123 @@ struct CompressKernel {
     }
   }
 
+  // Long windows (c128a: 128 tokens), attention entry only: the kWideWarps warps of the
+  // token's block each take a contiguous quarter of the window. The same two passes as
+  // window_sum (the window's max first, then the exponentials against it), with the max and
+  // the partial sums exchanged through shared memory and the partial sums added in warp
+  // order; every warp returns the same decision, warp 0 the sums.
+  static constexpr int kWideWarps = 4;
+  struct WideSmem {
+    float m[kWideWarps][CPL][32];
+    float l[kWideWarps][CPL][32];
+    float a[kWideWarps][CPL][32];
+  };
+  template <class Fetch>
+  static __device__ __forceinline__ bool window_sum_wide(const CompressParams& p, int lane, int w,
+                                                         const Fetch& fetch, float (&c)[CPL], WideSmem& sm) {
+    constexpr int N = CPL;
+    for (int o = 0; o < p.W; ++o) {                // a missing row stops every warp
+      WindowRow r;
+      const int st = fetch(o, r);
+      if (st < 0) {
+        if (w == 0) raise_err(p.err, st == -2 ? V4A_DEV_BAD_PAGE : V4A_DEV_MISSING_PAGE);
+        return false;
+      }
+    }
+    const int per = (p.W + kWideWarps - 1) / kWideWarps;
+    const int o0 = w * per, o1 = min(p.W, o0 + per);
+    float m[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) m[k] = -INFINITY;
+#pragma unroll 8
+    for (int o = o0; o < o1; ++o) {
+      WindowRow r;
+      if (fetch(o, r) == 0) continue;
+      float sv[N], bv[N];
+      load_g<TIn, N>(r.s + lane * N, sv);
+      load_f<float, N>(p.bias + (int64_t)o * D + lane * N, bv);
+#pragma unroll
+      for (int k = 0; k < N; ++k) m[k] = fmaxf(m[k], (sv[k] + bv[k]) * kLog2e);
+    }
+#pragma unroll
+    for (int k = 0; k < N; ++k) sm.m[w][k][lane] = m[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      float mx = sm.m[0][k][lane];
+#pragma unroll
+      for (int v = 1; v < kWideWarps; ++v) mx = fmaxf(mx, sm.m[v][k][lane]);
+      m[k] = mx;
+    }
+    float l[N], acc[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) { l[k] = 0.f; acc[k] = 0.f; }
+#pragma unroll 8
+    for (int o = o0; o < o1; ++o) {
+      WindowRow r;
+      if (fetch(o, r) <= 0) continue;
+      float sv[N], bv[N], xv[N];
+      load_g<TIn, N>(r.s + lane * N, sv);
+      load_g<TIn, N>(r.kv + lane * N, xv);
+      load_f<float, N>(p.bias + (int64_t)o * D + lane * N, bv);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float e = exp2_approx((sv[k] + bv[k]) * kLog2e - m[k]);
+        l[k] += e;
+        acc[k] = fmaf(e, xv[k], acc[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      sm.l[w][k][lane] = l[k];
+      sm.a[w][k][lane] = acc[k];
+    }
+    __syncthreads();
+    if (w == 0) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        float lt = sm.l[0][k][lane], at = sm.a[0][k][lane];
+#pragma unroll
+        for (int v = 1; v < kWideWarps; ++v) {
+          lt += sm.l[v][k][lane];
+          at += sm.a[v][k][lane];
+        }
+        c[k] = __fdividef(at, lt);   // lt >= 1: the window's largest weight is 2^0
+      }
+    }
+    return true;
+  }
+
+  // build_entry for a long window and no indexer row, the whole block taking part
+  template <class Fetch>
+  static __device__ void build_entry_wide(const CompressParams& p, int b, int64_t j, int lane, int w,
+                                          const Fetch& fetch) {
+    __shared__ WideSmem sm;
+    const int64_t e_slot = slot_of(p.attn, b, j);
+    if (e_slot == -2 && w == 0) raise_err(p.err, V4A_DEV_BAD_PAGE);
+    if (e_slot < 0) return;
+    float c[CPL], g[CPL];
+    if (!window_sum_wide(p, lane, w, fetch, c, sm)) return;
+    if (w != 0) return;
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) ss = fmaf(c[k], c[k], ss);
+    ss = warp_sum(ss);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)D) + p.eps));
+    load_f<float, CPL>(p.gamma + lane * CPL, g);
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) c[k] = c[k] * inv * g[k];
+    rope_lane<CPL>(p.rope, c, lane, j * p.S);
+    store_row<CPL>(p.attn, e_slot, c, lane);
+  }
+
+  // kWide: blocks of kWideWarps warps, one token each (warp 0 writes its rows, all warps
+  // build an entry its window completes); otherwise one warp per token or query row.
+  template <bool kWide>
   static __device__ void run(const CompressParams& p) {
     const int lane = threadIdx.x & 31;
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int wb = kWide ? (int)(threadIdx.x >> 5) : 0;   // warp of the token's block
+    const int64_t i = kWide ? (int64_t)blockIdx.x : ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     // static warp dispatch: warps [0, n_tokens) insert tokens, the next n_qrows warps
     // normalise query head rows; no warp depends on another
     if (i >= p.n_tokens) {
@@ -322,7 +436,7 @@ struct CompressKernel {
     pdl_wait();
 
     // (1) sliding-window row: RoPE(kv_t, t)
-    {
+    if (wb == 0) {
       const int64_t s = swa_slot;
       if (s >= 0) {
         float y[CPL];
@@ -336,7 +450,7 @@ struct CompressKernel {
     }
 
     // (2) raw residual row for the last W new positions
-    if (keep_state) {
+    if (keep_state && wb == 0) {
       const int64_t s = state_slot;
       if (s >= 0) {
         TIn* dst = reinterpret_cast<TIn*>(p.state.data) + s * (int64_t)p.state.width;
@@ -365,7 +479,7 @@ struct CompressKernel {
     // row, < 0 a residual row without a usable page; ref = input row or pool row
     __shared__ int64_t s_ref[kMaxWindow];
     __shared__ int8_t s_st[kMaxWindow];
-    for (int o = lane; o < p.W; o += 32) {
+    for (int o = (int)threadIdx.x; o < p.W; o += (int)blockDim.x) {
       const int64_t pos = j * p.S + p.win_off + o;
       int st = 0;
       int64_t ref = 0;
@@ -379,8 +493,9 @@ struct CompressKernel {
       s_st[o] = (int8_t)st;
       s_ref[o] = ref;
     }
-    __syncwarp();
-    build_entry(p, b, j, lane, [&](int o, WindowRow& w) -> int {
+    if constexpr (kWide) __syncthreads();
+    else __syncwarp();
+    auto fetch = [&](int o, WindowRow& w) -> int {
       const int st = s_st[o];
       if (st <= 0) return st;                      // absent, or -1 / -2 (page errors)
       const int64_t ref = s_ref[o];
@@ -401,7 +516,9 @@ struct CompressKernel {
         }
       }
       return 1;
-    });
+    };
+    if constexpr (kWide) build_entry_wide(p, b, j, lane, wb, fetch);
+    else build_entry(p, b, j, lane, fetch);
   }
 };
 
@@ -686,10 +803,10 @@ __global__ void __launch_bounds__(512, 1) compress_tile_kernel(const __grid_cons
   CompressTile<TIn, CPL, ICPL, kFp8>::run(p);
 }
 
-template <typename TIn, int CPL, int ICPL, bool kFp8>
+template <typename TIn, int CPL, int ICPL, bool kFp8, bool kWide>
 __global__ void __launch_bounds__(256) compress_insert_kernel(const __grid_constant__ CompressParams p) {
   pdl_trigger();   // the kernel waits (pdl_wait) after loading its inputs
-  CompressKernel<TIn, CPL, ICPL, kFp8>::run(p);
+  CompressKernel<TIn, CPL, ICPL, kFp8>::template run<kWide>(p);
 }
 
 template <typename TIn, int CPL, int ICPL, bool kFp8>
@@ -716,9 +833,19 @@ cudaError_t launch(const CompressParams& p, cudaStream_t st) {
   // One warp per block (the c4a bf16 kernel compiles to 128 registers a thread): such a
   // block fits on an SM beside a persistent indexer CTA, so a small insert never holds
   // an SM the indexer is waiting for.
+  // Windows longer than a warp (c128a) and no indexer rows or query rows: blocks of four
+  // warps, one token each, so that an entry's 128-token window is summed by four warps.
+  if constexpr (ICPL == 0) {
+    using K = CompressKernel<TIn, CPL, ICPL, kFp8>;
+    if (p.W > 32 && p.n_qrows == 0) {
+      const cudaError_t e = launch_pdl(compress_insert_kernel<TIn, CPL, ICPL, kFp8, true>, dim3((unsigned)p.n_tokens),
+                                       dim3(32 * K::kWideWarps), 0, st, p);
+      return e != cudaSuccess ? e : cudaGetLastError();
+    }
+  }
   const int threads = 32;
   const int64_t blocks = p.n_tokens + p.n_qrows;
-  const cudaError_t e = launch_pdl(compress_insert_kernel<TIn, CPL, ICPL, kFp8>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
+  const cudaError_t e = launch_pdl(compress_insert_kernel<TIn, CPL, ICPL, kFp8, false>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
